@@ -1,0 +1,227 @@
+// C-ABI entry points of libstreamkl: argument validation, TMA tensor maps,
+// launches.  Every check that can fail does so before anything is enqueued.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "kernels.cuh"
+#include "streamkl.h"
+
+namespace {
+
+// The device status word that kernels set when they give up a wait.
+__device__ int g_status;
+
+int* status_ptr() {
+  int* p = nullptr;
+  if (cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_status) != cudaSuccess) return nullptr;
+  return p;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// [BH][N][d] bf16 viewed as a 3-D tensor; boxes of 64 elements x 128 rows x 1,
+// 128-byte swizzle.  Rows past N read as zeros.
+bool make_map(CUtensorMap* m, const void* ptr, long long BH, long long N, int d) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[3] = {cuuint64_t(d), cuuint64_t(N), cuuint64_t(BH)};
+  cuuint64_t strides[2] = {cuuint64_t(d) * 2, cuuint64_t(N) * d * 2};
+  cuuint32_t box[3] = {64, cuuint32_t(skl::kTile), 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+                  es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool head_dim_ok(int d) { return d == 64 || d == 128; }
+
+// Shared validation of the problem description.  Returns STREAMKL_OK, or the
+// status to report.  Sets *empty when there is no row to compute.
+int check_problem(const void* q1, const void* k1, const void* q2, const void* k2, int B, int H,
+                  int NQ, int NK, int d1, int d2, float scale, int causal, bool* empty) {
+  *empty = false;
+  if (B < 0 || H < 0 || NQ < 0 || NK < 0) return STREAMKL_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f) || scale > 1.0e4f) return STREAMKL_INVALID_ARG;
+  if (causal != 0 && causal != 1) return STREAMKL_INVALID_ARG;
+  if (!head_dim_ok(d1) || !head_dim_ok(d2)) return STREAMKL_UNSUPPORTED;
+  if (causal && NQ > NK) return STREAMKL_INVALID_ARG;
+  const long long BH = (long long)B * H;
+  if (BH == 0 || NQ == 0) {
+    *empty = true;
+    return STREAMKL_OK;
+  }
+  if (NK == 0) return STREAMKL_INVALID_ARG;
+  // grid.y carries B*H; per-row indices must stay in int range
+  if (BH > 65535 || BH * (long long)(NQ > NK ? NQ : NK) > (1ll << 31) - 1) return STREAMKL_INVALID_ARG;
+  if (!q1 || !k1 || !q2 || !k2) return STREAMKL_INVALID_ARG;
+  if (!aligned16(q1) || !aligned16(k1) || !aligned16(q2) || !aligned16(k2)) return STREAMKL_INVALID_ARG;
+  return STREAMKL_OK;
+}
+
+int device_ok() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return STREAMKL_CUDA_ERROR;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return STREAMKL_CUDA_ERROR;
+  if (major != 10 || minor != 3) return STREAMKL_UNSUPPORTED;  // built for sm_103a only
+  return STREAMKL_OK;
+}
+
+int make_maps(skl::TMaps* m, const void* q1, const void* k1, const void* q2, const void* k2, int BH,
+              int NQ, int NK, int d1, int d2) {
+  if (!make_map(&m->q1, q1, BH, NQ, d1) || !make_map(&m->k1, k1, BH, NK, d1) ||
+      !make_map(&m->q2, q2, BH, NQ, d2) || !make_map(&m->k2, k2, BH, NK, d2))
+    return STREAMKL_CUDA_ERROR;
+  return STREAMKL_OK;
+}
+
+int as_status(int cuda_err) { return cuda_err == 0 ? STREAMKL_OK : STREAMKL_CUDA_ERROR; }
+
+}  // namespace
+
+extern "C" {
+
+int streamkl_fwd(const void* q1, const void* k1, const void* q2, const void* k2, int B, int H,
+                 int NQ, int NK, int d1, int d2, float scale, int causal, float* kl, float* lse1,
+                 float* lse2, streamkl_stream_t stream) {
+  bool empty = false;
+  int s = check_problem(q1, k1, q2, k2, B, H, NQ, NK, d1, d2, scale, causal, &empty);
+  if (s != STREAMKL_OK || empty) return s;
+  if (!kl || !lse1 || !lse2 || !aligned16(kl) || !aligned16(lse1) || !aligned16(lse2))
+    return STREAMKL_INVALID_ARG;
+  if ((s = device_ok()) != STREAMKL_OK) return s;
+  skl::TMaps m;
+  if ((s = make_maps(&m, q1, k1, q2, k2, B * H, NQ, NK, d1, d2)) != STREAMKL_OK) return s;
+  int* st = status_ptr();
+  if (!st) return STREAMKL_CUDA_ERROR;
+  skl::FwdArgs a{B * H, NQ, NK, causal, 1, scale, kl, lse1, lse2, nullptr, st};
+  return as_status(skl::launch_fwd(m, d1, d2, a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t streamkl_fwd_splitk_workspace_bytes(int B, int H, int NQ, int num_splits) {
+  if (B < 0 || H < 0 || NQ < 0 || num_splits < 1 || num_splits > 1024) return 0;
+  return size_t(5) * 4 * size_t(num_splits) * size_t(B) * size_t(H) * size_t(NQ);
+}
+
+int streamkl_fwd_splitk(const void* q1, const void* k1, const void* q2, const void* k2, int B, int H,
+                        int NQ, int NK, int d1, int d2, float scale, int causal, int num_splits,
+                        void* workspace, size_t workspace_bytes, float* kl, float* lse1, float* lse2,
+                        streamkl_stream_t stream) {
+  bool empty = false;
+  int s = check_problem(q1, k1, q2, k2, B, H, NQ, NK, d1, d2, scale, causal, &empty);
+  if (s != STREAMKL_OK) return s;
+  if (num_splits < 1 || num_splits > 1024) return STREAMKL_INVALID_ARG;
+  if (empty) return STREAMKL_OK;
+  if (!kl || !lse1 || !lse2 || !aligned16(kl) || !aligned16(lse1) || !aligned16(lse2))
+    return STREAMKL_INVALID_ARG;
+  const size_t need = streamkl_fwd_splitk_workspace_bytes(B, H, NQ, num_splits);
+  if (!workspace || !aligned16(workspace) || workspace_bytes < need) return STREAMKL_INVALID_ARG;
+  if ((s = device_ok()) != STREAMKL_OK) return s;
+  skl::TMaps m;
+  if ((s = make_maps(&m, q1, k1, q2, k2, B * H, NQ, NK, d1, d2)) != STREAMKL_OK) return s;
+  int* st = status_ptr();
+  if (!st) return STREAMKL_CUDA_ERROR;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  float* part = static_cast<float*>(workspace);
+  skl::FwdArgs a{B * H, NQ, NK, causal, num_splits, scale, kl, lse1, lse2, part, st};
+  int e = skl::launch_fwd(m, d1, d2, a, cs);
+  if (e != 0) return STREAMKL_CUDA_ERROR;
+  return as_status(skl::launch_splitk_reduce(part, B * H * NQ, num_splits, kl, lse1, lse2, cs));
+}
+
+int streamkl_suggest_splits(int B, int H, int NQ, int NK, int causal) {
+  if (B <= 0 || H <= 0 || NQ <= 0 || NK <= 0 || (causal && NQ > NK)) return 0;
+  int dev = 0, sms = 152;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long ctas = (long long)B * H * ((NQ + skl::kTile - 1) / skl::kTile);
+  const int max_kt = (NK + skl::kTile - 1) / skl::kTile;
+  int s = 1;
+  // at least two full waves of one CTA per SM, and at least 8 key tiles per split
+  while (ctas * s < 2ll * sms && s * 2 <= max_kt / 8 && s < 1024) s *= 2;
+  return s;
+}
+
+int streamkl_bwd(const void* q1, const void* k1, const void* q2, const void* k2, int B, int H,
+                 int NQ, int NK, int d1, int d2, float scale, int causal, const float* kl,
+                 const float* lse1, const float* lse2, const float* dkl, int mode, int deterministic,
+                 float* dq, float* dk, streamkl_stream_t stream) {
+  bool empty = false;
+  int s = check_problem(q1, k1, q2, k2, B, H, NQ, NK, d1, d2, scale, causal, &empty);
+  if (s != STREAMKL_OK) return s;
+  if (mode != STREAMKL_GRAD_P2 && mode != STREAMKL_GRAD_P1) return STREAMKL_INVALID_ARG;
+  if (deterministic != 0 && deterministic != 1) return STREAMKL_INVALID_ARG;
+  const int dg = mode == STREAMKL_GRAD_P2 ? d2 : d1;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (empty) {
+    // no query rows: dK is zero (dq is empty)
+    const size_t bytes = size_t(B) * H * NK * dg * 4;
+    if (bytes == 0) return STREAMKL_OK;
+    if (!dk || !aligned16(dk)) return STREAMKL_INVALID_ARG;
+    return as_status(cudaMemsetAsync(dk, 0, bytes, cs));
+  }
+  if (!kl || !lse1 || !lse2 || !dkl || !dq || !dk) return STREAMKL_INVALID_ARG;
+  if (!aligned16(kl) || !aligned16(lse1) || !aligned16(lse2) || !aligned16(dkl) || !aligned16(dq) ||
+      !aligned16(dk))
+    return STREAMKL_INVALID_ARG;
+  if ((s = device_ok()) != STREAMKL_OK) return s;
+  skl::TMaps m;
+  if ((s = make_maps(&m, q1, k1, q2, k2, B * H, NQ, NK, d1, d2)) != STREAMKL_OK) return s;
+  int* st = status_ptr();
+  if (!st) return STREAMKL_CUDA_ERROR;
+  skl::BwdArgs a{B * H, NQ, NK, causal, mode, scale, kl, lse1, lse2, dkl, dq, dk, st, 1};
+  if (!deterministic) {
+    const size_t dq_bytes = size_t(B) * H * NQ * dg * 4;
+    if (cudaMemsetAsync(dq, 0, dq_bytes, cs) != cudaSuccess) return STREAMKL_CUDA_ERROR;
+    return as_status(skl::launch_bwd_fused(m, d1, d2, a, cs));
+  }
+  a.write_dq = 0;
+  int e = skl::launch_bwd_fused(m, d1, d2, a, cs);
+  if (e != 0) return STREAMKL_CUDA_ERROR;
+  return as_status(skl::launch_bwd_dq(m, d1, d2, a, cs));
+}
+
+const char* streamkl_status_string(int status) {
+  switch (status) {
+    case STREAMKL_OK: return "ok";
+    case STREAMKL_INVALID_ARG: return "invalid argument";
+    case STREAMKL_UNSUPPORTED: return "unsupported head dimension or device";
+    case STREAMKL_CUDA_ERROR: return "CUDA error";
+    case STREAMKL_DEVICE_TIMEOUT: return "a kernel abandoned a wait (device timeout)";
+    default: return "unknown status";
+  }
+}
+
+int streamkl_get_device_status(void) {
+  int v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status, sizeof(int)) != cudaSuccess) return STREAMKL_CUDA_ERROR;
+  if (cudaMemcpyToSymbol(g_status, &zero, sizeof(int)) != cudaSuccess) return STREAMKL_CUDA_ERROR;
+  return v;
+}
+
+int streamkl_probe_ex2(float* out, int blocks, int iters, streamkl_stream_t stream) {
+  if (!out || blocks < 1 || iters < 1 || blocks > (1 << 20)) return STREAMKL_INVALID_ARG;
+  return as_status(skl::launch_ex2_probe(out, blocks, iters, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

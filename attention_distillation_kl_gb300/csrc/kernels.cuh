@@ -1,0 +1,47 @@
+// Host-side launchers shared between the translation units of libstreamkl.
+#pragma once
+
+#include <cstddef>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace skl {
+
+constexpr int kTile = 128;  // query and key tile: 128 rows = 128 TMEM lanes
+
+struct TMaps {
+  CUtensorMap q1, k1, q2, k2;  // [BH][N][d] bf16, boxes of 64 x 128, 128-byte swizzle
+};
+
+struct FwdArgs {
+  int BH, NQ, NK, causal, num_splits;
+  float scale;
+  float* kl;
+  float* lse1;
+  float* lse2;
+  float* partial;  // key-split partials [num_splits][5][BH*NQ], or null
+  int* status;
+};
+
+struct BwdArgs {
+  int BH, NQ, NK, causal, mode;
+  float scale;
+  const float* kl;
+  const float* lse1;
+  const float* lse2;
+  const float* dkl;
+  float* dq;  // fp32 [BH][NQ][dg]
+  float* dk;  // fp32 [BH][NK][dg]
+  int* status;
+  int write_dq;  // 0: skip the dQ product (deterministic two-pass uses its own dQ kernel)
+};
+
+// Each returns a cudaError_t value (cudaSuccess = 0).
+int launch_fwd(const TMaps& m, int d1, int d2, const FwdArgs& a, cudaStream_t st);
+int launch_splitk_reduce(const float* partial, int rows, int num_splits, float* kl, float* lse1,
+                         float* lse2, cudaStream_t st);
+int launch_bwd_fused(const TMaps& m, int d1, int d2, const BwdArgs& a, cudaStream_t st);
+int launch_bwd_dq(const TMaps& m, int d1, int d2, const BwdArgs& a, cudaStream_t st);
+int launch_ex2_probe(float* out, int blocks, int iters, cudaStream_t st);
+
+}  // namespace skl

@@ -1,0 +1,145 @@
+/*
+ * libstreamkl -- fused attention KL divergence on GB300 (sm_103a).
+ *
+ * For every query row i it computes KL(P1_i || P2_i) with
+ *   P1 = softmax(s * Q1 K1^T), P2 = softmax(s * Q2 K2^T)
+ * over the visible keys (optionally causal), plus LSE1_i and LSE2_i, without
+ * materialising either N_Q x N_K matrix, and the gradient of
+ * L = sum_i dKL_i * KL_i with respect to one side's Q and K.
+ *
+ * Sources: StreamKL article on agidaily.cc, sections "Online formula"
+ * (L = acc/l1 + LSE2 - LSE1 with a B_Q-vector rescale of acc), "Forward"
+ * (one streaming pass, outputs KL, LSE1, LSE2 only), "Backward" (tile-by-tile
+ * recompute of P from the saved LSEs; modes "optimise P2" and "optimise P1"
+ * with a numerically stable log-ratio) and "GPU kernel engineering" (key
+ * split with a light reduce, fused dQ/dK backward with atomics); and the
+ * abstract of "StreamKL: Fast and Memory-Efficient KL Divergence for Boosting
+ * Attention Distillation" (arXiv 2606.20005).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Layout: q1 [B, H, NQ, d1], k1 [B, H, NK, d1], q2 [B, H, NQ, d2],
+ *   k2 [B, H, NK, d2], bf16, row-major and contiguous (BHSD).  Per-row
+ *   vectors (kl, lse1, lse2, dkl) are fp32 [B, H, NQ], contiguous.
+ * Pointers: all tensor pointers are DEVICE pointers on the current device,
+ *   16-byte aligned.  The caller owns every buffer (inputs, outputs and the
+ *   key-split workspace); the library never allocates, frees or synchronises
+ *   and keeps no state between calls other than the device status word.
+ * Streams: every call is asynchronous and stream-ordered on `stream`
+ *   (a cudaStream_t; NULL = legacy default stream).  Errors detected on the
+ *   host return before anything is enqueued.
+ * Scale: 0 < scale <= 1e4 and finite; S = scale * Q K^T on both sides.
+ * Causal: key j is visible to query i iff j <= i + (NK - NQ) (bottom-right
+ *   aligned; j <= i when NQ == NK).  causal with NQ > NK is INVALID_ARG.
+ * Head dims: d1, d2 in {64, 128}, independently (UNSUPPORTED otherwise).
+ * Empty problems: B*H*NQ == 0 is a no-op that returns OK (the backward then
+ *   zeroes dk); NK == 0 with NQ > 0 is INVALID_ARG (rows without keys).
+ * Return: a streamkl_status value; C++ exceptions never cross this ABI.
+ */
+#ifndef STREAMKL_H
+#define STREAMKL_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t, declared here so users need no CUDA header. */
+typedef struct CUstream_st* streamkl_stream_t;
+
+enum streamkl_status {
+  STREAMKL_OK = 0,
+  STREAMKL_INVALID_ARG = 1,    /* null/misaligned pointer, bad size, causal with NQ > NK, small workspace */
+  STREAMKL_UNSUPPORTED = 2,    /* head dim or device not supported */
+  STREAMKL_CUDA_ERROR = 3,     /* a CUDA runtime/driver call failed (launch, tensor map, attribute) */
+  STREAMKL_DEVICE_TIMEOUT = 4  /* reported by streamkl_get_device_status(): a kernel gave up a wait */
+};
+
+enum streamkl_grad_mode {
+  STREAMKL_GRAD_P2 = 0, /* dS2 = dKL (P2 - P1): gradient into Q2, K2 (head dim d2); standard distillation */
+  STREAMKL_GRAD_P1 = 1  /* dS1 = dKL P1 (log P1 - log P2 - KL): gradient into Q1, K1 (head dim d1) */
+};
+
+/*
+ * Forward: one streaming pass per query tile (article sections "Online
+ * formula" and "Forward").  Writes kl, lse1, lse2 (fp32 [B, H, NQ]; natural
+ * log).  No buffer beyond the inputs and these outputs is touched.
+ */
+int streamkl_fwd(const void* q1, const void* k1, const void* q2, const void* k2,
+                 int B, int H, int NQ, int NK, int d1, int d2, float scale, int causal,
+                 float* kl, float* lse1, float* lse2, streamkl_stream_t stream);
+
+/*
+ * Key-split forward (article section "GPU kernel engineering": split along
+ * the key dimension when B*H*NQ is too small to fill the GPU, write partial
+ * statistics, merge them with a light reduce kernel).  Each of num_splits
+ * partitions of every row's visible key tiles writes (m1, l1, acc, m2, l2)
+ * to `workspace`; a second kernel merges them into kl, lse1, lse2.
+ * workspace: caller-owned device buffer of at least
+ *   streamkl_fwd_splitk_workspace_bytes(B, H, NQ, num_splits) bytes, 16-byte
+ *   aligned; its contents on entry do not matter and are garbage on return.
+ * 1 <= num_splits <= 1024; more splits than key tiles leaves some empty
+ * (they contribute nothing).  Results equal streamkl_fwd's up to rounding.
+ */
+int streamkl_fwd_splitk(const void* q1, const void* k1, const void* q2, const void* k2,
+                        int B, int H, int NQ, int NK, int d1, int d2, float scale, int causal,
+                        int num_splits, void* workspace, size_t workspace_bytes,
+                        float* kl, float* lse1, float* lse2, streamkl_stream_t stream);
+
+/* 5 * 4 * num_splits * B * H * NQ bytes (0 for invalid arguments). */
+size_t streamkl_fwd_splitk_workspace_bytes(int B, int H, int NQ, int num_splits);
+
+/*
+ * Advisory split count for the current device: the smallest number of
+ * splits that gives at least two waves of CTAs, capped by the key tiles of
+ * the longest row.  Returns 1 when no split is needed, 0 on invalid sizes.
+ */
+int streamkl_suggest_splits(int B, int H, int NQ, int NK, int causal);
+
+/*
+ * Backward (article section "Backward"; fused dQ/dK with atomics from
+ * "GPU kernel engineering").  Recomputes P1 = exp(S1 - LSE1) and
+ * P2 = exp(S2 - LSE2) tile by tile from the forward's kl/lse1/lse2 and the
+ * upstream dkl (fp32 [B, H, NQ]), then writes the gradient of
+ * sum_i dkl_i * KL_i for the side `mode` selects:
+ *   STREAMKL_GRAD_P2: dq = dQ2 [B, H, NQ, d2], dk = dK2 [B, H, NK, d2]
+ *   STREAMKL_GRAD_P1: dq = dQ1 [B, H, NQ, d1], dk = dK1 [B, H, NK, d1]
+ * dq and dk are fp32 and fully overwritten.  deterministic = 0: one kernel,
+ * dq accumulated with fp32 atomics after an on-stream memset (summation order
+ * varies run to run).  deterministic = 1: dq and dk from separate passes
+ * without atomics (bitwise reproducible, one extra recompute of S).
+ * kl, lse1, lse2 must come from streamkl_fwd on the same inputs.
+ */
+int streamkl_bwd(const void* q1, const void* k1, const void* q2, const void* k2,
+                 int B, int H, int NQ, int NK, int d1, int d2, float scale, int causal,
+                 const float* kl, const float* lse1, const float* lse2, const float* dkl,
+                 int mode, int deterministic, float* dq, float* dk, streamkl_stream_t stream);
+
+/* Static, NUL-terminated description of a status value. */
+const char* streamkl_status_string(int status);
+
+/*
+ * Reads and clears the current device's status word.  Kernels bound every
+ * wait on an mbarrier (a few seconds); a kernel that gives up sets this word
+ * to STREAMKL_DEVICE_TIMEOUT, releases what it holds and exits, leaving its
+ * outputs undefined.  Synchronous (it waits for the device).  Returns
+ * STREAMKL_OK when no kernel has reported a problem since the last read, or
+ * STREAMKL_CUDA_ERROR if the word cannot be read.
+ */
+int streamkl_get_device_status(void);
+
+/*
+ * Device probe used for the roofline denominator: runs `blocks` CTAs of 256
+ * threads, each thread evaluating `iters` x 8 independent ex2.approx.f32
+ * chains, and writes a checksum to out[0] (device pointer) so the work is
+ * not eliminated.  Time it with events on `stream`; rate = blocks * 256 *
+ * iters * 8 / time.
+ */
+int streamkl_probe_ex2(float* out, int blocks, int iters, streamkl_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* STREAMKL_H */

@@ -1,0 +1,123 @@
+"""The C-ABI library loads, exports every symbol the header declares, and
+rejects bad arguments on the host before touching the device (no GPU needed:
+every call here fails validation before any CUDA call)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import attention_distillation_kl_gb300 as skl
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "streamkl.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not os.path.exists(skl.library_path):
+        import __graft_entry__
+        __graft_entry__.build()
+    return skl.lib()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:int|size_t|const char\*)\s+(streamkl_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_entry_points():
+    syms = declared_symbols()
+    for want in ("streamkl_fwd", "streamkl_fwd_splitk", "streamkl_bwd",
+                 "streamkl_fwd_splitk_workspace_bytes", "streamkl_suggest_splits",
+                 "streamkl_status_string", "streamkl_get_device_status"):
+        assert want in syms
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_symbols():
+        assert hasattr(L, name), name
+        assert name in skl._SIGS, f"binding lacks {name}"
+
+
+def test_status_strings(L):
+    for s in range(5):
+        assert skl.status_string(s) and skl.status_string(s) != "unknown status"
+    assert skl.status_string(99) == "unknown status"
+
+
+def test_workspace_bytes(L):
+    assert skl.streamkl_fwd_splitk_workspace_bytes(1, 4, 131072, 8) == 5 * 4 * 8 * 4 * 131072
+    assert skl.streamkl_fwd_splitk_workspace_bytes(1, 1, 10, 0) == 0
+    assert skl.streamkl_fwd_splitk_workspace_bytes(1, 1, 10, 1025) == 0
+    assert skl.streamkl_fwd_splitk_workspace_bytes(-1, 1, 10, 2) == 0
+
+
+def test_suggest_splits_rejects_bad_sizes(L):
+    assert skl.streamkl_suggest_splits(0, 4, 128, 128, 0) == 0
+    assert skl.streamkl_suggest_splits(1, 4, 256, 128, 1) == 0  # causal NQ > NK
+
+
+A = 4096  # a 16-byte aligned fake address: never dereferenced, validation fails first
+
+
+def fwd(L, q=(A, A, A, A), B=1, H=1, NQ=128, NK=128, d1=64, d2=64, scale=0.125, causal=0,
+        out=(A, A, A)):
+    return L.streamkl_fwd(*q, B, H, NQ, NK, d1, d2, scale, causal, *out, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(scale=0.0), skl.STREAMKL_INVALID_ARG),
+    (dict(scale=-1.0), skl.STREAMKL_INVALID_ARG),
+    (dict(scale=float("nan")), skl.STREAMKL_INVALID_ARG),
+    (dict(scale=float("inf")), skl.STREAMKL_INVALID_ARG),
+    (dict(causal=2), skl.STREAMKL_INVALID_ARG),
+    (dict(d1=96), skl.STREAMKL_UNSUPPORTED),
+    (dict(d2=32), skl.STREAMKL_UNSUPPORTED),
+    (dict(NQ=256, NK=128, causal=1), skl.STREAMKL_INVALID_ARG),
+    (dict(NK=0), skl.STREAMKL_INVALID_ARG),
+    (dict(B=-1), skl.STREAMKL_INVALID_ARG),
+    (dict(q=(0, A, A, A)), skl.STREAMKL_INVALID_ARG),
+    (dict(q=(A, A + 2, A, A)), skl.STREAMKL_INVALID_ARG),
+    (dict(out=(0, A, A)), skl.STREAMKL_INVALID_ARG),
+    (dict(out=(A, A, A + 4)), skl.STREAMKL_INVALID_ARG),
+    (dict(B=70000), skl.STREAMKL_INVALID_ARG),
+])
+def test_fwd_validation(L, kw, status):
+    assert fwd(L, **kw) == status
+
+
+def test_empty_problem_is_noop(L):
+    # no rows: returns OK without touching any pointer or the device
+    assert fwd(L, q=(0, 0, 0, 0), NQ=0, out=(0, 0, 0)) == skl.STREAMKL_OK
+    assert fwd(L, q=(0, 0, 0, 0), B=0, out=(0, 0, 0)) == skl.STREAMKL_OK
+
+
+def test_splitk_validation(L):
+    f = L.streamkl_fwd_splitk
+    ok_args = (A, A, A, A, 1, 2, 256, 256, 64, 64, 0.125, 0)
+    need = skl.streamkl_fwd_splitk_workspace_bytes(1, 2, 256, 4)
+    assert f(*ok_args, 0, A, need, A, A, A, None) == skl.STREAMKL_INVALID_ARG      # splits < 1
+    assert f(*ok_args, 2000, A, 1 << 40, A, A, A, None) == skl.STREAMKL_INVALID_ARG  # splits > 1024
+    assert f(*ok_args, 4, A, need - 1, A, A, A, None) == skl.STREAMKL_INVALID_ARG   # small workspace
+    assert f(*ok_args, 4, 0, need, A, A, A, None) == skl.STREAMKL_INVALID_ARG       # null workspace
+    assert f(*ok_args, 4, A + 8, need, A, A, A, None) == skl.STREAMKL_INVALID_ARG   # misaligned
+
+
+def test_bwd_validation(L):
+    f = L.streamkl_bwd
+    base = (A, A, A, A, 1, 1, 128, 128, 64, 64, 0.125, 0, A, A, A, A)
+    assert f(*base, 2, 0, A, A, None) == skl.STREAMKL_INVALID_ARG   # bad mode
+    assert f(*base, 0, 3, A, A, None) == skl.STREAMKL_INVALID_ARG   # bad deterministic flag
+    assert f(*base, 0, 0, 0, A, None) == skl.STREAMKL_INVALID_ARG   # null dq
+    assert f(*base, 0, 0, A, A + 4, None) == skl.STREAMKL_INVALID_ARG  # misaligned dk
+    bad_lse = base[:13] + (0,) + base[14:]
+    assert f(*bad_lse, 0, 0, A, A, None) == skl.STREAMKL_INVALID_ARG
+
+
+def test_binding_raises_without_cuda_tensors(L):
+    import torch
+    x = torch.zeros(1, 1, 4, 64, dtype=torch.bfloat16)
+    with pytest.raises(TypeError):
+        skl.streamkl_fwd(x, x, x, x, 0.125, False)
