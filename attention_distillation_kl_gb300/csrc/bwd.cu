@@ -1,10 +1,671 @@
-// Backward kernels (in progress).
+// Backward kernels: tile-by-tile recompute of P1 = exp(S1 - LSE1) and
+// P2 = exp(S2 - LSE2) from the saved log-sum-exps (StreamKL article,
+// "Backward"), for the gradient of L = sum_i dKL_i KL_i with respect to one
+// side ("optimise P2", the standard distillation case, or "optimise P1"):
+//   mode P2:  dS2_ij = dKL_i (P2_ij - P1_ij)
+//   mode P1:  dS1_ij = dKL_i P1_ij (r_ij - KL_i),
+//             r_ij = (S1_ij - LSE1_i) - (S2_ij - LSE2_i) taken from logits,
+//             so nothing is a logarithm of an underflowed probability.
+//   dQ = s dS K_g,  dK = s dS^T Q_g  (g = the gradient side).
+//
+// Fused kernel (article section "GPU kernel engineering": one visit per
+// query/key tile pair, dQ through atomics).  One CTA owns a 128-key tile and
+// walks the query tiles that can see it.  GB300 mapping, 10 warps:
+//   warp 8     TMA: K1, K2 once; per query tile Q_o (single buffer) and Q_g
+//              (double buffer; it is read again by the dK product)
+//   warp 9     TMEM owner, MMA issuer:
+//                S1^T = K1 Q1^T, S2^T = K2 Q2^T   (M = keys, N = queries)
+//                dK  += dS^T Q_g                   (accumulates in TMEM)
+//                dQ   = dS K_g                     (per query tile)
+//              with S of tile i+1 issued before the gradient products of
+//              tile i, so the tensor pipe stays busy while dS is formed
+//   warps 0-3  thread = key row: P1/P2 and dS from S^T (TMEM) and the
+//              per-query LSE/dKL/KL of the tile; dS goes to shared memory as
+//              bf16 in the 128-byte-swizzled layout both products read:
+//              K-major A for dK, M-major A for dQ
+//   warps 4-7  dQ tile: TMEM -> registers -> fp32 vector atomics to global;
+//              finally dK (each CTA owns its keys: plain stores)
+// TMEM: S1^T [0,128), S2^T [128,256), dK [256, 256+dg), dQ [384, 384+dg).
+//
+// dQ-only kernel (deterministic two-pass mode): one CTA per query tile walks
+// the key tiles, thread = query row, dQ accumulates in TMEM and is stored
+// once; dK then comes from the fused kernel with its dQ product switched off.
 #include "kernels.cuh"
 #include "ptx.cuh"
 
+#include <cuda_bf16.h>
+
 namespace skl {
 
-int launch_bwd_fused(const TMaps&, int, int, const BwdArgs&, cudaStream_t) { return cudaErrorNotSupported; }
-int launch_bwd_dq(const TMaps&, int, int, const BwdArgs&, cudaStream_t) { return cudaErrorNotSupported; }
+constexpr int kBwdThreads = 320;
+constexpr int kSlack = 16384;  // tail padding: descriptor reads never leave the CTA's window
+
+template <int D1, int D2, int MODE>
+struct BwdLayout {
+  static constexpr int DG = MODE == STREAMKL_GRAD_P2 ? D2 : D1;  // gradient side
+  static constexpr int DO = MODE == STREAMKL_GRAD_P2 ? D1 : D2;  // other side
+  static constexpr uint32_t kDS = kTile * kTile * 2;
+  static constexpr uint32_t kK1 = kTile * D1 * 2, kK2 = kTile * D2 * 2;
+  static constexpr uint32_t kQo = kTile * DO * 2, kQg = kTile * DG * 2;
+  static constexpr uint32_t oDS = 0, oK1 = kDS, oK2 = oK1 + kK1, oQo = oK2 + kK2, oQg = oQo + kQo;
+  static constexpr uint32_t oPar = oQg + 2 * kQg;  // 2 buffers x 3 arrays x 128 floats
+  static constexpr uint32_t oBar = oPar + 2 * 3 * kTile * 4;
+  enum {
+    B_KFULL, B_QOFULL, B_QOEMPTY, B_QGFULL0, B_QGFULL1, B_QGEMPTY0, B_QGEMPTY1, B_SFULL, B_SFREE,
+    B_DSFULL, B_DSEMPTY, B_DQFULL, B_DQEMPTY, B_DKFULL, B_PAR0, B_PAR1, B_DONE, kNumBars
+  };
+  static constexpr uint32_t oMisc = oBar + kNumBars * 8;
+  static constexpr uint32_t kBytes = oMisc + 16;
+  static constexpr uint32_t kAlloc = kBytes + 1024 + kSlack;
+  static_assert(kAlloc <= 232448, "over the 227 KB shared memory limit");
+};
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+
+__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
+               "f"(d)
+               : "memory");
+}
+
+// Writes one 128-element bf16 row (64 packed registers) of a [rows][128]
+// operand in the 128-byte-swizzled layout: two 64-column blocks of
+// [rows][128 B], 16-byte chunk c of row r stored at chunk c ^ (r % 8).
+__device__ __forceinline__ void store_row_sw128(uint32_t base, int r, const uint32_t (&v)[64]) {
+  const uint32_t rb = base + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+  for (int c16 = 0; c16 < 16; ++c16) {
+    const int blk = c16 >> 3, c = c16 & 7;
+    st_shared_v4(rb + blk * (kTile * 128) + ((c ^ (r & 7)) << 4), v[4 * c16], v[4 * c16 + 1],
+                 v[4 * c16 + 2], v[4 * c16 + 3]);
+  }
+}
+
+// dS for 32 consecutive query columns of one key row (thread), packed to
+// bf16 pairs.  pa/pb/pw: per-column parameters in shared memory:
+//   mode P2: pa = -LSE1 log2e, pb = -LSE2 log2e, pw = dKL
+//   mode P1: pa = -LSE1 log2e, pb = -(LSE1 - LSE2 + KL), pw = dKL
+// Columns < first_visible (causal) or all columns when the key is past NK
+// (first_visible > 128) give 0.
+template <int MODE, bool kMask>
+__device__ __forceinline__ void ds_chunk(const uint32_t (&x1u)[32], const uint32_t (&x2u)[32],
+                                         const float* pa, const float* pb, const float* pw, float c,
+                                         float s, int col0, int first_visible, uint32_t* out16) {
+#pragma unroll
+  for (int k = 0; k < 32; k += 4) {
+    const float4 A = *reinterpret_cast<const float4*>(pa + col0 + k);
+    const float4 Bv = *reinterpret_cast<const float4*>(pb + col0 + k);
+    const float4 W = *reinterpret_cast<const float4*>(pw + col0 + k);
+    const float av[4] = {A.x, A.y, A.z, A.w}, bv[4] = {Bv.x, Bv.y, Bv.z, Bv.w};
+    const float wv[4] = {W.x, W.y, W.z, W.w};
+    float d[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float x1 = __uint_as_float(x1u[k + e]), x2 = __uint_as_float(x2u[k + e]);
+      const float p1 = ex2(fmaf(x1, c, av[e]));
+      float v;
+      if (MODE == STREAMKL_GRAD_P2) {
+        const float p2 = ex2(fmaf(x2, c, bv[e]));
+        v = wv[e] * (p2 - p1);
+      } else {
+        v = wv[e] * p1 * fmaf(x1 - x2, s, bv[e]);
+      }
+      if (kMask && col0 + k + e < first_visible) v = 0.f;
+      d[e] = v;
+    }
+    out16[k / 2] = pack_bf16(d[0], d[1]);
+    out16[k / 2 + 1] = pack_bf16(d[2], d[3]);
+  }
+}
+
+template <int D1, int D2, int MODE>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_fused_kernel(const __grid_constant__ CUtensorMap tq1, const __grid_constant__ CUtensorMap tk1,
+                     const __grid_constant__ CUtensorMap tq2, const __grid_constant__ CUtensorMap tk2,
+                     const BwdArgs a) {
+  using L = BwdLayout<D1, D2, MODE>;
+  constexpr int DG = L::DG, DO = L::DO;
+  constexpr bool kP2 = MODE == STREAMKL_GRAD_P2;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const int kt = blockIdx.x, bh = blockIdx.y;
+  const int k0 = kt * kTile;
+  const int off = a.NK - a.NQ;
+  const int nqt = (a.NQ + kTile - 1) / kTile;
+  // causal: query i sees key j iff i >= j - off; the first query tile that
+  // sees any key of this tile starts at row max(0, k0 - off)
+  const int qt_lo = a.causal ? max(0, k0 - off) / kTile : 0;
+  const int n = nqt - qt_lo;
+
+  auto bar = [&](int id) { return sb + L::oBar + 8u * id; };
+  const CUtensorMap* tqo = kP2 ? &tq1 : &tq2;
+  const CUtensorMap* tqg = kP2 ? &tq2 : &tq1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::oMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::oMisc + 4);
+  const Ctl ctl{abort_flag, a.status};
+
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < L::kNumBars; ++b) {
+      uint32_t count = 1;  // TMA transaction barriers and tcgen05.commit targets
+      if (b == L::B_SFREE || b == L::B_DSFULL || b == L::B_DQEMPTY) count = 4;  // one per warp
+      if (b == L::B_PAR0 || b == L::B_PAR1) count = 128;                       // one per thread
+      mbar_init(bar(b), count);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t t_s1 = tmem, t_s2 = tmem + 128, t_dk = tmem + 256, t_dq = tmem + 384;
+
+  if (warp == 8) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0 && n > 0) {
+      tma_prefetch_desc(&tq1);
+      tma_prefetch_desc(&tk1);
+      tma_prefetch_desc(&tq2);
+      tma_prefetch_desc(&tk2);
+      mbar_arrive_expect_tx(bar(L::B_KFULL), L::kK1 + L::kK2);
+#pragma unroll
+      for (int c = 0; c < D1 / 64; ++c)
+        tma_load_3d(sb + L::oK1 + c * (kTile * 128), &tk1, bar(L::B_KFULL), c * 64, k0, bh);
+#pragma unroll
+      for (int c = 0; c < D2 / 64; ++c)
+        tma_load_3d(sb + L::oK2 + c * (kTile * 128), &tk2, bar(L::B_KFULL), c * 64, k0, bh);
+      int issued = 0;
+      for (int i = 0; i < n; ++i) {
+        const int q0 = (qt_lo + i) * kTile;
+        if (!mbar_wait(bar(L::B_QOEMPTY), (i & 1) ^ 1, ctl)) break;
+        mbar_arrive_expect_tx(bar(L::B_QOFULL), L::kQo);
+#pragma unroll
+        for (int c = 0; c < DO / 64; ++c)
+          tma_load_3d(sb + L::oQo + c * (kTile * 128), tqo, bar(L::B_QOFULL), c * 64, q0, bh);
+        const int g = i & 1;
+        if (!mbar_wait(bar(L::B_QGEMPTY0 + g), ((i >> 1) & 1) ^ 1, ctl)) break;
+        mbar_arrive_expect_tx(bar(L::B_QGFULL0 + g), L::kQg);
+#pragma unroll
+        for (int c = 0; c < DG / 64; ++c)
+          tma_load_3d(sb + L::oQg + g * L::kQg + c * (kTile * 128), tqg, bar(L::B_QGFULL0 + g), c * 64,
+                      q0, bh);
+        issued = i + 1;
+      }
+      if (*abort_flag) {  // let the copies already started land before the CTA exits
+        const uint64_t lim = 200000000ull;
+        mbar_drain(bar(L::B_KFULL), 0, lim);
+        if (issued > 0) mbar_drain(bar(L::B_QOFULL), (issued - 1) & 1, lim);
+        for (int i = issued > 2 ? issued - 2 : 0; i < issued; ++i)
+          mbar_drain(bar(L::B_QGFULL0 + (i & 1)), (i >> 1) & 1, lim);
+      }
+    }
+  } else if (warp == 9) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16(128, 128, 0, 0);
+      constexpr uint32_t id_dk = idesc_bf16(128, DG, 0, 1);  // A = dS^T K-major, B = Q_g N-major
+      constexpr uint32_t id_dq = idesc_bf16(128, DG, 1, 1);  // A = dS M-major,  B = K_g N-major
+      const uint32_t oKg = kP2 ? L::oK2 : L::oK1;
+      // gradient products of query tile t (dS(t) in shared memory)
+      auto grads = [&](int t) -> bool {
+        if (!mbar_wait(bar(L::B_DSFULL), t & 1, ctl)) return false;
+        if (a.write_dq && !mbar_wait(bar(L::B_DQEMPTY), (t & 1) ^ 1, ctl)) return false;
+        tc_fence_after();
+        const uint32_t qg = sb + L::oQg + (t & 1) * L::kQg;
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          const uint32_t ao = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
+          mma_bf16_ss(t_dk, sdesc_sw128(sb + L::oDS + ao, 16, 1024),
+                      sdesc_sw128(qg + kk * 2048, kTile * 128, 1024), id_dk, (t > 0 || kk > 0) ? 1u : 0u);
+        }
+        if (a.write_dq) {
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            mma_bf16_ss(t_dq, sdesc_sw128(sb + L::oDS + kk * 2048, kTile * 128, 1024),
+                        sdesc_sw128(sb + oKg + kk * 2048, kTile * 128, 1024), id_dq, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(L::B_DSEMPTY));
+        mma_commit(bar(L::B_QGEMPTY0 + (t & 1)));
+        if (a.write_dq) mma_commit(bar(L::B_DQFULL));
+        return true;
+      };
+      bool ok = n > 0 && mbar_wait(bar(L::B_KFULL), 0, ctl);
+      for (int i = 0; ok && i < n; ++i) {
+        if (!mbar_wait(bar(L::B_QOFULL), i & 1, ctl)) break;
+        if (!mbar_wait(bar(L::B_QGFULL0 + (i & 1)), (i >> 1) & 1, ctl)) break;
+        if (!mbar_wait(bar(L::B_SFREE), (i & 1) ^ 1, ctl)) break;
+        tc_fence_after();
+        const uint32_t q1s = sb + (kP2 ? L::oQo : L::oQg + (i & 1) * L::kQg);
+        const uint32_t q2s = sb + (kP2 ? L::oQg + (i & 1) * L::kQg : L::oQo);
+#pragma unroll
+        for (int kk = 0; kk < D1 / 16; ++kk) {
+          const uint32_t o = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
+          mma_bf16_ss(t_s1, sdesc_sw128(sb + L::oK1 + o, 16, 1024), sdesc_sw128(q1s + o, 16, 1024), id_s,
+                      kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D2 / 16; ++kk) {
+          const uint32_t o = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
+          mma_bf16_ss(t_s2, sdesc_sw128(sb + L::oK2 + o, 16, 1024), sdesc_sw128(q2s + o, 16, 1024), id_s,
+                      kk > 0);
+        }
+        mma_commit(bar(L::B_SFULL));
+        mma_commit(bar(L::B_QOEMPTY));
+        if (i > 0 && !grads(i - 1)) {
+          ok = false;
+          break;
+        }
+      }
+      if (ok && n > 0 && !*abort_flag && grads(n - 1)) mma_commit(bar(L::B_DKFULL));
+      mma_commit(bar(L::B_DONE));
+      mbar_drain(bar(L::B_DONE), 0, 1000000000ull);
+    }
+  } else if (warp < 4) {
+    // ---------------------------------------------------------------- dS (thread = key row)
+    const int row = warp * 32 + lane;
+    const int kj = k0 + row;
+    const float c = a.scale * kLog2e;
+    const uint32_t lane_off = uint32_t(warp * 32) << 16;
+    const bool key_ok = kj < a.NK;
+    float* par = reinterpret_cast<float*>(smem + L::oPar);
+    for (int i = 0; i < n; ++i) {
+      const int q0 = (qt_lo + i) * kTile;
+      const int pb = i & 1;
+      // per-query parameters of this tile, one query per thread
+      {
+        float* P = par + pb * 3 * kTile;
+        const int qi = q0 + row;
+        float va = -INFINITY, vb = 0.f, vw = 0.f;
+        if (qi < a.NQ) {
+          const size_t idx = size_t(bh) * a.NQ + qi;
+          const float l1 = a.lse1[idx];
+          va = -l1 * kLog2e;
+          vw = a.dkl[idx];
+          vb = kP2 ? -a.lse2[idx] * kLog2e : -(l1 - a.lse2[idx] + a.kl[idx]);
+        } else if (kP2) {
+          vb = -INFINITY;
+        }
+        P[row] = va;
+        P[kTile + row] = vb;
+        P[2 * kTile + row] = vw;
+        mbar_arrive(bar(L::B_PAR0 + pb));
+      }
+      if (!mbar_wait_warp(bar(L::B_PAR0 + pb), (i >> 1) & 1, ctl)) break;
+      if (!mbar_wait_warp(bar(L::B_SFULL), i & 1, ctl)) break;
+      tc_fence_after();
+      const float* P = par + pb * 3 * kTile;
+      const bool need_mask = (k0 + kTile > a.NK) || (a.causal && q0 < k0 + kTile - 1 - off);
+      const int first_visible = !key_ok ? (1 << 30) : (a.causal ? kj - off - q0 : 0);
+      uint32_t dsr[64];
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t x1[32], x2[32];
+        tmem_ld2x32(t_s1 + lane_off + ch * 32, t_s2 + lane_off + ch * 32, x1, x2);
+        if (ch == 3) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(L::B_SFREE));
+        }
+        if (need_mask)
+          ds_chunk<MODE, true>(x1, x2, P, P + kTile, P + 2 * kTile, c, a.scale, ch * 32, first_visible,
+                               dsr + ch * 16);
+        else
+          ds_chunk<MODE, false>(x1, x2, P, P + kTile, P + 2 * kTile, c, a.scale, ch * 32, 0, dsr + ch * 16);
+      }
+      // the previous tile's products must be done reading dS before it is replaced
+      if (!mbar_wait_warp(bar(L::B_DSEMPTY), (i & 1) ^ 1, ctl)) break;
+      store_row_sw128(sb + L::oDS, row, dsr);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::B_DSFULL));
+    }
+  } else {
+    // ---------------------------------------------------------------- dQ / dK epilogue
+    const int w4 = warp - 4;
+    const int row = w4 * 32 + lane;
+    const uint32_t lane_off = uint32_t(w4 * 32) << 16;
+    if (a.write_dq) {
+      for (int i = 0; i < n; ++i) {
+        if (!mbar_wait_warp(bar(L::B_DQFULL), i & 1, ctl)) break;
+        tc_fence_after();
+        const int qi = (qt_lo + i) * kTile + row;
+        float* dst = a.dq + (size_t(bh) * a.NQ + qi) * DG;
+        // drain the whole dQ tile from TMEM first, so the next product can start
+        uint32_t v[DG / 32][32];
+#pragma unroll
+        for (int ch = 0; ch < DG / 32; ++ch) tmem_ld32(t_dq + lane_off + ch * 32, v[ch]);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(L::B_DQEMPTY));
+        if (qi < a.NQ) {
+#pragma unroll
+          for (int ch = 0; ch < DG / 32; ++ch)
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+              red_add_v4(dst + ch * 32 + e, a.scale * __uint_as_float(v[ch][e]),
+                         a.scale * __uint_as_float(v[ch][e + 1]), a.scale * __uint_as_float(v[ch][e + 2]),
+                         a.scale * __uint_as_float(v[ch][e + 3]));
+        }
+      }
+    }
+    if (n > 0 && mbar_wait_warp(bar(L::B_DKFULL), 0, ctl)) {
+      tc_fence_after();
+      const int kj = k0 + row;
+      float* dst = a.dk + (size_t(bh) * a.NK + kj) * DG;
+#pragma unroll
+      for (int ch = 0; ch < DG / 32; ++ch) {
+        uint32_t v[32];
+        tmem_ld32(t_dk + lane_off + ch * 32, v);
+        if (kj < a.NK) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4*>(dst + ch * 32 + e) =
+                make_float4(a.scale * __uint_as_float(v[e]), a.scale * __uint_as_float(v[e + 1]),
+                            a.scale * __uint_as_float(v[e + 2]), a.scale * __uint_as_float(v[e + 3]));
+        }
+      }
+    } else if (n == 0) {
+      // no query row sees this key tile: its dK is zero
+      const int kj = k0 + row;
+      if (kj < a.NK)
+        for (int e = 0; e < DG; e += 4)
+          *reinterpret_cast<float4*>(a.dk + (size_t(bh) * a.NK + kj) * DG + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ------------------------------------------------------------------------
+// dQ-only kernel for the deterministic mode.  One CTA per 128-row query tile
+// streams the visible key tiles (like the forward kernel):
+//   warp 4     TMA: Q1, Q2 once; K1_j, K2_j into a two-stage ring
+//   warp 5     MMA: S1 = Q1 K1_j^T, S2 = Q2 K2_j^T, then dQ += dS_j K_g,j
+//              (dS K-major from shared memory, K_g N-major); S of tile j+1
+//              is issued before the dQ product of tile j
+//   warps 0-3  thread = query row: dS_j from S and the row's own
+//              LSE1/LSE2/dKL/KL (held in registers), stored bf16 as
+//              [row][key] with the 128-byte swizzle; at the end dQ is read
+//              from TMEM and stored once (no atomics: bitwise reproducible)
+// Shared memory: [K stages][Q1][Q2][dS][barriers]; TMEM: S1 [0,128),
+// S2 [128,256), dQ [256, 256+dg).
+constexpr int kDqThreads = 192;
+
+template <int D1, int D2, int MODE>
+struct DqLayout {
+  static constexpr int DG = MODE == STREAMKL_GRAD_P2 ? D2 : D1;
+  static constexpr uint32_t kQ1 = kTile * D1 * 2, kQ2 = kTile * D2 * 2;
+  static constexpr uint32_t kK1 = kTile * D1 * 2, kK2 = kTile * D2 * 2;
+  static constexpr uint32_t kStage = kK1 + kK2;
+  static constexpr int kStages = 2;
+  static constexpr uint32_t oK = 0, oQ1 = kStages * kStage, oQ2 = oQ1 + kQ1, oDS = oQ2 + kQ2;
+  static constexpr uint32_t oBar = oDS + kTile * kTile * 2;
+  enum { B_QFULL, B_KFULL0, B_KFULL1, B_KEMPTY0, B_KEMPTY1, B_SFULL, B_SFREE, B_DSFULL, B_DSEMPTY,
+         B_DQFULL, B_DONE, kNumBars };
+  static constexpr uint32_t oMisc = oBar + kNumBars * 8;
+  static constexpr uint32_t kBytes = oMisc + 16;
+  static constexpr uint32_t kAlloc = kBytes + 1024;
+  static_assert(kAlloc <= 232448, "over the 227 KB shared memory limit");
+};
+
+template <int D1, int D2, int MODE>
+__global__ void __launch_bounds__(kDqThreads, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tq1, const __grid_constant__ CUtensorMap tk1,
+                  const __grid_constant__ CUtensorMap tq2, const __grid_constant__ CUtensorMap tk2,
+                  const BwdArgs a) {
+  using L = DqLayout<D1, D2, MODE>;
+  constexpr int DG = L::DG;
+  constexpr bool kP2 = MODE == STREAMKL_GRAD_P2;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const int nqt = (a.NQ + kTile - 1) / kTile;
+  const int qt = a.causal ? (nqt - 1 - int(blockIdx.x)) : int(blockIdx.x);
+  const int bh = blockIdx.y;
+  const int q0 = qt * kTile;
+  const int off = a.NK - a.NQ;
+  const int kend = a.causal ? min(q0 + kTile, a.NQ) + off : a.NK;
+  const int nkt = (kend + kTile - 1) / kTile;
+
+  auto bar = [&](int id) { return sb + L::oBar + 8u * id; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::oMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::oMisc + 4);
+  const Ctl ctl{abort_flag, a.status};
+
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < L::kNumBars; ++b)
+      mbar_init(bar(b), (b == L::B_SFREE || b == L::B_DSFULL) ? 4u : 1u);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t t_s1 = tmem, t_s2 = tmem + 128, t_dq = tmem + 256;
+
+  if (warp == 4) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar(L::B_QFULL), L::kQ1 + L::kQ2);
+#pragma unroll
+      for (int c = 0; c < D1 / 64; ++c)
+        tma_load_3d(sb + L::oQ1 + c * (kTile * 128), &tq1, bar(L::B_QFULL), c * 64, q0, bh);
+#pragma unroll
+      for (int c = 0; c < D2 / 64; ++c)
+        tma_load_3d(sb + L::oQ2 + c * (kTile * 128), &tq2, bar(L::B_QFULL), c * 64, q0, bh);
+      int issued = 0;
+      for (int j = 0; j < nkt; ++j) {
+        const int s = j & 1;
+        if (!mbar_wait(bar(L::B_KEMPTY0 + s), ((j >> 1) & 1) ^ 1, ctl)) break;
+        mbar_arrive_expect_tx(bar(L::B_KFULL0 + s), L::kStage);
+        const uint32_t st = sb + L::oK + s * L::kStage;
+#pragma unroll
+        for (int c = 0; c < D1 / 64; ++c)
+          tma_load_3d(st + c * (kTile * 128), &tk1, bar(L::B_KFULL0 + s), c * 64, j * kTile, bh);
+#pragma unroll
+        for (int c = 0; c < D2 / 64; ++c)
+          tma_load_3d(st + L::kK1 + c * (kTile * 128), &tk2, bar(L::B_KFULL0 + s), c * 64, j * kTile, bh);
+        issued = j + 1;
+      }
+      if (*abort_flag) {
+        mbar_drain(bar(L::B_QFULL), 0, 200000000ull);
+        for (int j = issued > 2 ? issued - 2 : 0; j < issued; ++j)
+          mbar_drain(bar(L::B_KFULL0 + (j & 1)), (j >> 1) & 1, 200000000ull);
+      }
+    }
+  } else if (warp == 5) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16(128, 128, 0, 0);
+      constexpr uint32_t id_dq = idesc_bf16(128, DG, 0, 1);  // A = dS K-major, B = K_g N-major
+      auto dq_product = [&](int t) -> bool {
+        if (!mbar_wait(bar(L::B_DSFULL), t & 1, ctl)) return false;
+        tc_fence_after();
+        const uint32_t kg = sb + L::oK + (t & 1) * L::kStage + (kP2 ? L::kK1 : 0);
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          const uint32_t ao = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
+          mma_bf16_ss(t_dq, sdesc_sw128(sb + L::oDS + ao, 16, 1024),
+                      sdesc_sw128(kg + kk * 2048, kTile * 128, 1024), id_dq, (t > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(bar(L::B_DSEMPTY));
+        mma_commit(bar(L::B_KEMPTY0 + (t & 1)));
+        return true;
+      };
+      bool ok = mbar_wait(bar(L::B_QFULL), 0, ctl);
+      for (int j = 0; ok && j < nkt; ++j) {
+        const int s = j & 1;
+        if (!mbar_wait(bar(L::B_KFULL0 + s), (j >> 1) & 1, ctl)) break;
+        if (!mbar_wait(bar(L::B_SFREE), (j & 1) ^ 1, ctl)) break;
+        tc_fence_after();
+        const uint32_t k1s = sb + L::oK + s * L::kStage, k2s = k1s + L::kK1;
+#pragma unroll
+        for (int kk = 0; kk < D1 / 16; ++kk) {
+          const uint32_t o = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
+          mma_bf16_ss(t_s1, sdesc_sw128(sb + L::oQ1 + o, 16, 1024), sdesc_sw128(k1s + o, 16, 1024), id_s,
+                      kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D2 / 16; ++kk) {
+          const uint32_t o = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
+          mma_bf16_ss(t_s2, sdesc_sw128(sb + L::oQ2 + o, 16, 1024), sdesc_sw128(k2s + o, 16, 1024), id_s,
+                      kk > 0);
+        }
+        mma_commit(bar(L::B_SFULL));
+        if (j > 0 && !dq_product(j - 1)) {
+          ok = false;
+          break;
+        }
+      }
+      if (ok && nkt > 0 && !*abort_flag && dq_product(nkt - 1)) mma_commit(bar(L::B_DQFULL));
+      mma_commit(bar(L::B_DONE));
+      mbar_drain(bar(L::B_DONE), 0, 1000000000ull);
+    }
+  } else {
+    // ---------------------------------------------------------------- dS (thread = query row)
+    const int row = warp * 32 + lane;
+    const int qi = q0 + row;
+    const float c = a.scale * kLog2e;
+    const uint32_t lane_off = uint32_t(warp * 32) << 16;
+    const int lim = a.causal ? min(qi + off, a.NK - 1) : a.NK - 1;  // last visible key
+    float na = -INFINITY, nb = kP2 ? -INFINITY : 0.f, w = 0.f;
+    if (qi < a.NQ) {
+      const size_t idx = size_t(bh) * a.NQ + qi;
+      const float l1 = a.lse1[idx];
+      na = -l1 * kLog2e;
+      w = a.dkl[idx];
+      nb = kP2 ? -a.lse2[idx] * kLog2e : -(l1 - a.lse2[idx] + a.kl[idx]);
+    }
+    for (int j = 0; j < nkt; ++j) {
+      if (!mbar_wait_warp(bar(L::B_SFULL), j & 1, ctl)) break;
+      tc_fence_after();
+      const int k0 = j * kTile;
+      const bool need_mask = (k0 + kTile > a.NK) || (a.causal && k0 + kTile - 1 > q0 + off);
+      const int lim_rel = lim - k0;
+      uint32_t dsr[64];
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t x1[32], x2[32];
+        tmem_ld2x32(t_s1 + lane_off + ch * 32, t_s2 + lane_off + ch * 32, x1, x2);
+        if (ch == 3) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(L::B_SFREE));
+        }
+#pragma unroll
+        for (int k = 0; k < 32; k += 2) {
+          float d[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const float x1f = __uint_as_float(x1[k + e]), x2f = __uint_as_float(x2[k + e]);
+            const float p1 = ex2(fmaf(x1f, c, na));
+            float v = kP2 ? w * (ex2(fmaf(x2f, c, nb)) - p1) : w * p1 * fmaf(x1f - x2f, a.scale, nb);
+            if (need_mask && ch * 32 + k + e > lim_rel) v = 0.f;
+            d[e] = v;
+          }
+          dsr[ch * 16 + k / 2] = pack_bf16(d[0], d[1]);
+        }
+      }
+      if (!mbar_wait_warp(bar(L::B_DSEMPTY), (j & 1) ^ 1, ctl)) break;
+      store_row_sw128(sb + L::oDS, row, dsr);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::B_DSFULL));
+    }
+    if (nkt > 0 && mbar_wait_warp(bar(L::B_DQFULL), 0, ctl)) {
+      tc_fence_after();
+      float* dst = a.dq + (size_t(bh) * a.NQ + qi) * DG;
+#pragma unroll
+      for (int ch = 0; ch < DG / 32; ++ch) {
+        uint32_t v[32];
+        tmem_ld32(t_dq + lane_off + ch * 32, v);
+        if (qi < a.NQ) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4*>(dst + ch * 32 + e) =
+                make_float4(a.scale * __uint_as_float(v[e]), a.scale * __uint_as_float(v[e + 1]),
+                            a.scale * __uint_as_float(v[e + 2]), a.scale * __uint_as_float(v[e + 3]));
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D1, int D2, int MODE>
+static int launch_fused_t(const TMaps& m, const BwdArgs& a, cudaStream_t st) {
+  using L = BwdLayout<D1, D2, MODE>;
+  auto kern = bwd_fused_kernel<D1, D2, MODE>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  if (e != cudaSuccess) return e;
+  dim3 grid((a.NK + kTile - 1) / kTile, a.BH);
+  kern<<<grid, kBwdThreads, L::kAlloc, st>>>(m.q1, m.k1, m.q2, m.k2, a);
+  return cudaGetLastError();
+}
+
+template <int D1, int D2, int MODE>
+static int launch_dq_t(const TMaps& m, const BwdArgs& a, cudaStream_t st) {
+  using L = DqLayout<D1, D2, MODE>;
+  auto kern = bwd_dq_kernel<D1, D2, MODE>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  if (e != cudaSuccess) return e;
+  dim3 grid((a.NQ + kTile - 1) / kTile, a.BH);
+  kern<<<grid, kDqThreads, L::kAlloc, st>>>(m.q1, m.k1, m.q2, m.k2, a);
+  return cudaGetLastError();
+}
+
+#define SKL_DISPATCH(FN)                                                                    \
+  do {                                                                                      \
+    const bool p2 = a.mode == STREAMKL_GRAD_P2;                                             \
+    if (d1 == 128 && d2 == 128) return p2 ? FN<128, 128, 0>(m, a, st) : FN<128, 128, 1>(m, a, st); \
+    if (d1 == 128 && d2 == 64) return p2 ? FN<128, 64, 0>(m, a, st) : FN<128, 64, 1>(m, a, st);    \
+    if (d1 == 64 && d2 == 128) return p2 ? FN<64, 128, 0>(m, a, st) : FN<64, 128, 1>(m, a, st);    \
+    if (d1 == 64 && d2 == 64) return p2 ? FN<64, 64, 0>(m, a, st) : FN<64, 64, 1>(m, a, st);       \
+    return cudaErrorInvalidValue;                                                           \
+  } while (0)
+
+int launch_bwd_fused(const TMaps& m, int d1, int d2, const BwdArgs& a, cudaStream_t st) {
+  SKL_DISPATCH(launch_fused_t);
+}
+
+int launch_bwd_dq(const TMaps& m, int d1, int d2, const BwdArgs& a, cudaStream_t st) {
+  SKL_DISPATCH(launch_dq_t);
+}
 
 }  // namespace skl

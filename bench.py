@@ -1,0 +1,326 @@
+"""Benchmark: fused attention-KL forward + P2-side backward at 64K context x
+32 heads (d = 128, causal, bf16), one JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mine|reference]
+
+A step is one pass of the whole path over one batch: streamkl_fwd (KL, LSE1,
+LSE2) then streamkl_bwd in the standard-distillation mode (dQ2, dK2, fused
+with atomics).  value = algorithmic TFLOP/s of the step: 2(d1+d2) flops per
+unmasked (query, key) pair forward, 2(d1+d2) + 4 d2 backward.  Inputs
+(2.15 GB) are larger than L2, so no flush is needed between steps.  Under
+torchrun every rank runs its own batch (weak scaling, no collective on the
+data path); the reported time is the max over ranks.
+
+--impl reference times the float64 CPU oracle (the reference arm for this
+method) on a bounded sample of the same workload.
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from attention_distillation_kl_gb300.workloads import WORKLOADS, generate, generate_dkl  # noqa: E402
+
+W = WORKLOADS["c4"]
+METRIC = "fused attn-KL fwd+bwd TFLOP/s at 64K ctx x 32 heads (d=128, causal, P2-side grad)"
+UNIT = "TFLOP/s"
+
+# DRAM bytes per launch of the dominant kernel from one ncu capture, valid
+# only while its source is unchanged (sha256 of the file it lives in).
+TRAFFIC = {}
+
+
+def flops(w):
+    p = w.pairs
+    return 2 * (w.d1 + w.d2) * p, (2 * (w.d1 + w.d2) + 4 * w.d2) * p
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return d["bf16_tflops"], d["bf16_tflops_sustained"], d["hbm_gbs"], "measured"
+    return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+class Clocks:
+    """Samples SM clocks and throttle reasons while the timed region runs."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            self.proc.wait(timeout=10)
+            self.t.join(timeout=5)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = float(f[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def src_sha(name):
+    p = os.path.join(ROOT, "attention_distillation_kl_gb300", "csrc", name)
+    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+
+
+def cpu_sample(rows):
+    """The oracle, as it stands, on the last `rows` query rows of one head of
+    the workload (each sees ~64K keys): forward plus P2-side backward.  The
+    causal sub-problem (rows x all keys, bottom-right aligned) is exactly
+    those rows of the full problem."""
+    import oracle
+    from attention_distillation_kl_gb300.workloads import generate_head, to_f64
+    q1, k1, q2, k2 = [to_f64(t) for t in generate_head(W, 0, 0)]
+    q1, q2 = q1[-rows:], q2[-rows:]
+    t0 = time.perf_counter()
+    oracle.forward_head(q1, k1, q2, k2, W.scale, True)
+    oracle.backward_head(q1, k1, q2, k2, W.scale, True, np.ones(rows), oracle.MODE_P2)
+    dt = time.perf_counter() - t0
+    nk = W.NK
+    pairs = rows * (nk - rows) + rows * (rows + 1) // 2
+    fl = (2 * (W.d1 + W.d2) + 2 * (W.d1 + W.d2) + 4 * W.d2) * pairs
+    return fl / dt / 1e12, dt
+
+
+def run_reference(args, rank):
+    if rank != 0:
+        return
+    rows = 512
+    for _ in range(args.warmup):
+        cpu_sample(rows)
+    vals, dts = [], []
+    for _ in range(args.steps):
+        v, dt = cpu_sample(rows)
+        vals.append(v)
+        dts.append(dt)
+    value = float(np.median(vals))
+    cores = len(os.sched_getaffinity(0))
+    sample = f"last {rows} query rows of head (0,0) of the 64K x 32-head workload, fwd + P2 bwd, float64 numpy"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": float(np.median(dts)) * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded normal, perturbed student)",
+        "config": {"workload": "c4: B=1 H=32 NQ=NK=65536 d1=d2=128 causal bf16 inputs", "sample_rows": rows},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def ex2_rate(skl):
+    out = torch.empty(1, device="cuda")
+    blocks, iters = 152 * 8, 4096
+    skl.streamkl_probe_ex2(out, blocks, iters)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    best = None
+    for _ in range(3):
+        e0.record()
+        skl.streamkl_probe_ex2(out, blocks, iters)
+        e1.record()
+        torch.cuda.synchronize()
+        t = e0.elapsed_time(e1) * 1e-3
+        best = t if best is None else min(best, t)
+    return blocks * 256 * iters * 8 / best
+
+
+def run_mine(args, rank, world, local):
+    import attention_distillation_kl_gb300 as skl  # raises if the CUDA library is missing
+    torch.cuda.set_device(local)
+    dev_id = torch.cuda.current_device()
+    w = W.with_(seed=W.seed + 1000 * rank)  # each rank its own batch
+    host = [t.pin_memory() for t in generate(w)]
+    dkl_h = generate_dkl(w).pin_memory()
+    dev = [t.cuda() for t in host]
+    dkl = dkl_h.cuda()
+    B, H, N = w.B, w.H, w.NQ
+    kl = torch.empty(B, H, N, device="cuda")
+    l1, l2 = torch.empty_like(kl), torch.empty_like(kl)
+    dq = torch.empty(B, H, N, w.d2, device="cuda")
+    dk = torch.empty(B, H, w.NK, w.d2, device="cuda")
+    kl_h = torch.empty(B, H, N).pin_memory()
+    f_fwd, f_bwd = flops(w)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        skl.streamkl_fwd(*dev, w.scale, w.causal, kl, l1, l2)
+        if ev is not None:
+            ev[1].record(stream)
+        skl.streamkl_bwd(*dev, w.scale, w.causal, kl, l1, l2, dkl, skl.STREAMKL_GRAD_P2, False, dq, dk)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if skl.streamkl_get_device_status() != 0:
+        raise RuntimeError("device status reported a timeout during warm-up")
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with Clocks(dev_id) as clk:
+        t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for k in range(args.steps):
+            step(evs[k])
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    fwd_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
+    bwd_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in evs]))
+    if world > 1:
+        t = torch.tensor([total_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * (f_fwd + f_bwd) / (ms_per_step * 1e-3) / 1e12
+
+    # end to end through the public API: pinned host inputs in, KL out, every step
+    e2e_steps = max(2, min(args.steps, 5))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        for d, h in zip(dev, host):
+            d.copy_(h, non_blocking=True)
+        dkl.copy_(dkl_h, non_blocking=True)
+        step()
+        kl_h.copy_(kl, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = sum(t.numel() * t.element_size() for t in host) + dkl_h.numel() * 4
+    d2h = kl_h.numel() * 4
+
+    rate = ex2_rate(skl)
+    burst, sustained, _hbm, src = peaks()
+    pairs = w.pairs
+    # roofline time of each kernel: the slower of the tensor pipe and the ex2 unit
+    t_fwd = max(f_fwd / (sustained * 1e12), 2 * pairs / rate)
+    t_bwd = max(f_bwd / (sustained * 1e12), 2 * pairs / rate)
+    bwd_tf = f_bwd / (bwd_ms * 1e-3) / 1e12
+    fwd_tf = f_fwd / (fwd_ms * 1e-3) / 1e12
+    dom = "bwd" if bwd_ms >= fwd_ms else "fwd"
+    tr = TRAFFIC.get("bwd_fused" if dom == "bwd" else "fwd")
+    traffic = None
+    if tr and tr["src_sha"] == src_sha("bwd.cu" if dom == "bwd" else "fwd.cu"):
+        traffic = tr["bytes"]
+    if skl.streamkl_get_device_status() != 0:
+        raise RuntimeError("device status reported a timeout")
+
+    out = None
+    if rank == 0:
+        out = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded normal, perturbed student)",
+            "config": {"workload": "c4: B=1 H=32 NQ=NK=65536 d1=d2=128 causal, fwd + P2-side bwd (fused)",
+                       "global_batch": world * w.B, "seq_len": w.NQ, "heads": w.H,
+                       "parallelism": f"replicas{world}",
+                       "l2": "inputs (2.15 GB) larger than L2, no flush"},
+            "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
+            "fwd_roofline_frac": t_fwd / (fwd_ms * 1e-3), "bwd_roofline_frac": t_bwd / (bwd_ms * 1e-3),
+            "ex2_per_s": rate,
+            "roofline": {"bound": "tensor", "achieved": bwd_tf if dom == "bwd" else fwd_tf,
+                         "peak": sustained, "unit": "TFLOP/s",
+                         "frac": (bwd_tf if dom == "bwd" else fwd_tf) / sustained,
+                         "traffic": traffic, "kernel": "bwd_fused_kernel<128,128,P2>" if dom == "bwd"
+                         else "fwd_kernel<128,128>", "peak_source": f"{src} bf16 sustained",
+                         "frac_of_burst": (bwd_tf if dom == "bwd" else fwd_tf) / burst},
+            "e2e": {"value": (f_fwd + f_bwd) / (e2e_ms * 1e-3) / 1e12 * world, "unit": UNIT,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": 2 * args.steps,
+            "clocks": clk.summary(),
+        }
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    if world > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl")
+    out = run_mine(args, rank, world, local)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, dt = cpu_sample(3072)
+        out["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+                               "sample": "last 3072 query rows of head (0,0) of the 64K x 32-head workload, "
+                                         f"fwd + P2 bwd, float64 numpy ({dt:.1f} s)"}
+    if rank == 0:
+        print(json.dumps(out))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -291,13 +291,22 @@ def backward_dq_rows(q1, k1, q2, k2, scale, causal, dkl, mode, rows):
     return scale * (ds @ kg)
 
 
-def backward_dk_keys(q1, k1, q2, k2, scale, causal, dkl, mode, keys, row_block=256):
-    """dK for selected keys of one head: dK_j = s sum_i dS_ij Q_i over all rows."""
+def backward_dk_keys(q1, k1, q2, k2, scale, causal, dkl, mode, keys, row_block=256, first_row=0):
+    """dK for selected keys of one head: dK_j = s sum_i dS_ij Q_i over all rows.
+
+    ``first_row`` skips rows that see none of ``keys`` under the causal mask
+    (their dS entries are exactly zero); it must not exceed min(keys) - (NK - NQ).
+    """
     keys = np.asarray(keys)
-    nq = q1.shape[0]
+    nq, nk = q1.shape[0], k1.shape[0]
+    if first_row > 0 and (not causal or first_row > keys.min() - (nk - nq)):
+        raise ValueError("first_row would skip rows that see the requested keys")
     qg, kg = (q2, k2) if mode == MODE_P2 else (q1, k1)
     dk = np.zeros((keys.shape[0], kg.shape[1]))
     for rows in _row_blocks(nq, row_block):
+        rows = rows[rows >= first_row]
+        if rows.shape[0] == 0:
+            continue
         r = _head_rows(q1, k1, q2, k2, scale, causal, rows)
         ds = _grad_scores(r, dkl[rows], mode)[:, keys]
         dk += scale * (ds.T @ qg[rows])

@@ -276,6 +276,10 @@ def pin_sampled_backward(o):
                                        dq[rows], rtol=1e-13, atol=1e-15)
             np.testing.assert_allclose(o.backward_dk_keys(q1, k1, q2, k2, 0.8, causal, dkl, mode, keys,
                                                           row_block=4), dk[keys], rtol=1e-12, atol=1e-15)
+            if causal:  # rows before key 13 - (26 - 21) = 8 see none of keys 13, 25
+                np.testing.assert_allclose(o.backward_dk_keys(q1, k1, q2, k2, 0.8, causal, dkl, mode,
+                                                              [13, 25], row_block=4, first_row=8),
+                                           dk[[13, 25]], rtol=1e-12, atol=1e-15)
 
 
 def pin_underflow_is_finite(o):
