@@ -272,7 +272,8 @@ def run_mine(args, rank, world, local):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded normal, perturbed student)",
-            "config": {"workload": "c4: B=1 H=32 NQ=NK=65536 d1=d2=128 causal, fwd + P2-side bwd (fused)",
+            "config": {"workload": (f"{w.name}: B={w.B} H={w.H} NQ={w.NQ} NK={w.NK} d1={w.d1} d2={w.d2} "
+                                    f"{'causal' if w.causal else 'non-causal'}, fwd + P2-side bwd (fused)"),
                        "global_batch": world * w.B, "seq_len": w.NQ, "heads": w.H,
                        "parallelism": f"replicas{world}",
                        "l2": "inputs (2.15 GB) larger than L2, no flush"},
@@ -282,8 +283,8 @@ def run_mine(args, rank, world, local):
             "roofline": {"bound": "tensor", "achieved": bwd_tf if dom == "bwd" else fwd_tf,
                          "peak": sustained, "unit": "TFLOP/s",
                          "frac": (bwd_tf if dom == "bwd" else fwd_tf) / sustained,
-                         "traffic": traffic, "kernel": "bwd_fused_kernel<128,128,P2>" if dom == "bwd"
-                         else "fwd_kernel<128,128>", "peak_source": f"{src} bf16 sustained",
+                         "traffic": traffic, "kernel": f"bwd_fused_kernel<{w.d1},{w.d2},P2>" if dom == "bwd"
+                         else f"fwd_kernel<{w.d1},{w.d2}>", "peak_source": f"{src} bf16 sustained",
                          "frac_of_burst": (bwd_tf if dom == "bwd" else fwd_tf) / burst},
             "e2e": {"value": (f_fwd + f_bwd) / (e2e_ms * 1e-3) / 1e12 * world, "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -300,10 +301,16 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="c4", choices=sorted(WORKLOADS),
+                    help="profiling aid: run the same step on another named workload")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
     local = int(os.environ.get("LOCAL_RANK", 0))
+    global W
+    if args.workload != "c4":
+        W = WORKLOADS[args.workload]
+        args.no_cpu_baseline = True
     if args.impl == "reference":
         run_reference(args, rank)
         return
