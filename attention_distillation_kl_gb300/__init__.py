@@ -16,7 +16,7 @@ import torch
 __all__ = [
     "StreamKLError", "lib", "library_path",
     "streamkl_fwd", "streamkl_fwd_splitk", "streamkl_fwd_splitk_workspace_bytes",
-    "streamkl_suggest_splits", "streamkl_bwd", "streamkl_status_string",
+    "streamkl_suggest_splits", "streamkl_fwd_splitk_noalloc", "streamkl_bwd", "streamkl_status_string",
     "streamkl_get_device_status", "streamkl_probe_ex2",
     "STREAMKL_OK", "STREAMKL_INVALID_ARG", "STREAMKL_UNSUPPORTED", "STREAMKL_CUDA_ERROR",
     "STREAMKL_DEVICE_TIMEOUT", "STREAMKL_GRAD_P2", "STREAMKL_GRAD_P1",
@@ -44,6 +44,8 @@ _SIGS = {
     "streamkl_fwd_splitk": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P, _SZ,
                                  _P, _P, _P, _P]),
     "streamkl_fwd_splitk_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
+    "streamkl_fwd_splitk_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I,
+                                         _P, _P, _P, _P]),
     "streamkl_suggest_splits": (_I, [_I, _I, _I, _I, _I]),
     "streamkl_bwd": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P, _P, _I, _I,
                           _P, _P, _P]),
@@ -155,6 +157,33 @@ def streamkl_fwd_splitk(q1, k1, q2, k2, scale, causal, num_splits, workspace=Non
                                      workspace.numel() * workspace.element_size(),
                                      kl.data_ptr(), lse1.data_ptr(), lse2.data_ptr(), _stream(stream)),
            "streamkl_fwd_splitk")
+    return kl, lse1, lse2
+
+
+# Size in bytes of the library's fixed key-split workspace (see the header).
+STREAMKL_STATIC_WORKSPACE_BYTES = 32 << 20
+
+
+def streamkl_fwd_splitk_noalloc(q1, k1, q2, k2, scale, causal, num_splits, kl=None, lse1=None,
+                                lse2=None, stream=None):
+    """Key-split forward that allocates no device memory inside the library.
+
+    For callers that cannot provide scratch memory (for example code running
+    under an allocator that owns all device memory): the per-split partials
+    live in a fixed array of STREAMKL_STATIC_WORKSPACE_BYTES inside the
+    library.  Calls overlapping on the GPU race on that array; the first call
+    on a device should precede any stream capture there.  Pass preallocated
+    ``kl``/``lse1``/``lse2`` to keep this wrapper allocation-free as well.
+    """
+    B, H, NQ, NK, d1, d2 = _dims(q1, k1, q2, k2)
+    kl = _out(kl, (B, H, NQ), q1.device, "kl")
+    lse1 = _out(lse1, (B, H, NQ), q1.device, "lse1")
+    lse2 = _out(lse2, (B, H, NQ), q1.device, "lse2")
+    _check(lib().streamkl_fwd_splitk_noalloc(q1.data_ptr(), k1.data_ptr(), q2.data_ptr(), k2.data_ptr(),
+                                             B, H, NQ, NK, d1, d2, float(scale), int(bool(causal)),
+                                             int(num_splits), kl.data_ptr(), lse1.data_ptr(),
+                                             lse2.data_ptr(), _stream(stream)),
+           "streamkl_fwd_splitk_noalloc")
     return kl, lse1, lse2
 
 

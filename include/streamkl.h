@@ -91,6 +91,35 @@ int streamkl_fwd_splitk(const void* q1, const void* k1, const void* q2, const vo
 size_t streamkl_fwd_splitk_workspace_bytes(int B, int H, int NQ, int num_splits);
 
 /*
+ * Key-split forward that allocates nothing (the pages have no counterpart:
+ * this is an interface for callers, not part of the method).  Some callers
+ * cannot call cudaMalloc or hand over a scratch buffer -- for example code
+ * inside a framework whose caching allocator owns all device memory, where a
+ * raw allocation can synchronise the device and upset its accounting, or a
+ * runtime that must not fail for lack of memory in the middle of a step.
+ * This variant keeps the per-split partials in one fixed array inside the
+ * library: STREAMKL_STATIC_WORKSPACE_BYTES of device memory that every GPU
+ * loading the library holds until the process exits.  The caller still
+ * passes inputs and outputs exactly as for streamkl_fwd_splitk.
+ * Limits: streamkl_fwd_splitk_workspace_bytes(B, H, NQ, num_splits) must not
+ *   exceed STREAMKL_STATIC_WORKSPACE_BYTES, else STREAMKL_INVALID_ARG and
+ *   nothing is enqueued.
+ * Set-up: the first call on a device (with that device current) looks up the
+ *   array's device address and caches it; make that first call before any
+ *   stream capture on the device.
+ * Sharing: all calls on a device share the array, which keeps the last
+ *   call's contents (nothing in it needs to start at zero).  Calls that
+ *   overlap on the GPU -- on different streams, or from different host
+ *   threads -- race on it; serialise them.
+ * No cudaMalloc, cudaFree or other allocating routine is called.
+ */
+#define STREAMKL_STATIC_WORKSPACE_BYTES ((size_t)32 << 20)
+int streamkl_fwd_splitk_noalloc(const void* q1, const void* k1, const void* q2, const void* k2,
+                                int B, int H, int NQ, int NK, int d1, int d2, float scale,
+                                int causal, int num_splits, float* kl, float* lse1, float* lse2,
+                                streamkl_stream_t stream);
+
+/*
  * Advisory split count for the current device: the smallest number of
  * splits that gives at least two waves of CTAs, capped by the key tiles of
  * the longest row.  Returns 1 when no split is needed, 0 on invalid sizes.

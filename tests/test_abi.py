@@ -121,3 +121,14 @@ def test_binding_raises_without_cuda_tensors(L):
     x = torch.zeros(1, 1, 4, 64, dtype=torch.bfloat16)
     with pytest.raises(TypeError):
         skl.streamkl_fwd(x, x, x, x, 0.125, False)
+
+
+def test_noalloc_constant_and_host_refusal(L):
+    text = open(HEADER).read()
+    m = re.search(r"#define STREAMKL_STATIC_WORKSPACE_BYTES \(\(size_t\)(\d+) << (\d+)\)", text)
+    assert m and int(m.group(1)) << int(m.group(2)) == skl.STREAMKL_STATIC_WORKSPACE_BYTES
+    f = L.streamkl_fwd_splitk_noalloc
+    # partials of 5*4*1024*16*2048 bytes exceed the fixed array: refused before any device call
+    assert f(A, A, A, A, 1, 16, 2048, 128, 64, 64, 0.125, 0, 1024, A, A, A, None) == skl.STREAMKL_INVALID_ARG
+    assert f(A, A, A, A, 1, 1, 128, 128, 64, 64, 0.125, 0, 0, A, A, A, None) == skl.STREAMKL_INVALID_ARG
+    assert f(0, 0, 0, 0, 1, 1, 0, 128, 64, 64, 0.125, 0, 2, 0, 0, 0, None) == skl.STREAMKL_OK  # no rows
