@@ -50,6 +50,21 @@ bool make_map(CUtensorMap* m, const void* ptr, long long BH, long long N, int d)
   return r == CUDA_SUCCESS;
 }
 
+// dQ [BH][NQ][dg] fp32 as a 3-D tensor: boxes of 32 elements x 32 rows x 1,
+// 128-byte swizzle, the target of the backward's bulk reduce-adds.
+bool make_map_dq(CUtensorMap* m, void* ptr, long long BH, long long NQ, int dg) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[3] = {cuuint64_t(dg), cuuint64_t(NQ), cuuint64_t(BH)};
+  cuuint64_t strides[2] = {cuuint64_t(dg) * 4, cuuint64_t(NQ) * dg * 4};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool head_dim_ok(int d) { return d == 64 || d == 128; }
@@ -111,7 +126,7 @@ int streamkl_fwd(const void* q1, const void* k1, const void* q2, const void* k2,
   if (!kl || !lse1 || !lse2 || !aligned16(kl) || !aligned16(lse1) || !aligned16(lse2))
     return STREAMKL_INVALID_ARG;
   if ((s = device_ok()) != STREAMKL_OK) return s;
-  skl::TMaps m;
+  skl::TMaps m{};
   if ((s = make_maps(&m, q1, k1, q2, k2, B * H, NQ, NK, d1, d2)) != STREAMKL_OK) return s;
   int* st = status_ptr();
   if (!st) return STREAMKL_CUDA_ERROR;
@@ -138,7 +153,7 @@ int streamkl_fwd_splitk(const void* q1, const void* k1, const void* q2, const vo
   const size_t need = streamkl_fwd_splitk_workspace_bytes(B, H, NQ, num_splits);
   if (!workspace || !aligned16(workspace) || workspace_bytes < need) return STREAMKL_INVALID_ARG;
   if ((s = device_ok()) != STREAMKL_OK) return s;
-  skl::TMaps m;
+  skl::TMaps m{};
   if ((s = make_maps(&m, q1, k1, q2, k2, B * H, NQ, NK, d1, d2)) != STREAMKL_OK) return s;
   int* st = status_ptr();
   if (!st) return STREAMKL_CUDA_ERROR;
@@ -185,13 +200,14 @@ int streamkl_bwd(const void* q1, const void* k1, const void* q2, const void* k2,
       !aligned16(dk))
     return STREAMKL_INVALID_ARG;
   if ((s = device_ok()) != STREAMKL_OK) return s;
-  skl::TMaps m;
+  skl::TMaps m{};
   if ((s = make_maps(&m, q1, k1, q2, k2, B * H, NQ, NK, d1, d2)) != STREAMKL_OK) return s;
   int* st = status_ptr();
   if (!st) return STREAMKL_CUDA_ERROR;
   skl::BwdArgs a{B * H, NQ, NK, causal, mode, scale, kl, lse1, lse2, dkl, dq, dk, st, 1};
   if (!deterministic) {
     const size_t dq_bytes = size_t(B) * H * NQ * dg * 4;
+    if (!make_map_dq(&m.dq, dq, (long long)B * H, NQ, dg)) return STREAMKL_CUDA_ERROR;
     if (cudaMemsetAsync(dq, 0, dq_bytes, cs) != cudaSuccess) return STREAMKL_CUDA_ERROR;
     return as_status(skl::launch_bwd_fused(m, d1, d2, a, cs));
   }

@@ -23,8 +23,11 @@
 //              per-query LSE/dKL/KL of the tile; dS goes to shared memory as
 //              bf16 in the 128-byte-swizzled layout both products read:
 //              K-major A for dK, M-major A for dQ
-//   warps 4-7  dQ tile: TMEM -> registers -> fp32 vector atomics to global;
-//              finally dK (each CTA owns its keys: plain stores)
+//   warps 4-7  dQ tile: TMEM -> registers (scaled) -> a 32 x 32 fp32 block per
+//              warp in 128-byte-swizzled shared memory -> TMA bulk tensor
+//              reduce-add into global dQ (full 128-byte lines; rows past NQ
+//              are clipped by the tensor map); finally dK (each CTA owns its
+//              keys: plain stores)
 // TMEM: S1^T [0,128), S2^T [128,256), dK [256, 256+dg), dQ [384, 384+dg).
 //
 // dQ-only kernel (deterministic two-pass mode): one CTA per query tile walks
@@ -38,7 +41,6 @@
 namespace skl {
 
 constexpr int kBwdThreads = 320;
-constexpr int kSlack = 16384;  // tail padding: descriptor reads never leave the CTA's window
 
 template <int D1, int D2, int MODE>
 struct BwdLayout {
@@ -48,7 +50,8 @@ struct BwdLayout {
   static constexpr uint32_t kK1 = kTile * D1 * 2, kK2 = kTile * D2 * 2;
   static constexpr uint32_t kQo = kTile * DO * 2, kQg = kTile * DG * 2;
   static constexpr uint32_t oDS = 0, oK1 = kDS, oK2 = oK1 + kK1, oQo = oK2 + kK2, oQg = oQo + kQo;
-  static constexpr uint32_t oPar = oQg + 2 * kQg;  // 2 buffers x 3 arrays x 128 floats
+  static constexpr uint32_t oStage = oQg + 2 * kQg;  // dQ staging: 4 warps x [32 rows][128 B]
+  static constexpr uint32_t oPar = oStage + 4 * 4096;  // 2 buffers x 3 arrays x 128 floats
   static constexpr uint32_t oBar = oPar + 2 * 3 * kTile * 4;
   enum {
     B_KFULL, B_QOFULL, B_QOEMPTY, B_QGFULL0, B_QGFULL1, B_QGEMPTY0, B_QGEMPTY1, B_SFULL, B_SFREE,
@@ -56,7 +59,7 @@ struct BwdLayout {
   };
   static constexpr uint32_t oMisc = oBar + kNumBars * 8;
   static constexpr uint32_t kBytes = oMisc + 16;
-  static constexpr uint32_t kAlloc = kBytes + 1024 + kSlack;
+  static constexpr uint32_t kAlloc = kBytes + 1024;
   static_assert(kAlloc <= 232448, "over the 227 KB shared memory limit");
 };
 
@@ -68,12 +71,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
-               : "memory");
-}
-
-__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
-               "f"(d)
                : "memory");
 }
 
@@ -131,7 +128,7 @@ template <int D1, int D2, int MODE>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_fused_kernel(const __grid_constant__ CUtensorMap tq1, const __grid_constant__ CUtensorMap tk1,
                      const __grid_constant__ CUtensorMap tq2, const __grid_constant__ CUtensorMap tk2,
-                     const BwdArgs a) {
+                     const __grid_constant__ CUtensorMap tdq, const BwdArgs a) {
   using L = BwdLayout<D1, D2, MODE>;
   constexpr int DG = L::DG, DO = L::DO;
   constexpr bool kP2 = MODE == STREAMKL_GRAD_P2;
@@ -342,11 +339,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int row = w4 * 32 + lane;
     const uint32_t lane_off = uint32_t(w4 * 32) << 16;
     if (a.write_dq) {
+      // this warp's staging block: row r of 128 B at r * 128, 16-byte chunk c at c ^ (r % 8)
+      const uint32_t stage = sb + L::oStage + w4 * 4096;
+      const uint32_t my_row = stage + lane * 128;
+      if (lane == 0) tma_prefetch_desc(&tdq);
       for (int i = 0; i < n; ++i) {
         if (!mbar_wait_warp(bar(L::B_DQFULL), i & 1, ctl)) break;
         tc_fence_after();
-        const int qi = (qt_lo + i) * kTile + row;
-        float* dst = a.dq + (size_t(bh) * a.NQ + qi) * DG;
+        const int q0 = (qt_lo + i) * kTile;
         // drain the whole dQ tile from TMEM first, so the next product can start
         uint32_t v[DG / 32][32];
 #pragma unroll
@@ -354,16 +354,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(L::B_DQEMPTY));
-        if (qi < a.NQ) {
 #pragma unroll
-          for (int ch = 0; ch < DG / 32; ++ch)
+        for (int ch = 0; ch < DG / 32; ++ch) {
+          if (lane == 0) bulk_wait_read_all();  // the previous block has left the staging buffer
+          __syncwarp();
 #pragma unroll
-            for (int e = 0; e < 32; e += 4)
-              red_add_v4(dst + ch * 32 + e, a.scale * __uint_as_float(v[ch][e]),
-                         a.scale * __uint_as_float(v[ch][e + 1]), a.scale * __uint_as_float(v[ch][e + 2]),
-                         a.scale * __uint_as_float(v[ch][e + 3]));
+          for (int c = 0; c < 8; ++c) {
+            const float4 f = make_float4(a.scale * __uint_as_float(v[ch][4 * c]),
+                                         a.scale * __uint_as_float(v[ch][4 * c + 1]),
+                                         a.scale * __uint_as_float(v[ch][4 * c + 2]),
+                                         a.scale * __uint_as_float(v[ch][4 * c + 3]));
+            st_shared_v4(my_row + ((c ^ (lane & 7)) << 4), __float_as_uint(f.x), __float_as_uint(f.y),
+                         __float_as_uint(f.z), __float_as_uint(f.w));
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && q0 + w4 * 32 < a.NQ) {  // a box starting past NQ has nothing to add
+            tma_reduce_add_3d(&tdq, stage, ch * 32, q0 + w4 * 32, bh);
+            bulk_commit();
+          }
         }
       }
+      if (lane == 0) bulk_wait_all();  // every reduce has landed before the CTA exits
     }
     if (n > 0 && mbar_wait_warp(bar(L::B_DKFULL), 0, ctl)) {
       tc_fence_after();
@@ -635,7 +647,7 @@ static int launch_fused_t(const TMaps& m, const BwdArgs& a, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
   dim3 grid((a.NK + kTile - 1) / kTile, a.BH);
-  kern<<<grid, kBwdThreads, L::kAlloc, st>>>(m.q1, m.k1, m.q2, m.k2, a);
+  kern<<<grid, kBwdThreads, L::kAlloc, st>>>(m.q1, m.k1, m.q2, m.k2, m.dq, a);
   return cudaGetLastError();
 }
 
