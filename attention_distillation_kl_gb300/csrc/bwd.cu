@@ -10,20 +10,22 @@
 //
 // Fused kernel (article section "GPU kernel engineering": one visit per
 // query/key tile pair, dQ through atomics).  One CTA owns a 128-key tile and
-// walks the query tiles that can see it.  GB300 mapping, 10 warps:
-//   warp 8     TMA: K1, K2 once; per query tile Q_o (single buffer) and Q_g
+// walks the query tiles that can see it.  GB300 mapping, 14 warps:
+//   warp 12    TMA: K1, K2 once; per query tile Q_o (single buffer) and Q_g
 //              (double buffer; it is read again by the dK product)
-//   warp 9     TMEM owner, MMA issuer:
+//   warp 13    TMEM owner, MMA issuer:
 //                S1^T = K1 Q1^T, S2^T = K2 Q2^T   (M = keys, N = queries)
 //                dK  += dS^T Q_g                   (accumulates in TMEM)
 //                dQ   = dS K_g                     (per query tile)
 //              with S of tile i+1 issued before the gradient products of
 //              tile i, so the tensor pipe stays busy while dS is formed
-//   warps 0-3  thread = key row: P1/P2 and dS from S^T (TMEM) and the
-//              per-query LSE/dKL/KL of the tile; dS goes to shared memory as
-//              bf16 in the 128-byte-swizzled layout both products read:
-//              K-major A for dK, M-major A for dQ
-//   warps 4-7  dQ tile: TMEM -> registers (scaled) -> a 32 x 32 fp32 block per
+//   warps 0-7  thread = key row: P1/P2 and dS from S^T (TMEM) and the
+//              per-query LSE/dKL/KL of the tile; warps 0-3 take query
+//              columns 0-63, warps 4-7 columns 64-127 (two warps per SM
+//              sub-partition, and S^T is released after half the work).  dS
+//              goes to shared memory as bf16 in the 128-byte-swizzled layout
+//              both products read: K-major A for dK, M-major A for dQ
+//   warps 8-11 dQ tile: TMEM -> registers (scaled) -> a 32 x 32 fp32 block per
 //              warp in 128-byte-swizzled shared memory -> TMA bulk tensor
 //              reduce-add into global dQ (full 128-byte lines; rows past NQ
 //              are clipped by the tensor map); finally dK (each CTA owns its
@@ -40,7 +42,7 @@
 
 namespace skl {
 
-constexpr int kBwdThreads = 320;
+constexpr int kBwdThreads = 448;
 
 template <int D1, int D2, int MODE>
 struct BwdLayout {
@@ -51,11 +53,11 @@ struct BwdLayout {
   static constexpr uint32_t kQo = kTile * DO * 2, kQg = kTile * DG * 2;
   static constexpr uint32_t oDS = 0, oK1 = kDS, oK2 = oK1 + kK1, oQo = oK2 + kK2, oQg = oQo + kQo;
   static constexpr uint32_t oStage = oQg + 2 * kQg;  // dQ staging: 4 warps x [32 rows][128 B]
-  static constexpr uint32_t oPar = oStage + 4 * 4096;  // 2 buffers x 3 arrays x 128 floats
-  static constexpr uint32_t oBar = oPar + 2 * 3 * kTile * 4;
+  static constexpr uint32_t oPar = oStage + 4 * 4096;  // 2 warpgroups x 2 buffers x 3 x 128 floats
+  static constexpr uint32_t oBar = oPar + 2 * 2 * 3 * kTile * 4;
   enum {
     B_KFULL, B_QOFULL, B_QOEMPTY, B_QGFULL0, B_QGFULL1, B_QGEMPTY0, B_QGEMPTY1, B_SFULL, B_SFREE,
-    B_DSFULL, B_DSEMPTY, B_DQFULL, B_DQEMPTY, B_DKFULL, B_PAR0, B_PAR1, B_DONE, kNumBars
+    B_DSFULL, B_DSEMPTY, B_DQFULL, B_DQEMPTY, B_DKFULL, B_PAR0, B_PAR1, B_PAR2, B_PAR3, B_DONE, kNumBars
   };
   static constexpr uint32_t oMisc = oBar + kNumBars * 8;
   static constexpr uint32_t kBytes = oMisc + 16;
@@ -85,6 +87,14 @@ __device__ __forceinline__ void store_row_sw128(uint32_t base, int r, const uint
     st_shared_v4(rb + blk * (kTile * 128) + ((c ^ (r & 7)) << 4), v[4 * c16], v[4 * c16 + 1],
                  v[4 * c16 + 2], v[4 * c16 + 3]);
   }
+}
+
+// Writes one 64-element half (block `blk`) of such a row from 32 packed registers.
+__device__ __forceinline__ void store_half_row_sw128(uint32_t base, int r, int blk, const uint32_t (&v)[32]) {
+  const uint32_t rb = base + blk * (kTile * 128) + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    st_shared_v4(rb + ((c ^ (r & 7)) << 4), v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
 }
 
 // dS for 32 consecutive query columns of one key row (thread), packed to
@@ -157,14 +167,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (threadIdx.x == 0) {
     for (int b = 0; b < L::kNumBars; ++b) {
       uint32_t count = 1;  // TMA transaction barriers and tcgen05.commit targets
-      if (b == L::B_SFREE || b == L::B_DSFULL || b == L::B_DQEMPTY) count = 4;  // one per warp
-      if (b == L::B_PAR0 || b == L::B_PAR1) count = 128;                       // one per thread
+      if (b == L::B_SFREE || b == L::B_DSFULL) count = 8;  // one per dS warp
+      if (b == L::B_DQEMPTY) count = 4;                    // one per epilogue warp
+      if (b >= L::B_PAR0 && b <= L::B_PAR3) count = 128;   // one per thread of a dS warpgroup
       mbar_init(bar(b), count);
     }
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 9) {
+  if (warp == 13) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
@@ -174,7 +185,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const uint32_t t_s1 = tmem, t_s2 = tmem + 128, t_dk = tmem + 256, t_dq = tmem + 384;
 
-  if (warp == 8) {
+  if (warp == 12) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0 && n > 0) {
       tma_prefetch_desc(&tq1);
@@ -213,7 +224,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mbar_drain(bar(L::B_QGFULL0 + (i & 1)), (i >> 1) & 1, lim);
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == 13) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16(128, 128, 0, 0);
@@ -274,18 +285,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mma_commit(bar(L::B_DONE));
       mbar_drain(bar(L::B_DONE), 0, 1000000000ull);
     }
-  } else if (warp < 4) {
+  } else if (warp < 8) {
     // ---------------------------------------------------------------- dS (thread = key row)
-    const int row = warp * 32 + lane;
+    // warpgroup wg takes query columns [64 wg, 64 wg + 64) of every tile
+    const int wg = warp >> 2;
+    const int row = (warp & 3) * 32 + lane;
     const int kj = k0 + row;
     const float c = a.scale * kLog2e;
-    const uint32_t lane_off = uint32_t(warp * 32) << 16;
+    const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
     const bool key_ok = kj < a.NK;
-    float* par = reinterpret_cast<float*>(smem + L::oPar);
+    float* par = reinterpret_cast<float*>(smem + L::oPar) + wg * 2 * 3 * kTile;
     for (int i = 0; i < n; ++i) {
       const int q0 = (qt_lo + i) * kTile;
       const int pb = i & 1;
-      // per-query parameters of this tile, one query per thread
+      const uint32_t par_bar = bar(L::B_PAR0 + 2 * wg + pb);
+      // per-query parameters of this tile (each warpgroup keeps its own copy)
       {
         float* P = par + pb * 3 * kTile;
         const int qi = q0 + row;
@@ -302,40 +316,41 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         P[row] = va;
         P[kTile + row] = vb;
         P[2 * kTile + row] = vw;
-        mbar_arrive(bar(L::B_PAR0 + pb));
+        mbar_arrive(par_bar);
       }
-      if (!mbar_wait_warp(bar(L::B_PAR0 + pb), (i >> 1) & 1, ctl)) break;
+      if (!mbar_wait_warp(par_bar, (i >> 1) & 1, ctl)) break;
       if (!mbar_wait_warp(bar(L::B_SFULL), i & 1, ctl)) break;
       tc_fence_after();
       const float* P = par + pb * 3 * kTile;
       const bool need_mask = (k0 + kTile > a.NK) || (a.causal && q0 < k0 + kTile - 1 - off);
       const int first_visible = !key_ok ? (1 << 30) : (a.causal ? kj - off - q0 : 0);
-      uint32_t dsr[64];
+      uint32_t dsr[32];
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
+      for (int ch = 0; ch < 2; ++ch) {
+        const int col = wg * 64 + ch * 32;
         uint32_t x1[32], x2[32];
-        tmem_ld2x32(t_s1 + lane_off + ch * 32, t_s2 + lane_off + ch * 32, x1, x2);
-        if (ch == 3) {
+        tmem_ld2x32(t_s1 + lane_off + col, t_s2 + lane_off + col, x1, x2);
+        if (ch == 1) {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(L::B_SFREE));
         }
         if (need_mask)
-          ds_chunk<MODE, true>(x1, x2, P, P + kTile, P + 2 * kTile, c, a.scale, ch * 32, first_visible,
+          ds_chunk<MODE, true>(x1, x2, P, P + kTile, P + 2 * kTile, c, a.scale, col, first_visible,
                                dsr + ch * 16);
         else
-          ds_chunk<MODE, false>(x1, x2, P, P + kTile, P + 2 * kTile, c, a.scale, ch * 32, 0, dsr + ch * 16);
+          ds_chunk<MODE, false>(x1, x2, P, P + kTile, P + 2 * kTile, c, a.scale, col, 0, dsr + ch * 16);
       }
       // the previous tile's products must be done reading dS before it is replaced
       if (!mbar_wait_warp(bar(L::B_DSEMPTY), (i & 1) ^ 1, ctl)) break;
-      store_row_sw128(sb + L::oDS, row, dsr);
+      store_half_row_sw128(sb + L::oDS, row, wg, dsr);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(L::B_DSFULL));
     }
   } else {
     // ---------------------------------------------------------------- dQ / dK epilogue
-    const int w4 = warp - 4;
+    const int w4 = warp - 8;
     const int row = w4 * 32 + lane;
     const uint32_t lane_off = uint32_t(w4 * 32) << 16;
     if (a.write_dq) {
@@ -347,23 +362,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!mbar_wait_warp(bar(L::B_DQFULL), i & 1, ctl)) break;
         tc_fence_after();
         const int q0 = (qt_lo + i) * kTile;
-        // drain the whole dQ tile from TMEM first, so the next product can start
-        uint32_t v[DG / 32][32];
-#pragma unroll
-        for (int ch = 0; ch < DG / 32; ++ch) tmem_ld32(t_dq + lane_off + ch * 32, v[ch]);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(L::B_DQEMPTY));
+        // 32 columns at a time: TMEM -> registers -> staging -> bulk reduce;
+        // TMEM is released right after the last load
 #pragma unroll
         for (int ch = 0; ch < DG / 32; ++ch) {
+          uint32_t v[32];
+          tmem_ld32(t_dq + lane_off + ch * 32, v);
+          if (ch == DG / 32 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(L::B_DQEMPTY));
+          }
           if (lane == 0) bulk_wait_read_all();  // the previous block has left the staging buffer
           __syncwarp();
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
-            const float4 f = make_float4(a.scale * __uint_as_float(v[ch][4 * c]),
-                                         a.scale * __uint_as_float(v[ch][4 * c + 1]),
-                                         a.scale * __uint_as_float(v[ch][4 * c + 2]),
-                                         a.scale * __uint_as_float(v[ch][4 * c + 3]));
+            const float4 f = make_float4(a.scale * __uint_as_float(v[4 * c]),
+                                         a.scale * __uint_as_float(v[4 * c + 1]),
+                                         a.scale * __uint_as_float(v[4 * c + 2]),
+                                         a.scale * __uint_as_float(v[4 * c + 3]));
             st_shared_v4(my_row + ((c ^ (lane & 7)) << 4), __float_as_uint(f.x), __float_as_uint(f.y),
                          __float_as_uint(f.z), __float_as_uint(f.w));
           }
@@ -404,7 +421,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 13) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
