@@ -107,30 +107,37 @@ template <int MODE, bool kMask>
 __device__ __forceinline__ void ds_chunk(const uint32_t (&x1u)[32], const uint32_t (&x2u)[32],
                                          const float* pa, const float* pb, const float* pw, float c,
                                          float s, int col0, int first_visible, uint32_t* out16) {
+  const uint64_t C = f2(c, c), S = f2(s, s);
 #pragma unroll
   for (int k = 0; k < 32; k += 4) {
     const float4 A = *reinterpret_cast<const float4*>(pa + col0 + k);
     const float4 Bv = *reinterpret_cast<const float4*>(pb + col0 + k);
     const float4 W = *reinterpret_cast<const float4*>(pw + col0 + k);
-    const float av[4] = {A.x, A.y, A.z, A.w}, bv[4] = {Bv.x, Bv.y, Bv.z, Bv.w};
-    const float wv[4] = {W.x, W.y, W.z, W.w};
-    float d[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float x1 = __uint_as_float(x1u[k + e]), x2 = __uint_as_float(x2u[k + e]);
-      const float p1 = ex2(fmaf(x1, c, av[e]));
-      float v;
+    for (int e = 0; e < 4; e += 2) {
+      const uint64_t X1 = f2(__uint_as_float(x1u[k + e]), __uint_as_float(x1u[k + e + 1]));
+      const uint64_t X2 = f2(__uint_as_float(x2u[k + e]), __uint_as_float(x2u[k + e + 1]));
+      const uint64_t AA = e == 0 ? f2(A.x, A.y) : f2(A.z, A.w);
+      const uint64_t BB = e == 0 ? f2(Bv.x, Bv.y) : f2(Bv.z, Bv.w);
+      const uint64_t WW = e == 0 ? f2(W.x, W.y) : f2(W.z, W.w);
+      float ea, eb;
+      f2_split(f2_fma(X1, C, AA), ea, eb);
+      const uint64_t P1 = f2(ex2(ea), ex2(eb));
+      uint64_t D;
       if (MODE == STREAMKL_GRAD_P2) {
-        const float p2 = ex2(fmaf(x2, c, bv[e]));
-        v = wv[e] * (p2 - p1);
+        f2_split(f2_fma(X2, C, BB), ea, eb);
+        D = f2_mul(WW, f2_sub(f2(ex2(ea), ex2(eb)), P1));
       } else {
-        v = wv[e] * p1 * fmaf(x1 - x2, s, bv[e]);
+        D = f2_mul(f2_mul(WW, P1), f2_fma(f2_sub(X1, X2), S, BB));
       }
-      if (kMask && col0 + k + e < first_visible) v = 0.f;
-      d[e] = v;
+      float da, db;
+      f2_split(D, da, db);
+      if (kMask) {
+        if (col0 + k + e < first_visible) da = 0.f;
+        if (col0 + k + e + 1 < first_visible) db = 0.f;
+      }
+      out16[(k + e) / 2] = pack_bf16(da, db);
     }
-    out16[k / 2] = pack_bf16(d[0], d[1]);
-    out16[k / 2 + 1] = pack_bf16(d[2], d[3]);
   }
 }
 
@@ -243,6 +250,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mma_bf16_ss(t_dk, sdesc_sw128(sb + L::oDS + ao, 16, 1024),
                       sdesc_sw128(qg + kk * 2048, kTile * 128, 1024), id_dk, (t > 0 || kk > 0) ? 1u : 0u);
         }
+        // Q_g(t) is free once dK has read it: its reload starts before dQ runs
+        mma_commit(bar(L::B_QGEMPTY0 + (t & 1)));
         if (a.write_dq) {
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk)
@@ -250,32 +259,32 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         sdesc_sw128(sb + oKg + kk * 2048, kTile * 128, 1024), id_dq, kk > 0 ? 1u : 0u);
         }
         mma_commit(bar(L::B_DSEMPTY));
-        mma_commit(bar(L::B_QGEMPTY0 + (t & 1)));
         if (a.write_dq) mma_commit(bar(L::B_DQFULL));
         return true;
       };
+      // S^T of one side for query tile i: K (A, K-major) x Q tile (B, K-major)
+      auto s_product = [&](int side, uint32_t qs) {
+        const uint32_t ks = sb + (side == 1 ? L::oK1 : L::oK2);
+        const uint32_t d = side == 1 ? t_s1 : t_s2;
+        const int steps = (side == 1 ? D1 : D2) / 16;
+#pragma unroll
+        for (int kk = 0; kk < steps; ++kk) {
+          const uint32_t o = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
+          mma_bf16_ss(d, sdesc_sw128(ks + o, 16, 1024), sdesc_sw128(qs + o, 16, 1024), id_s, kk > 0);
+        }
+      };
       bool ok = n > 0 && mbar_wait(bar(L::B_KFULL), 0, ctl);
       for (int i = 0; ok && i < n; ++i) {
-        if (!mbar_wait(bar(L::B_QOFULL), i & 1, ctl)) break;
-        if (!mbar_wait(bar(L::B_QGFULL0 + (i & 1)), (i >> 1) & 1, ctl)) break;
         if (!mbar_wait(bar(L::B_SFREE), (i & 1) ^ 1, ctl)) break;
+        if (!mbar_wait(bar(L::B_QOFULL), i & 1, ctl)) break;
         tc_fence_after();
-        const uint32_t q1s = sb + (kP2 ? L::oQo : L::oQg + (i & 1) * L::kQg);
-        const uint32_t q2s = sb + (kP2 ? L::oQg + (i & 1) * L::kQg : L::oQo);
-#pragma unroll
-        for (int kk = 0; kk < D1 / 16; ++kk) {
-          const uint32_t o = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
-          mma_bf16_ss(t_s1, sdesc_sw128(sb + L::oK1 + o, 16, 1024), sdesc_sw128(q1s + o, 16, 1024), id_s,
-                      kk > 0);
-        }
-#pragma unroll
-        for (int kk = 0; kk < D2 / 16; ++kk) {
-          const uint32_t o = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
-          mma_bf16_ss(t_s2, sdesc_sw128(sb + L::oK2 + o, 16, 1024), sdesc_sw128(q2s + o, 16, 1024), id_s,
-                      kk > 0);
-        }
-        mma_commit(bar(L::B_SFULL));
+        // the other side first: its single Q buffer is released as early as possible
+        s_product(kP2 ? 1 : 2, sb + L::oQo);
         mma_commit(bar(L::B_QOEMPTY));
+        if (!mbar_wait(bar(L::B_QGFULL0 + (i & 1)), (i >> 1) & 1, ctl)) break;
+        tc_fence_after();
+        s_product(kP2 ? 2 : 1, sb + L::oQg + (i & 1) * L::kQg);
+        mma_commit(bar(L::B_SFULL));
         if (i > 0 && !grads(i - 1)) {
           ok = false;
           break;
@@ -595,6 +604,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       w = a.dkl[idx];
       nb = kP2 ? -a.lse2[idx] * kLog2e : -(l1 - a.lse2[idx] + a.kl[idx]);
     }
+    const uint64_t C = f2(c, c), SS = f2(a.scale, a.scale), NA = f2(na, na), NB = f2(nb, nb), WW = f2(w, w);
     for (int j = 0; j < nkt; ++j) {
       if (!mbar_wait_warp(bar(L::B_SFULL), j & 1, ctl)) break;
       tc_fence_after();
@@ -613,16 +623,25 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         }
 #pragma unroll
         for (int k = 0; k < 32; k += 2) {
-          float d[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const float x1f = __uint_as_float(x1[k + e]), x2f = __uint_as_float(x2[k + e]);
-            const float p1 = ex2(fmaf(x1f, c, na));
-            float v = kP2 ? w * (ex2(fmaf(x2f, c, nb)) - p1) : w * p1 * fmaf(x1f - x2f, a.scale, nb);
-            if (need_mask && ch * 32 + k + e > lim_rel) v = 0.f;
-            d[e] = v;
+          const uint64_t X1 = f2(__uint_as_float(x1[k]), __uint_as_float(x1[k + 1]));
+          const uint64_t X2 = f2(__uint_as_float(x2[k]), __uint_as_float(x2[k + 1]));
+          float ea, eb;
+          f2_split(f2_fma(X1, C, NA), ea, eb);
+          const uint64_t P1 = f2(ex2(ea), ex2(eb));
+          uint64_t D;
+          if (kP2) {
+            f2_split(f2_fma(X2, C, NB), ea, eb);
+            D = f2_mul(WW, f2_sub(f2(ex2(ea), ex2(eb)), P1));
+          } else {
+            D = f2_mul(f2_mul(WW, P1), f2_fma(f2_sub(X1, X2), SS, NB));
           }
-          dsr[ch * 16 + k / 2] = pack_bf16(d[0], d[1]);
+          float da, db;
+          f2_split(D, da, db);
+          if (need_mask) {
+            if (ch * 32 + k > lim_rel) da = 0.f;
+            if (ch * 32 + k + 1 > lim_rel) db = 0.f;
+          }
+          dsr[ch * 16 + k / 2] = pack_bf16(da, db);
         }
       }
       if (!mbar_wait_warp(bar(L::B_DSEMPTY), (j & 1) ^ 1, ctl)) break;

@@ -54,40 +54,44 @@ struct RowStats {
 
 // Folds 32 consecutive key columns into the running state.  Columns k with
 // k > lim_rel are masked (causal or past NK): they neither move the maxima
-// nor add to the sums.
+// nor add to the sums.  Pairs of columns go through the packed FP32 pipe.
 template <bool kMask>
 __device__ __forceinline__ void fold_chunk(RowStats& st, const uint32_t (&x1u)[32],
                                            const uint32_t (&x2u)[32], float c, int lim_rel) {
   float t1 = st.m1, t2 = st.m2;
 #pragma unroll
-  for (int k = 0; k < 32; ++k) {
-    const bool ok = !kMask || k <= lim_rel;
-    t1 = fmaxf(t1, ok ? __uint_as_float(x1u[k]) : kNegBig);
-    t2 = fmaxf(t2, ok ? __uint_as_float(x2u[k]) : kNegBig);
+  for (int k = 0; k < 32; k += 2) {
+    const bool oa = !kMask || k <= lim_rel, ob = !kMask || k + 1 <= lim_rel;
+    t1 = max3(t1, oa ? __uint_as_float(x1u[k]) : kNegBig, ob ? __uint_as_float(x1u[k + 1]) : kNegBig);
+    t2 = max3(t2, oa ? __uint_as_float(x2u[k]) : kNegBig, ob ? __uint_as_float(x2u[k + 1]) : kNegBig);
   }
   const float a1 = ex2((st.m1 - t1) * c);
   const float a2 = ex2((st.m2 - t2) * c);
   st.m1 = t1;
   st.m2 = t2;
-  const float nb1 = -t1 * c, nb2 = -t2 * c;
-  float l1a = 0.f, l1b = 0.f, l2a = 0.f, l2b = 0.f, aca = 0.f, acb = 0.f;
+  const uint64_t C = f2(c, c), NB1 = f2(-t1 * c, -t1 * c), NB2 = f2(-t2 * c, -t2 * c);
+  uint64_t L1 = f2(0.f, 0.f), L2 = L1, ACC = L1;
 #pragma unroll
   for (int k = 0; k < 32; k += 2) {
-    const float x1a = __uint_as_float(x1u[k]), x1b = __uint_as_float(x1u[k + 1]);
-    const float x2a = __uint_as_float(x2u[k]), x2b = __uint_as_float(x2u[k + 1]);
-    float p1a = ex2(fmaf(x1a, c, nb1)), p1b = ex2(fmaf(x1b, c, nb1));
-    float p2a = ex2(fmaf(x2a, c, nb2)), p2b = ex2(fmaf(x2b, c, nb2));
+    const uint64_t X1 = f2(__uint_as_float(x1u[k]), __uint_as_float(x1u[k + 1]));
+    const uint64_t X2 = f2(__uint_as_float(x2u[k]), __uint_as_float(x2u[k + 1]));
+    float e1a, e1b, e2a, e2b;
+    f2_split(f2_fma(X1, C, NB1), e1a, e1b);
+    f2_split(f2_fma(X2, C, NB2), e2a, e2b);
+    float p1a = ex2(e1a), p1b = ex2(e1b), p2a = ex2(e2a), p2b = ex2(e2b);
     if (kMask) {
       if (k > lim_rel) { p1a = 0.f; p2a = 0.f; }
       if (k + 1 > lim_rel) { p1b = 0.f; p2b = 0.f; }
     }
-    l1a += p1a;
-    l1b += p1b;
-    l2a += p2a;
-    l2b += p2b;
-    aca = fmaf(p1a, x1a - x2a, aca);
-    acb = fmaf(p1b, x1b - x2b, acb);
+    const uint64_t P1 = f2(p1a, p1b);
+    L1 = f2_add(L1, P1);
+    L2 = f2_add(L2, f2(p2a, p2b));
+    ACC = f2_fma(P1, f2_sub(X1, X2), ACC);
   }
+  float l1a, l1b, l2a, l2b, aca, acb;
+  f2_split(L1, l1a, l1b);
+  f2_split(L2, l2a, l2b);
+  f2_split(ACC, aca, acb);
   st.l1 = fmaf(st.l1, a1, l1a + l1b);
   st.acc = fmaf(st.acc, a1, aca + acb);
   st.l2 = fmaf(st.l2, a2, l2a + l2b);
