@@ -50,17 +50,17 @@ bool make_map(CUtensorMap* m, const void* ptr, long long BH, long long N, int d)
   return r == CUDA_SUCCESS;
 }
 
-// dQ [BH][NQ][dg] fp32 as a 3-D tensor: boxes of 32 elements x 32 rows x 1,
-// 128-byte swizzle, the target of the backward's bulk reduce-adds.
+// dQ [BH][NQ][dg] fp32 as a 3-D tensor: boxes of 16 elements x 32 rows x 1,
+// 64-byte swizzle, the target of the backward's bulk reduce-adds.
 bool make_map_dq(CUtensorMap* m, void* ptr, long long BH, long long NQ, int dg) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[3] = {cuuint64_t(dg), cuuint64_t(NQ), cuuint64_t(BH)};
   cuuint64_t strides[2] = {cuuint64_t(dg) * 4, cuuint64_t(NQ) * dg * 4};
-  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t box[3] = {16, 32, 1};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, es,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }

@@ -25,10 +25,10 @@
 //              sub-partition, and S^T is released after half the work).  dS
 //              goes to shared memory as bf16 in the 128-byte-swizzled layout
 //              both products read: K-major A for dK, M-major A for dQ
-//   warps 8-11 dQ tile: TMEM -> registers (scaled) -> a 32 x 32 fp32 block per
-//              warp in 128-byte-swizzled shared memory -> TMA bulk tensor
-//              reduce-add into global dQ (full 128-byte lines; rows past NQ
-//              are clipped by the tensor map); finally dK (each CTA owns its
+//   warps 8-11 dQ tile: TMEM -> registers (scaled) -> 32 x 16 fp32 boxes in
+//              swizzled shared memory (three per warp, round robin) -> TMA
+//              bulk tensor reduce-add into global dQ (rows past NQ are
+//              clipped by the tensor map); finally dK (each CTA owns its
 //              keys: plain stores)
 // TMEM: S1^T [0,128), S2^T [128,256), dK [256, 256+dg), dQ [384, 384+dg).
 //
@@ -52,8 +52,8 @@ struct BwdLayout {
   static constexpr uint32_t kK1 = kTile * D1 * 2, kK2 = kTile * D2 * 2;
   static constexpr uint32_t kQo = kTile * DO * 2, kQg = kTile * DG * 2;
   static constexpr uint32_t oDS = 0, oK1 = kDS, oK2 = oK1 + kK1, oQo = oK2 + kK2, oQg = oQo + kQo;
-  static constexpr uint32_t oStage = oQg + 2 * kQg;  // dQ staging: 4 warps x [32 rows][128 B]
-  static constexpr uint32_t oPar = oStage + 4 * 4096;  // 2 warpgroups x 2 buffers x 3 x 128 floats
+  static constexpr uint32_t oStage = oQg + 2 * kQg;  // dQ staging: 4 warps x 3 x [32 rows][64 B]
+  static constexpr uint32_t oPar = oStage + 4 * 3 * 2048;  // 2 warpgroups x 2 buffers x 3 x 128 floats
   static constexpr uint32_t oBar = oPar + 2 * 2 * 3 * kTile * 4;
   enum {
     B_KFULL, B_QOFULL, B_QOEMPTY, B_QGFULL0, B_QGFULL1, B_QGEMPTY0, B_QGEMPTY1, B_SFULL, B_SFREE,
@@ -363,16 +363,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int row = w4 * 32 + lane;
     const uint32_t lane_off = uint32_t(w4 * 32) << 16;
     if (a.write_dq) {
-      // this warp's staging block: row r of 128 B at r * 128, 16-byte chunk c at c ^ (r % 8)
-      const uint32_t stage = sb + L::oStage + w4 * 4096;
-      const uint32_t my_row = stage + lane * 128;
+      // Three 2 KB staging boxes per warp ([32 rows][16 fp32], 64-byte
+      // swizzle: 16-byte chunk c of row r at chunk c ^ ((r / 2) % 4)), used
+      // round robin so up to three bulk reduce-adds are in flight.
+      const uint32_t stage = sb + L::oStage + w4 * (3 * 2048);
+      const uint32_t swz = (lane >> 1) & 3;
+      int nred = 0;
       if (lane == 0) tma_prefetch_desc(&tdq);
       for (int i = 0; i < n; ++i) {
         if (!mbar_wait_warp(bar(L::B_DQFULL), i & 1, ctl)) break;
         tc_fence_after();
-        const int q0 = (qt_lo + i) * kTile;
-        // 32 columns at a time: TMEM -> registers -> staging -> bulk reduce;
-        // TMEM is released right after the last load
+        const int r0 = (qt_lo + i) * kTile + w4 * 32;  // first query row of this warp
 #pragma unroll
         for (int ch = 0; ch < DG / 32; ++ch) {
           uint32_t v[32];
@@ -382,22 +383,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(L::B_DQEMPTY));
           }
-          if (lane == 0) bulk_wait_read_all();  // the previous block has left the staging buffer
-          __syncwarp();
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const float4 f = make_float4(a.scale * __uint_as_float(v[4 * c]),
-                                         a.scale * __uint_as_float(v[4 * c + 1]),
-                                         a.scale * __uint_as_float(v[4 * c + 2]),
-                                         a.scale * __uint_as_float(v[4 * c + 3]));
-            st_shared_v4(my_row + ((c ^ (lane & 7)) << 4), __float_as_uint(f.x), __float_as_uint(f.y),
-                         __float_as_uint(f.z), __float_as_uint(f.w));
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0 && q0 + w4 * 32 < a.NQ) {  // a box starting past NQ has nothing to add
-            tma_reduce_add_3d(&tdq, stage, ch * 32, q0 + w4 * 32, bh);
-            bulk_commit();
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t box = stage + (nred % 3) * 2048;
+            if (lane == 0) bulk_wait_read_le2();  // the box used three reduces ago has been read
+            __syncwarp();
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const int e = h * 16 + 4 * c;
+              st_shared_v4(box + lane * 64 + ((c ^ swz) << 4), __float_as_uint(a.scale * __uint_as_float(v[e])),
+                           __float_as_uint(a.scale * __uint_as_float(v[e + 1])),
+                           __float_as_uint(a.scale * __uint_as_float(v[e + 2])),
+                           __float_as_uint(a.scale * __uint_as_float(v[e + 3])));
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0 && r0 < a.NQ) {  // a box starting past NQ has nothing to add
+              tma_reduce_add_3d(&tdq, box, ch * 32 + h * 16, r0, bh);
+              bulk_commit();
+            }
+            ++nred;
           }
         }
       }

@@ -11,7 +11,7 @@ constexpr int kTile = 128;  // query and key tile: 128 rows = 128 TMEM lanes
 
 struct TMaps {
   CUtensorMap q1, k1, q2, k2;  // [BH][N][d] bf16, boxes of 64 x 128, 128-byte swizzle
-  CUtensorMap dq;              // [BH][NQ][dg] fp32, boxes of 32 x 32, 128-byte swizzle (fused backward)
+  CUtensorMap dq;              // [BH][NQ][dg] fp32, boxes of 16 x 32, 64-byte swizzle (fused backward)
 };
 
 struct FwdArgs {
