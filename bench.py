@@ -45,6 +45,26 @@ TRAFFIC = {
 }
 
 
+def rank_workload(w, rank):
+    """Each rank runs its own batch of the same shape (weak scaling): same
+    workload, seed offset by the rank, so no two ranks process the same data."""
+    return w.with_(seed=w.seed + 1000 * rank)
+
+
+def max_over_ranks(x, world, device):
+    """The slowest rank's time defines the job's time."""
+    if world <= 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world, flops_per_rank, ms_per_step):
+    """Whole-job throughput: the work of every rank over the slowest time."""
+    return world * flops_per_rank / (ms_per_step * 1e-3) / 1e12
+
+
 def flops(w):
     p = w.pairs
     return 2 * (w.d1 + w.d2) * p, (2 * (w.d1 + w.d2) + 4 * w.d2) * p
@@ -181,7 +201,7 @@ def run_mine(args, rank, world, local):
     import attention_distillation_kl_gb300 as skl  # raises if the CUDA library is missing
     torch.cuda.set_device(local)
     dev_id = torch.cuda.current_device()
-    w = W.with_(seed=W.seed + 1000 * rank)  # each rank its own batch
+    w = rank_workload(W, rank)  # each rank its own batch
     host = [t.pin_memory() for t in generate(w)]
     dkl_h = generate_dkl(w).pin_memory()
     dev = [t.cuda() for t in host]
@@ -226,12 +246,9 @@ def run_mine(args, rank, world, local):
     total_ms = t_start.elapsed_time(t_end)
     fwd_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
     bwd_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in evs]))
-    if world > 1:
-        t = torch.tensor([total_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, "cuda")
     ms_per_step = total_ms / args.steps
-    value = world * (f_fwd + f_bwd) / (ms_per_step * 1e-3) / 1e12
+    value = job_tflops(world, f_fwd + f_bwd, ms_per_step)
 
     # end to end through the public API: pinned host inputs in, KL out, every step
     e2e_steps = max(2, min(args.steps, 5))
@@ -247,10 +264,7 @@ def run_mine(args, rank, world, local):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, world, "cuda")
     h2d = sum(t.numel() * t.element_size() for t in host) + dkl_h.numel() * 4
     d2h = kl_h.numel() * 4
 
@@ -290,7 +304,7 @@ def run_mine(args, rank, world, local):
                          "traffic": traffic, "kernel": f"bwd_fused_kernel<{w.d1},{w.d2},P2>" if dom == "bwd"
                          else f"fwd_kernel<{w.d1},{w.d2}>", "peak_source": f"{src} bf16 sustained",
                          "frac_of_burst": (bwd_tf if dom == "bwd" else fwd_tf) / burst},
-            "e2e": {"value": (f_fwd + f_bwd) / (e2e_ms * 1e-3) / 1e12 * world, "unit": UNIT,
+            "e2e": {"value": job_tflops(world, f_fwd + f_bwd, e2e_ms), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": 2 * args.steps,
             "clocks": clk.summary(),
