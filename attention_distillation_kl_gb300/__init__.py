@@ -17,7 +17,7 @@ __all__ = [
     "StreamKLError", "lib", "library_path",
     "streamkl_fwd", "streamkl_fwd_splitk", "streamkl_fwd_splitk_workspace_bytes",
     "streamkl_suggest_splits", "streamkl_fwd_splitk_noalloc", "streamkl_bwd", "streamkl_status_string",
-    "streamkl_get_device_status", "streamkl_probe_ex2",
+    "streamkl_get_device_status", "streamkl_probe_ex2", "streamkl_selftest_wait_timeout",
     "STREAMKL_OK", "STREAMKL_INVALID_ARG", "STREAMKL_UNSUPPORTED", "STREAMKL_CUDA_ERROR",
     "STREAMKL_DEVICE_TIMEOUT", "STREAMKL_GRAD_P2", "STREAMKL_GRAD_P1",
 ]
@@ -52,6 +52,7 @@ _SIGS = {
     "streamkl_status_string": (ctypes.c_char_p, [_I]),
     "streamkl_get_device_status": (_I, []),
     "streamkl_probe_ex2": (_I, [_P, _I, _I, _P]),
+    "streamkl_selftest_wait_timeout": (_I, [_I, _P]),
 }
 
 
@@ -212,3 +213,9 @@ def streamkl_get_device_status():
 def streamkl_probe_ex2(out, blocks, iters, stream=None):
     _check(lib().streamkl_probe_ex2(out.data_ptr(), int(blocks), int(iters), _stream(stream)),
            "streamkl_probe_ex2")
+
+
+def streamkl_selftest_wait_timeout(limit_us, stream=None):
+    """Runs a kernel whose barrier wait must time out (see the header)."""
+    _check(lib().streamkl_selftest_wait_timeout(int(limit_us), _stream(stream)),
+           "streamkl_selftest_wait_timeout")

@@ -352,6 +352,21 @@ __global__ void __launch_bounds__(256) ex2_probe_kernel(float* out, int iters) {
   if (blockIdx.x == 0 && threadIdx.x == 0) out[0] = s;
 }
 
+// Exercises the bounded-wait path: one thread waits on an mbarrier that no
+// one arrives on, gives up after `limit_ns`, records the timeout in the
+// status word and returns, leaving the context usable.
+__global__ void wait_timeout_selftest_kernel(int* status, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar), 1);
+    fence_barrier_init();
+    const Ctl ctl{&abort_flag, status};
+    mbar_wait_limit(smem_u32(&bar), 0, ctl, limit_ns);  // nothing ever arrives
+  }
+}
+
 template <int D1, int D2>
 static int launch_fwd_t(const TMaps& m, const FwdArgs& a, cudaStream_t st) {
   using L = FwdLayout<D1, D2>;
@@ -381,6 +396,11 @@ int launch_splitk_reduce(const float* partial, int rows, int num_splits, float* 
   if (blocks > sms * 8) blocks = sms * 8;
   if (blocks < 1) blocks = 1;
   splitk_reduce_kernel<<<blocks, 256, 0, st>>>(partial, rows, num_splits, kl, lse1, lse2);
+  return cudaGetLastError();
+}
+
+int launch_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t st) {
+  wait_timeout_selftest_kernel<<<1, 32, 0, st>>>(status, limit_ns);
   return cudaGetLastError();
 }
 

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstddef>
+#include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -44,5 +45,6 @@ int launch_splitk_reduce(const float* partial, int rows, int num_splits, float* 
 int launch_bwd_fused(const TMaps& m, int d1, int d2, const BwdArgs& a, cudaStream_t st);
 int launch_bwd_dq(const TMaps& m, int d1, int d2, const BwdArgs& a, cudaStream_t st);
 int launch_ex2_probe(float* out, int blocks, int iters, cudaStream_t st);
+int launch_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t st);
 
 }  // namespace skl

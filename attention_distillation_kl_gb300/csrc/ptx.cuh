@@ -118,18 +118,23 @@ struct Ctl {
 // Waits for the phase of `bar` with parity `parity` to complete.  Returns
 // false (without waiting further) once any thread of the CTA has aborted;
 // after STREAMKL_WAIT_LIMIT_NS it aborts the CTA and reports a timeout.
-static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, Ctl ctl) {
+static __device__ __noinline__ bool mbar_wait_limit(uint32_t bar, uint32_t parity, Ctl ctl,
+                                                    uint64_t limit_ns) {
   if (mbar_try(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
     if (mbar_try(bar, parity)) return true;
     if (*ctl.abort) return false;
-    if (globaltimer() - t0 > STREAMKL_WAIT_LIMIT_NS) {
+    if (globaltimer() - t0 > limit_ns) {
       *ctl.abort = 1;
       atomicCAS(ctl.status, 0, (int)STREAMKL_DEVICE_TIMEOUT);
       return false;
     }
   }
+}
+
+static __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, Ctl ctl) {
+  return mbar_wait_limit(bar, parity, ctl, STREAMKL_WAIT_LIMIT_NS);
 }
 
 // Bounded wait that ignores the abort flag: used on the way out to let copies

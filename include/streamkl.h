@@ -159,6 +159,15 @@ const char* streamkl_status_string(int status);
 int streamkl_get_device_status(void);
 
 /*
+ * Self-test of the timeout path (no counterpart on the pages): launches one
+ * tiny kernel that waits on a barrier nothing ever completes, gives up after
+ * `limit_us` microseconds (1 .. 1e6), sets the device status word to
+ * STREAMKL_DEVICE_TIMEOUT and returns; the CUDA context stays usable.  Read
+ * the result with streamkl_get_device_status() after synchronising.
+ */
+int streamkl_selftest_wait_timeout(int limit_us, streamkl_stream_t stream);
+
+/*
  * Device probe used for the roofline denominator: runs `blocks` CTAs of 256
  * threads, each thread evaluating `iters` x 8 independent ex2.approx.f32
  * chains, and writes a checksum to out[0] (device pointer) so the work is
