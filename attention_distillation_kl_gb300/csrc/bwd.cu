@@ -6,7 +6,8 @@
 //   mode P1:  dS1_ij = dKL_i P1_ij (r_ij - KL_i),
 //             r_ij = (S1_ij - LSE1_i) - (S2_ij - LSE2_i) taken from logits,
 //             so nothing is a logarithm of an underflowed probability.
-//   dQ = s dS K_g,  dK = s dS^T Q_g  (g = the gradient side).
+//   dQ = s dS K_g,  dK = s dS^T Q_g  (g = the gradient side; the kernels
+//   form s dS before rounding it to bf16, so the products come out scaled).
 //
 // Fused kernel (article section "GPU kernel engineering": one visit per
 // query/key tile pair, dQ through atomics).  One CTA owns a 128-key tile and
@@ -99,8 +100,10 @@ __device__ __forceinline__ void store_half_row_sw128(uint32_t base, int r, int b
 
 // dS for 32 consecutive query columns of one key row (thread), packed to
 // bf16 pairs.  pa/pb/pw: per-column parameters in shared memory:
-//   mode P2: pa = -LSE1 log2e, pb = -LSE2 log2e, pw = dKL
-//   mode P1: pa = -LSE1 log2e, pb = -(LSE1 - LSE2 + KL), pw = dKL
+//   mode P2: pa = -LSE1 log2e, pb = -LSE2 log2e, pw = s dKL
+//   mode P1: pa = -LSE1 log2e, pb = -(LSE1 - LSE2 + KL), pw = s dKL
+// (the softmax scale s rides on dS, so dK = dS^T Q and dQ = dS K need no
+// further scaling)
 // Columns < first_visible (causal) or all columns when the key is past NK
 // (first_visible > 128) give 0.
 template <int MODE, bool kMask>
@@ -317,7 +320,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const size_t idx = size_t(bh) * a.NQ + qi;
           const float l1 = a.lse1[idx];
           va = -l1 * kLog2e;
-          vw = a.dkl[idx];
+          vw = a.scale * a.dkl[idx];  // s folded into dS: dK and dQ come out scaled
           vb = kP2 ? -a.lse2[idx] * kLog2e : -(l1 - a.lse2[idx] + a.kl[idx]);
         } else if (kP2) {
           vb = -INFINITY;
@@ -391,10 +394,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
               const int e = h * 16 + 4 * c;
-              st_shared_v4(box + lane * 64 + ((c ^ swz) << 4), __float_as_uint(a.scale * __uint_as_float(v[e])),
-                           __float_as_uint(a.scale * __uint_as_float(v[e + 1])),
-                           __float_as_uint(a.scale * __uint_as_float(v[e + 2])),
-                           __float_as_uint(a.scale * __uint_as_float(v[e + 3])));
+              st_shared_v4(box + lane * 64 + ((c ^ swz) << 4), v[e], v[e + 1], v[e + 2], v[e + 3]);
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -420,8 +420,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
           for (int e = 0; e < 32; e += 4)
             *reinterpret_cast<float4*>(dst + ch * 32 + e) =
-                make_float4(a.scale * __uint_as_float(v[e]), a.scale * __uint_as_float(v[e + 1]),
-                            a.scale * __uint_as_float(v[e + 2]), a.scale * __uint_as_float(v[e + 3]));
+                make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]), __uint_as_float(v[e + 2]),
+                            __uint_as_float(v[e + 3]));
         }
       }
     } else if (n == 0) {
@@ -609,7 +609,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       w = a.dkl[idx];
       nb = kP2 ? -a.lse2[idx] * kLog2e : -(l1 - a.lse2[idx] + a.kl[idx]);
     }
-    const uint64_t C = f2(c, c), SS = f2(a.scale, a.scale), NA = f2(na, na), NB = f2(nb, nb), WW = f2(w, w);
+    const float ws = a.scale * w;  // s folded into dS
+    const uint64_t C = f2(c, c), SS = f2(a.scale, a.scale), NA = f2(na, na), NB = f2(nb, nb), WW = f2(ws, ws);
     for (int j = 0; j < nkt; ++j) {
       if (!mbar_wait_warp(bar(L::B_SFULL), j & 1, ctl)) break;
       tc_fence_after();
@@ -666,8 +667,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 #pragma unroll
           for (int e = 0; e < 32; e += 4)
             *reinterpret_cast<float4*>(dst + ch * 32 + e) =
-                make_float4(a.scale * __uint_as_float(v[e]), a.scale * __uint_as_float(v[e + 1]),
-                            a.scale * __uint_as_float(v[e + 2]), a.scale * __uint_as_float(v[e + 3]));
+                make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]), __uint_as_float(v[e + 2]),
+                            __uint_as_float(v[e + 3]));
         }
       }
     }
