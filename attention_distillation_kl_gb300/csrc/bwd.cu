@@ -36,10 +36,9 @@
 // dQ-only kernel (deterministic two-pass mode): one CTA per query tile walks
 // the key tiles, thread = query row, dQ accumulates in TMEM and is stored
 // once; dK then comes from the fused kernel with its dQ product switched off.
+#include "bwd_common.cuh"
 #include "kernels.cuh"
 #include "ptx.cuh"
-
-#include <cuda_bf16.h>
 
 namespace skl {
 
@@ -65,84 +64,6 @@ struct BwdLayout {
   static constexpr uint32_t kAlloc = kBytes + 1024;
   static_assert(kAlloc <= 232448, "over the 227 KB shared memory limit");
 };
-
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                             uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
-               : "memory");
-}
-
-// Writes one 128-element bf16 row (64 packed registers) of a [rows][128]
-// operand in the 128-byte-swizzled layout: two 64-column blocks of
-// [rows][128 B], 16-byte chunk c of row r stored at chunk c ^ (r % 8).
-__device__ __forceinline__ void store_row_sw128(uint32_t base, int r, const uint32_t (&v)[64]) {
-  const uint32_t rb = base + (r >> 3) * 1024 + (r & 7) * 128;
-#pragma unroll
-  for (int c16 = 0; c16 < 16; ++c16) {
-    const int blk = c16 >> 3, c = c16 & 7;
-    st_shared_v4(rb + blk * (kTile * 128) + ((c ^ (r & 7)) << 4), v[4 * c16], v[4 * c16 + 1],
-                 v[4 * c16 + 2], v[4 * c16 + 3]);
-  }
-}
-
-// Writes one 64-element half (block `blk`) of such a row from 32 packed registers.
-__device__ __forceinline__ void store_half_row_sw128(uint32_t base, int r, int blk, const uint32_t (&v)[32]) {
-  const uint32_t rb = base + blk * (kTile * 128) + (r >> 3) * 1024 + (r & 7) * 128;
-#pragma unroll
-  for (int c = 0; c < 8; ++c)
-    st_shared_v4(rb + ((c ^ (r & 7)) << 4), v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-}
-
-// dS for 32 consecutive query columns of one key row (thread), packed to
-// bf16 pairs.  pa/pb/pw: per-column parameters in shared memory:
-//   mode P2: pa = -LSE1 log2e, pb = -LSE2 log2e, pw = s dKL
-//   mode P1: pa = -LSE1 log2e, pb = -(LSE1 - LSE2 + KL), pw = s dKL
-// (the softmax scale s rides on dS, so dK = dS^T Q and dQ = dS K need no
-// further scaling)
-// Columns < first_visible (causal) or all columns when the key is past NK
-// (first_visible > 128) give 0.
-template <int MODE, bool kMask>
-__device__ __forceinline__ void ds_chunk(const uint32_t (&x1u)[32], const uint32_t (&x2u)[32],
-                                         const float* pa, const float* pb, const float* pw, float c,
-                                         float s, int col0, int first_visible, uint32_t* out16) {
-  const uint64_t C = f2(c, c), S = f2(s, s);
-#pragma unroll
-  for (int k = 0; k < 32; k += 4) {
-    const float4 A = *reinterpret_cast<const float4*>(pa + col0 + k);
-    const float4 Bv = *reinterpret_cast<const float4*>(pb + col0 + k);
-    const float4 W = *reinterpret_cast<const float4*>(pw + col0 + k);
-#pragma unroll
-    for (int e = 0; e < 4; e += 2) {
-      const uint64_t X1 = f2(__uint_as_float(x1u[k + e]), __uint_as_float(x1u[k + e + 1]));
-      const uint64_t X2 = f2(__uint_as_float(x2u[k + e]), __uint_as_float(x2u[k + e + 1]));
-      const uint64_t AA = e == 0 ? f2(A.x, A.y) : f2(A.z, A.w);
-      const uint64_t BB = e == 0 ? f2(Bv.x, Bv.y) : f2(Bv.z, Bv.w);
-      const uint64_t WW = e == 0 ? f2(W.x, W.y) : f2(W.z, W.w);
-      float ea, eb;
-      f2_split(f2_fma(X1, C, AA), ea, eb);
-      const uint64_t P1 = f2(ex2(ea), ex2(eb));
-      uint64_t D;
-      if (MODE == STREAMKL_GRAD_P2) {
-        f2_split(f2_fma(X2, C, BB), ea, eb);
-        D = f2_mul(WW, f2_sub(f2(ex2(ea), ex2(eb)), P1));
-      } else {
-        D = f2_mul(f2_mul(WW, P1), f2_fma(f2_sub(X1, X2), S, BB));
-      }
-      float da, db;
-      f2_split(D, da, db);
-      if (kMask) {
-        if (col0 + k + e < first_visible) da = 0.f;
-        if (col0 + k + e + 1 < first_visible) db = 0.f;
-      }
-      out16[(k + e) / 2] = pack_bf16(da, db);
-    }
-  }
-}
 
 template <int D1, int D2, int MODE>
 __global__ void __launch_bounds__(kBwdThreads, 1)
@@ -212,13 +133,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       int issued = 0;
       for (int i = 0; i < n; ++i) {
         const int q0 = (qt_lo + i) * kTile;
-        if (!mbar_wait(bar(L::B_QOEMPTY), (i & 1) ^ 1, ctl)) break;
+        if (!mbar_wait_polled(bar(L::B_QOEMPTY), (i & 1) ^ 1, ctl)) break;
         mbar_arrive_expect_tx(bar(L::B_QOFULL), L::kQo);
 #pragma unroll
         for (int c = 0; c < DO / 64; ++c)
           tma_load_3d(sb + L::oQo + c * (kTile * 128), tqo, bar(L::B_QOFULL), c * 64, q0, bh);
         const int g = i & 1;
-        if (!mbar_wait(bar(L::B_QGEMPTY0 + g), ((i >> 1) & 1) ^ 1, ctl)) break;
+        if (!mbar_wait_polled(bar(L::B_QGEMPTY0 + g), ((i >> 1) & 1) ^ 1, ctl)) break;
         mbar_arrive_expect_tx(bar(L::B_QGFULL0 + g), L::kQg);
 #pragma unroll
         for (int c = 0; c < DG / 64; ++c)
@@ -243,8 +164,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint32_t oKg = kP2 ? L::oK2 : L::oK1;
       // gradient products of query tile t (dS(t) in shared memory)
       auto grads = [&](int t) -> bool {
-        if (!mbar_wait(bar(L::B_DSFULL), t & 1, ctl)) return false;
-        if (a.write_dq && !mbar_wait(bar(L::B_DQEMPTY), (t & 1) ^ 1, ctl)) return false;
+        if (!mbar_wait_polled(bar(L::B_DSFULL), t & 1, ctl)) return false;
+        if (a.write_dq && !mbar_wait_polled(bar(L::B_DQEMPTY), (t & 1) ^ 1, ctl)) return false;
         tc_fence_after();
         const uint32_t qg = sb + L::oQg + (t & 1) * L::kQg;
 #pragma unroll
@@ -276,15 +197,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mma_bf16_ss(d, sdesc_sw128(ks + o, 16, 1024), sdesc_sw128(qs + o, 16, 1024), id_s, kk > 0);
         }
       };
-      bool ok = n > 0 && mbar_wait(bar(L::B_KFULL), 0, ctl);
+      bool ok = n > 0 && mbar_wait_polled(bar(L::B_KFULL), 0, ctl);
       for (int i = 0; ok && i < n; ++i) {
-        if (!mbar_wait(bar(L::B_SFREE), (i & 1) ^ 1, ctl)) break;
-        if (!mbar_wait(bar(L::B_QOFULL), i & 1, ctl)) break;
+        if (!mbar_wait_polled(bar(L::B_SFREE), (i & 1) ^ 1, ctl)) break;
+        if (!mbar_wait_polled(bar(L::B_QOFULL), i & 1, ctl)) break;
         tc_fence_after();
         // the other side first: its single Q buffer is released as early as possible
         s_product(kP2 ? 1 : 2, sb + L::oQo);
         mma_commit(bar(L::B_QOEMPTY));
-        if (!mbar_wait(bar(L::B_QGFULL0 + (i & 1)), (i >> 1) & 1, ctl)) break;
+        if (!mbar_wait_polled(bar(L::B_QGFULL0 + (i & 1)), (i >> 1) & 1, ctl)) break;
         tc_fence_after();
         s_product(kP2 ? 2 : 1, sb + L::oQg + (i & 1) * L::kQg);
         mma_commit(bar(L::B_SFULL));
@@ -529,7 +450,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       int issued = 0;
       for (int j = 0; j < nkt; ++j) {
         const int s = j & 1;
-        if (!mbar_wait(bar(L::B_KEMPTY0 + s), ((j >> 1) & 1) ^ 1, ctl)) break;
+        if (!mbar_wait_polled(bar(L::B_KEMPTY0 + s), ((j >> 1) & 1) ^ 1, ctl)) break;
         mbar_arrive_expect_tx(bar(L::B_KFULL0 + s), L::kStage);
         const uint32_t st = sb + L::oK + s * L::kStage;
 #pragma unroll
@@ -552,7 +473,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       constexpr uint32_t id_s = idesc_bf16(128, 128, 0, 0);
       constexpr uint32_t id_dq = idesc_bf16(128, DG, 0, 1);  // A = dS K-major, B = K_g N-major
       auto dq_product = [&](int t) -> bool {
-        if (!mbar_wait(bar(L::B_DSFULL), t & 1, ctl)) return false;
+        if (!mbar_wait_polled(bar(L::B_DSFULL), t & 1, ctl)) return false;
         tc_fence_after();
         const uint32_t kg = sb + L::oK + (t & 1) * L::kStage + (kP2 ? L::kK1 : 0);
 #pragma unroll
@@ -565,11 +486,11 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         mma_commit(bar(L::B_KEMPTY0 + (t & 1)));
         return true;
       };
-      bool ok = mbar_wait(bar(L::B_QFULL), 0, ctl);
+      bool ok = mbar_wait_polled(bar(L::B_QFULL), 0, ctl);
       for (int j = 0; ok && j < nkt; ++j) {
         const int s = j & 1;
-        if (!mbar_wait(bar(L::B_KFULL0 + s), (j >> 1) & 1, ctl)) break;
-        if (!mbar_wait(bar(L::B_SFREE), (j & 1) ^ 1, ctl)) break;
+        if (!mbar_wait_polled(bar(L::B_KFULL0 + s), (j >> 1) & 1, ctl)) break;
+        if (!mbar_wait_polled(bar(L::B_SFREE), (j & 1) ^ 1, ctl)) break;
         tc_fence_after();
         const uint32_t k1s = sb + L::oK + s * L::kStage, k2s = k1s + L::kK1;
 #pragma unroll

@@ -115,12 +115,25 @@ struct Ctl {
   int* status;          // device status word (global)
 };
 
-// Waits for the phase of `bar` with parity `parity` to complete.  Returns
-// false (without waiting further) once any thread of the CTA has aborted;
-// after STREAMKL_WAIT_LIMIT_NS it aborts the CTA and reports a timeout.
-static __device__ __noinline__ bool mbar_wait_limit(uint32_t bar, uint32_t parity, Ctl ctl,
-                                                    uint64_t limit_ns) {
-  if (mbar_try(bar, parity)) return true;
+// Non-blocking probe of the phase with parity `parity`.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Slow path of the bounded wait (kept out of line): polls with try_wait
+// until the phase completes, another thread of the CTA aborts, or
+// `limit_ns` of %globaltimer pass -- then it aborts the CTA and reports a
+// timeout in the status word.
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, Ctl ctl,
+                                                   uint64_t limit_ns) {
   const uint64_t t0 = globaltimer();
   while (true) {
     if (mbar_try(bar, parity)) return true;
@@ -133,8 +146,24 @@ static __device__ __noinline__ bool mbar_wait_limit(uint32_t bar, uint32_t parit
   }
 }
 
-static __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, Ctl ctl) {
+// Waits for the phase of `bar` with parity `parity` to complete.  Returns
+// false (without waiting further) once any thread of the CTA has aborted;
+// after `limit_ns` it aborts the CTA and reports a timeout.  A phase that is
+// already complete costs one inline test.
+__device__ __forceinline__ bool mbar_wait_limit(uint32_t bar, uint32_t parity, Ctl ctl, uint64_t limit_ns) {
+  if (mbar_test(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, ctl, limit_ns);
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, Ctl ctl) {
   return mbar_wait_limit(bar, parity, ctl, STREAMKL_WAIT_LIMIT_NS);
+}
+
+// The same bounded wait without the inline probe: a call straight into the
+// polling loop.  Timed faster for the backward's single-thread roles (the
+// MMA issuer above all), whose barriers are rarely complete on arrival.
+__device__ __forceinline__ bool mbar_wait_polled(uint32_t bar, uint32_t parity, Ctl ctl) {
+  return mbar_wait_slow(bar, parity, ctl, STREAMKL_WAIT_LIMIT_NS);
 }
 
 // Bounded wait that ignores the abort flag: used on the way out to let copies

@@ -268,6 +268,24 @@ def run_mine(args, rank, world, local):
     h2d = sum(t.numel() * t.element_size() for t in host) + dkl_h.numel() * 4
     d2h = kl_h.numel() * 4
 
+    # mode P1 backward timed on its own (outside the step): the other gradient side, d1-wide
+    dq1 = torch.empty(B, H, N, w.d1, device="cuda")
+    dk1 = torch.empty(B, H, w.NK, w.d1, device="cuda")
+    free0 = torch.cuda.mem_get_info()[0]
+    p1_ms = []
+    for k in range(4):
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        skl.streamkl_bwd(*dev, w.scale, w.causal, kl, l1, l2, dkl, skl.STREAMKL_GRAD_P1, False, dq1, dk1)
+        b_.record(stream)
+        torch.cuda.synchronize()
+        if k > 0:  # the first is warm-up
+            p1_ms.append(a.elapsed_time(b_))
+    p1_ms = float(np.median(p1_ms))
+    # the library allocates nothing: device memory free before and after the calls must agree
+    extra_bytes = free0 - torch.cuda.mem_get_info()[0]
+    f_p1 = (2 * (w.d1 + w.d2) + 4 * w.d1) * w.pairs
+
     rate = ex2_rate(skl)
     burst, sustained, _hbm, src = peaks()
     pairs = w.pairs
@@ -297,6 +315,9 @@ def run_mine(args, rank, world, local):
                        "l2": "inputs (2.15 GB) larger than L2, no flush"},
             "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
             "fwd_roofline_frac": t_fwd / (fwd_ms * 1e-3), "bwd_roofline_frac": t_bwd / (bwd_ms * 1e-3),
+            "bwd_p1_ms": p1_ms, "bwd_p1_tflops": f_p1 / (p1_ms * 1e-3) / 1e12,
+            "bwd_p1_roofline_frac": max(f_p1 / (sustained * 1e12), pairs / rate) / (p1_ms * 1e-3),
+            "extra_device_bytes": extra_bytes,
             "ex2_per_s": rate,
             "roofline": {"bound": "tensor", "achieved": bwd_tf if dom == "bwd" else fwd_tf,
                          "peak": sustained, "unit": "TFLOP/s",
