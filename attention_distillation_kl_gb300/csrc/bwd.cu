@@ -171,19 +171,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
           const uint32_t ao = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
-          mma_bf16_ss(t_dk, sdesc_sw128(sb + L::oDS + ao, 16, 1024),
+          mma_bf16_ss(1u, t_dk, sdesc_sw128(sb + L::oDS + ao, 16, 1024),
                       sdesc_sw128(qg + kk * 2048, kTile * 128, 1024), id_dk, (t > 0 || kk > 0) ? 1u : 0u);
         }
         // Q_g(t) is free once dK has read it: its reload starts before dQ runs
-        mma_commit(bar(L::B_QGEMPTY0 + (t & 1)));
+        mma_commit(1u, bar(L::B_QGEMPTY0 + (t & 1)));
         if (a.write_dq) {
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_bf16_ss(t_dq, sdesc_sw128(sb + L::oDS + kk * 2048, kTile * 128, 1024),
+            mma_bf16_ss(1u, t_dq, sdesc_sw128(sb + L::oDS + kk * 2048, kTile * 128, 1024),
                         sdesc_sw128(sb + oKg + kk * 2048, kTile * 128, 1024), id_dq, kk > 0 ? 1u : 0u);
         }
-        mma_commit(bar(L::B_DSEMPTY));
-        if (a.write_dq) mma_commit(bar(L::B_DQFULL));
+        mma_commit(1u, bar(L::B_DSEMPTY));
+        if (a.write_dq) mma_commit(1u, bar(L::B_DQFULL));
         return true;
       };
       // S^T of one side for query tile i: K (A, K-major) x Q tile (B, K-major)
@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < steps; ++kk) {
           const uint32_t o = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
-          mma_bf16_ss(d, sdesc_sw128(ks + o, 16, 1024), sdesc_sw128(qs + o, 16, 1024), id_s, kk > 0);
+          mma_bf16_ss(1u, d, sdesc_sw128(ks + o, 16, 1024), sdesc_sw128(qs + o, 16, 1024), id_s, kk > 0);
         }
       };
       bool ok = n > 0 && mbar_wait_polled(bar(L::B_KFULL), 0, ctl);
@@ -204,18 +204,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_after();
         // the other side first: its single Q buffer is released as early as possible
         s_product(kP2 ? 1 : 2, sb + L::oQo);
-        mma_commit(bar(L::B_QOEMPTY));
+        mma_commit(1u, bar(L::B_QOEMPTY));
         if (!mbar_wait_polled(bar(L::B_QGFULL0 + (i & 1)), (i >> 1) & 1, ctl)) break;
         tc_fence_after();
         s_product(kP2 ? 2 : 1, sb + L::oQg + (i & 1) * L::kQg);
-        mma_commit(bar(L::B_SFULL));
+        mma_commit(1u, bar(L::B_SFULL));
         if (i > 0 && !grads(i - 1)) {
           ok = false;
           break;
         }
       }
-      if (ok && n > 0 && !*abort_flag && grads(n - 1)) mma_commit(bar(L::B_DKFULL));
-      mma_commit(bar(L::B_DONE));
+      if (ok && n > 0 && !*abort_flag && grads(n - 1)) mma_commit(1u, bar(L::B_DKFULL));
+      mma_commit(1u, bar(L::B_DONE));
       mbar_drain(bar(L::B_DONE), 0, 1000000000ull);
     }
   } else if (warp < 8) {
@@ -479,11 +479,11 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
           const uint32_t ao = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
-          mma_bf16_ss(t_dq, sdesc_sw128(sb + L::oDS + ao, 16, 1024),
+          mma_bf16_ss(1u, t_dq, sdesc_sw128(sb + L::oDS + ao, 16, 1024),
                       sdesc_sw128(kg + kk * 2048, kTile * 128, 1024), id_dq, (t > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(bar(L::B_DSEMPTY));
-        mma_commit(bar(L::B_KEMPTY0 + (t & 1)));
+        mma_commit(1u, bar(L::B_DSEMPTY));
+        mma_commit(1u, bar(L::B_KEMPTY0 + (t & 1)));
         return true;
       };
       bool ok = mbar_wait_polled(bar(L::B_QFULL), 0, ctl);
@@ -496,23 +496,23 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D1 / 16; ++kk) {
           const uint32_t o = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
-          mma_bf16_ss(t_s1, sdesc_sw128(sb + L::oQ1 + o, 16, 1024), sdesc_sw128(k1s + o, 16, 1024), id_s,
+          mma_bf16_ss(1u, t_s1, sdesc_sw128(sb + L::oQ1 + o, 16, 1024), sdesc_sw128(k1s + o, 16, 1024), id_s,
                       kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < D2 / 16; ++kk) {
           const uint32_t o = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
-          mma_bf16_ss(t_s2, sdesc_sw128(sb + L::oQ2 + o, 16, 1024), sdesc_sw128(k2s + o, 16, 1024), id_s,
+          mma_bf16_ss(1u, t_s2, sdesc_sw128(sb + L::oQ2 + o, 16, 1024), sdesc_sw128(k2s + o, 16, 1024), id_s,
                       kk > 0);
         }
-        mma_commit(bar(L::B_SFULL));
+        mma_commit(1u, bar(L::B_SFULL));
         if (j > 0 && !dq_product(j - 1)) {
           ok = false;
           break;
         }
       }
-      if (ok && nkt > 0 && !*abort_flag && dq_product(nkt - 1)) mma_commit(bar(L::B_DQFULL));
-      mma_commit(bar(L::B_DONE));
+      if (ok && nkt > 0 && !*abort_flag && dq_product(nkt - 1)) mma_commit(1u, bar(L::B_DQFULL));
+      mma_commit(1u, bar(L::B_DONE));
       mbar_drain(bar(L::B_DONE), 0, 1000000000ull);
     }
   } else {

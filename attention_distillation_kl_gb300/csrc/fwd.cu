@@ -13,11 +13,15 @@
 //   warp 9      TMEM owner and MMA issuer: S1 = Q1 K1_j^T and S2 = Q2 K2_j^T
 //               (tcgen05, M = N = 128, bf16 -> fp32) into one of two TMEM
 //               buffers of 256 columns, so tile j+1 is multiplied while the
-//               statistics of tile j are reduced
+//               statistics of tile j are reduced.  The whole warp runs the
+//               loop and one elected lane issues (see elect_one).
 //   warps 0-7   statistics: thread = query row (TMEM lane); warps 0-3 take
 //               key columns 0-63 of every tile, warps 4-7 columns 64-127, and
 //               the two partial states are merged at the end with the same
-//               algebra as the key-split reduce.
+//               algebra as the key-split reduce.  (Four warpgroups of 32
+//               columns each were timed slower: the statistics loop is close
+//               to the one-instruction-per-cycle issue limit, and more warps
+//               only add per-tile overhead.)
 // With num_splits > 1 (article section "GPU kernel engineering", split-K) a
 // CTA covers only its share of the key tiles and writes (m1, l1, acc, m2, l2)
 // instead of the final values; splitk_reduce_kernel merges them.
@@ -26,7 +30,15 @@
 
 namespace skl {
 
-constexpr int kFwdThreads = 320;
+// Statistics warpgroups: each takes kTile / kStatWGs key columns of every
+// tile (32-column chunks), so every SM sub-partition runs kStatWGs warps
+// of row statistics; then one producer warp and one MMA warp.
+constexpr int kStatWGs = 2;
+constexpr int kStatWarps = 4 * kStatWGs;
+constexpr int kColsPerWG = kTile / kStatWGs;
+constexpr int kProdWarp = kStatWarps, kMmaWarp = kStatWarps + 1;
+constexpr int kFwdThreads = 32 * (kStatWarps + 2);
+static_assert(kColsPerWG % 32 == 0, "whole 32-column chunks per warpgroup");
 
 template <int D1, int D2>
 struct FwdLayout {
@@ -41,7 +53,7 @@ struct FwdLayout {
   static constexpr int kNumBars = 1 + 2 * kStages + 4 + 1;
   static constexpr uint32_t oMisc = oBar + kNumBars * 8;  // tmem base, abort flag
   static constexpr uint32_t oMerge = (oMisc + 8 + 15) / 16 * 16;
-  static constexpr uint32_t kBytes = oMerge + kTile * 5 * 4;
+  static constexpr uint32_t kBytes = oMerge + (kStatWGs - 1) * kTile * 5 * 4;
   static constexpr uint32_t kAlloc = kBytes + 1024;
   static_assert(kStages >= 2, "shared memory ring needs two stages");
   static_assert(kAlloc <= 232448, "over the 227 KB shared memory limit");
@@ -139,13 +151,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar_sfull(b), 1);
-      mbar_init(bar_sempty(b), 8);
+      mbar_init(bar_sempty(b), kStatWarps);
     }
     mbar_init(bar_done, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 9) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
@@ -154,7 +166,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 8) {
+  if (warp == kProdWarp) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0 && nkt > 0) {
       tma_prefetch_desc(&tq1);
@@ -190,41 +202,41 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           mbar_drain(bar_kfull(j % L::kStages), (j / L::kStages) & 1, 200000000ull);
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(128, 128, 0, 0);
-      if (nkt > 0 && mbar_wait(bar_q, 0, ctl)) {
-        for (int j = 0; j < nkt; ++j) {
-          const int s = j % L::kStages;
-          const uint32_t ph = (j / L::kStages) & 1;
-          const int b = j & 1;
-          const uint32_t bph = (j >> 1) & 1;
-          if (!mbar_wait(bar_kfull(s), ph, ctl)) break;
-          if (!mbar_wait(bar_sempty(b), bph ^ 1, ctl)) break;
-          tc_fence_after();
-          const uint32_t d1 = tmem + b * 256, d2 = d1 + 128;
-          const uint32_t k1s = sb + L::oK + s * L::kStage, k2s = k1s + L::kK1;
+    // (the whole warp runs the loop; the elected lane issues)
+    const uint32_t leader = elect_one();
+    constexpr uint32_t idesc = idesc_bf16(128, 128, 0, 0);
+    if (nkt > 0 && mbar_wait_warp(bar_q, 0, ctl)) {
+      for (int j = 0; j < nkt; ++j) {
+        const int s = j % L::kStages;
+        const uint32_t ph = (j / L::kStages) & 1;
+        const int b = j & 1;
+        const uint32_t bph = (j >> 1) & 1;
+        if (!mbar_wait_warp(bar_kfull(s), ph, ctl)) break;
+        if (!mbar_wait_warp(bar_sempty(b), bph ^ 1, ctl)) break;
+        tc_fence_after();
+        const uint32_t d1 = tmem + b * 256, d2 = d1 + 128;
+        const uint32_t k1s = sb + L::oK + s * L::kStage, k2s = k1s + L::kK1;
 #pragma unroll
-          for (int kk = 0; kk < D1 / 16; ++kk) {
-            const uint32_t o = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
-            mma_bf16_ss(d1, sdesc_sw128(sb + L::oQ1 + o, 16, 1024), sdesc_sw128(k1s + o, 16, 1024),
-                        idesc, kk > 0);
-          }
-#pragma unroll
-          for (int kk = 0; kk < D2 / 16; ++kk) {
-            const uint32_t o = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
-            mma_bf16_ss(d2, sdesc_sw128(sb + L::oQ2 + o, 16, 1024), sdesc_sw128(k2s + o, 16, 1024),
-                        idesc, kk > 0);
-          }
-          mma_commit(bar_kempty(s));
-          mma_commit(bar_sfull(b));
+        for (int kk = 0; kk < D1 / 16; ++kk) {
+          const uint32_t o = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
+          mma_bf16_ss(leader, d1, sdesc_sw128(sb + L::oQ1 + o, 16, 1024), sdesc_sw128(k1s + o, 16, 1024),
+                      idesc, kk > 0);
         }
+#pragma unroll
+        for (int kk = 0; kk < D2 / 16; ++kk) {
+          const uint32_t o = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
+          mma_bf16_ss(leader, d2, sdesc_sw128(sb + L::oQ2 + o, 16, 1024), sdesc_sw128(k2s + o, 16, 1024),
+                      idesc, kk > 0);
+        }
+        mma_commit(leader, bar_kempty(s));
+        mma_commit(leader, bar_sfull(b));
       }
-      // every MMA this thread issued has finished before TMEM is released
-      mma_commit(bar_done);
-      mbar_drain(bar_done, 0, 1000000000ull);
     }
+    // every MMA this warp issued has finished before TMEM is released
+    mma_commit(leader, bar_done);
+    mbar_drain(bar_done, 0, 1000000000ull);
   } else {
     // ---------------------------------------------------------------- statistics
     const int wg = warp >> 2;
@@ -242,12 +254,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const int k0 = (kt_lo + j) * kTile;
       const bool need_mask = (k0 + kTile > a.NK) || (a.causal && k0 + kTile - 1 > q0 + off);
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        const int col = wg * 64 + ch * 32;
+      for (int ch = 0; ch < kColsPerWG / 32; ++ch) {
+        const int col = wg * kColsPerWG + ch * 32;
         uint32_t x1[32], x2[32];
         const uint32_t t = tmem + lane_off + uint32_t(b * 256 + col);
         tmem_ld2x32(t, t + 128, x1, x2);
-        if (ch == 1) {
+        if (ch == kColsPerWG / 32 - 1) {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar_sempty(b));
@@ -258,25 +270,35 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           fold_chunk<false>(st, x1, x2, c, 0);
       }
     }
-    // merge the two column halves of every row (warps 4-7 -> warps 0-3)
+    // merge the column shares of every row (warpgroups 1.. -> warpgroup 0)
+    // with the same algebra as the key-split reduce
     float* mg = reinterpret_cast<float*>(smem + L::oMerge);
-    if (wg == 1) {
-      mg[row * 5 + 0] = st.m1;
-      mg[row * 5 + 1] = st.l1;
-      mg[row * 5 + 2] = st.acc;
-      mg[row * 5 + 3] = st.m2;
-      mg[row * 5 + 4] = st.l2;
+    if (wg > 0) {
+      float* o = mg + (wg - 1) * kTile * 5 + row * 5;
+      o[0] = st.m1;
+      o[1] = st.l1;
+      o[2] = st.acc;
+      o[3] = st.m2;
+      o[4] = st.l2;
     }
-    named_bar_sync(1, 256);
+    named_bar_sync(1, 32 * kStatWarps);
     if (wg == 0 && !*abort_flag && grow < a.NQ) {
-      const float bm1 = mg[row * 5 + 0], bl1 = mg[row * 5 + 1], bacc = mg[row * 5 + 2];
-      const float bm2 = mg[row * 5 + 3], bl2 = mg[row * 5 + 4];
-      const float M1 = fmaxf(st.m1, bm1), M2 = fmaxf(st.m2, bm2);
-      const float wa1 = ex2((st.m1 - M1) * c), wb1 = ex2((bm1 - M1) * c);
-      const float wa2 = ex2((st.m2 - M2) * c), wb2 = ex2((bm2 - M2) * c);
-      const float L1 = st.l1 * wa1 + bl1 * wb1;
-      const float A = st.acc * wa1 + bacc * wb1;
-      const float L2 = st.l2 * wa2 + bl2 * wb2;
+      float M1 = st.m1, M2 = st.m2;
+#pragma unroll
+      for (int w = 0; w < kStatWGs - 1; ++w) {
+        M1 = fmaxf(M1, mg[w * kTile * 5 + row * 5 + 0]);
+        M2 = fmaxf(M2, mg[w * kTile * 5 + row * 5 + 3]);
+      }
+      const float e1 = ex2((st.m1 - M1) * c), e2 = ex2((st.m2 - M2) * c);
+      float L1 = st.l1 * e1, A = st.acc * e1, L2 = st.l2 * e2;
+#pragma unroll
+      for (int w = 0; w < kStatWGs - 1; ++w) {
+        const float* o = mg + w * kTile * 5 + row * 5;
+        const float f1 = ex2((o[0] - M1) * c), f2 = ex2((o[3] - M2) * c);
+        L1 = fmaf(o[1], f1, L1);
+        A = fmaf(o[2], f1, A);
+        L2 = fmaf(o[4], f2, L2);
+      }
       const size_t rows = size_t(a.BH) * a.NQ;
       const size_t idx = size_t(bh) * a.NQ + grow;
       if (a.partial != nullptr) {
@@ -298,7 +320,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
