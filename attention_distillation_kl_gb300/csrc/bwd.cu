@@ -15,23 +15,24 @@
 //   warp 12    TMA: K1, K2 once; per query tile Q_o (single buffer) and Q_g
 //              (double buffer; it is read again by the dK product)
 //   warp 13    TMEM owner, MMA issuer:
-//                S1^T = K1 Q1^T, S2^T = K2 Q2^T   (M = keys, N = queries)
+//                S1 = Q1 K1^T, S2 = Q2 K2^T      (M = queries, N = keys)
 //                dK  += dS^T Q_g                   (accumulates in TMEM)
 //                dQ   = dS K_g                     (per query tile)
 //              with S of tile i+1 issued before the gradient products of
 //              tile i, so the tensor pipe stays busy while dS is formed
-//   warps 0-7  thread = key row: P1/P2 and dS from S^T (TMEM) and the
-//              per-query LSE/dKL/KL of the tile; warps 0-3 take query
-//              columns 0-63, warps 4-7 columns 64-127 (two warps per SM
-//              sub-partition, and S^T is released after half the work).  dS
-//              goes to shared memory as bf16 in the 128-byte-swizzled layout
-//              both products read: K-major A for dK, M-major A for dQ
+//   warps 0-7  thread = query row: P1/P2 and dS from S (TMEM) with the
+//              row's LSE/dKL/KL in registers (loaded one tile ahead);
+//              warps 0-3 take key columns 0-63, warps 4-7 columns 64-127
+//              (two warps per SM sub-partition, and S is released after
+//              half the work).  dS goes to shared memory as bf16 rows in the
+//              128-byte-swizzled layout both products read: K-major A for
+//              dQ, M-major A (dS^T) for dK
 //   warps 8-11 dQ tile: TMEM -> registers (scaled) -> 32 x 16 fp32 boxes in
 //              swizzled shared memory (three per warp, round robin) -> TMA
 //              bulk tensor reduce-add into global dQ (rows past NQ are
 //              clipped by the tensor map); finally dK (each CTA owns its
 //              keys: plain stores)
-// TMEM: S1^T [0,128), S2^T [128,256), dK [256, 256+dg), dQ [384, 384+dg).
+// TMEM: S1 [0,128), S2 [128,256), dK [256, 256+dg), dQ [384, 384+dg).
 //
 // dQ-only kernel (deterministic two-pass mode): one CTA per query tile walks
 // the key tiles, thread = query row, dQ accumulates in TMEM and is stored
@@ -53,11 +54,10 @@ struct BwdLayout {
   static constexpr uint32_t kQo = kTile * DO * 2, kQg = kTile * DG * 2;
   static constexpr uint32_t oDS = 0, oK1 = kDS, oK2 = oK1 + kK1, oQo = oK2 + kK2, oQg = oQo + kQo;
   static constexpr uint32_t oStage = oQg + 2 * kQg;  // dQ staging: 4 warps x 3 x [32 rows][64 B]
-  static constexpr uint32_t oPar = oStage + 4 * 3 * 2048;  // 2 warpgroups x 2 buffers x 3 x 128 floats
-  static constexpr uint32_t oBar = oPar + 2 * 2 * 3 * kTile * 4;
+  static constexpr uint32_t oBar = oStage + 4 * 3 * 2048;
   enum {
     B_KFULL, B_QOFULL, B_QOEMPTY, B_QGFULL0, B_QGFULL1, B_QGEMPTY0, B_QGEMPTY1, B_SFULL, B_SFREE,
-    B_DSFULL, B_DSEMPTY, B_DQFULL, B_DQEMPTY, B_DKFULL, B_PAR0, B_PAR1, B_PAR2, B_PAR3, B_DONE, kNumBars
+    B_DSFULL, B_DSEMPTY, B_DQFULL, B_DQEMPTY, B_DKFULL, B_DONE, kNumBars
   };
   static constexpr uint32_t oMisc = oBar + kNumBars * 8;
   static constexpr uint32_t kBytes = oMisc + 16;
@@ -100,7 +100,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       uint32_t count = 1;  // TMA transaction barriers and tcgen05.commit targets
       if (b == L::B_SFREE || b == L::B_DSFULL) count = 8;  // one per dS warp
       if (b == L::B_DQEMPTY) count = 4;                    // one per epilogue warp
-      if (b >= L::B_PAR0 && b <= L::B_PAR3) count = 128;   // one per thread of a dS warpgroup
       mbar_init(bar(b), count);
     }
     *abort_flag = 0;
@@ -159,8 +158,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16(128, 128, 0, 0);
-      constexpr uint32_t id_dk = idesc_bf16(128, DG, 0, 1);  // A = dS^T K-major, B = Q_g N-major
-      constexpr uint32_t id_dq = idesc_bf16(128, DG, 1, 1);  // A = dS M-major,  B = K_g N-major
+      constexpr uint32_t id_dk = idesc_bf16(128, DG, 1, 1);  // A = dS^T M-major, B = Q_g N-major
+      constexpr uint32_t id_dq = idesc_bf16(128, DG, 0, 1);  // A = dS K-major,   B = K_g N-major
       const uint32_t oKg = kP2 ? L::oK2 : L::oK1;
       // gradient products of query tile t (dS(t) in shared memory)
       auto grads = [&](int t) -> bool {
@@ -169,24 +168,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_after();
         const uint32_t qg = sb + L::oQg + (t & 1) * L::kQg;
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint32_t ao = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
-          mma_bf16_ss(1u, t_dk, sdesc_sw128(sb + L::oDS + ao, 16, 1024),
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_bf16_ss(1u, t_dk, sdesc_sw128(sb + L::oDS + kk * 2048, kTile * 128, 1024),
                       sdesc_sw128(qg + kk * 2048, kTile * 128, 1024), id_dk, (t > 0 || kk > 0) ? 1u : 0u);
-        }
         // Q_g(t) is free once dK has read it: its reload starts before dQ runs
         mma_commit(1u, bar(L::B_QGEMPTY0 + (t & 1)));
         if (a.write_dq) {
 #pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_bf16_ss(1u, t_dq, sdesc_sw128(sb + L::oDS + kk * 2048, kTile * 128, 1024),
+          for (int kk = 0; kk < kTile / 16; ++kk) {
+            const uint32_t ao = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
+            mma_bf16_ss(1u, t_dq, sdesc_sw128(sb + L::oDS + ao, 16, 1024),
                         sdesc_sw128(sb + oKg + kk * 2048, kTile * 128, 1024), id_dq, kk > 0 ? 1u : 0u);
+          }
         }
         mma_commit(1u, bar(L::B_DSEMPTY));
         if (a.write_dq) mma_commit(1u, bar(L::B_DQFULL));
         return true;
       };
-      // S^T of one side for query tile i: K (A, K-major) x Q tile (B, K-major)
+      // S of one side for query tile i: Q tile (A, K-major) x K (B, K-major)
       auto s_product = [&](int side, uint32_t qs) {
         const uint32_t ks = sb + (side == 1 ? L::oK1 : L::oK2);
         const uint32_t d = side == 1 ? t_s1 : t_s2;
@@ -194,7 +193,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < steps; ++kk) {
           const uint32_t o = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
-          mma_bf16_ss(1u, d, sdesc_sw128(ks + o, 16, 1024), sdesc_sw128(qs + o, 16, 1024), id_s, kk > 0);
+          mma_bf16_ss(1u, d, sdesc_sw128(qs + o, 16, 1024), sdesc_sw128(ks + o, 16, 1024), id_s, kk > 0);
         }
       };
       bool ok = n > 0 && mbar_wait_polled(bar(L::B_KFULL), 0, ctl);
@@ -219,44 +218,37 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_drain(bar(L::B_DONE), 0, 1000000000ull);
     }
   } else if (warp < 8) {
-    // ---------------------------------------------------------------- dS (thread = key row)
-    // warpgroup wg takes query columns [64 wg, 64 wg + 64) of every tile
+    // ---------------------------------------------------------------- dS (thread = query row)
+    // warpgroup wg takes key columns [64 wg, 64 wg + 64) of every tile
     const int wg = warp >> 2;
     const int row = (warp & 3) * 32 + lane;
-    const int kj = k0 + row;
-    const float c = a.scale * kLog2e;
     const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
-    const bool key_ok = kj < a.NK;
-    float* par = reinterpret_cast<float*>(smem + L::oPar) + wg * 2 * 3 * kTile;
+    const uint64_t C = f2(a.scale * kLog2e, a.scale * kLog2e), SS = f2(a.scale, a.scale);
+    // per-row parameters of query tile i (see ds_chunk_row)
+    auto params = [&](int i, float& na, float& nb, float& ws) {
+      const int qi = (qt_lo + i) * kTile + row;
+      na = -INFINITY;
+      nb = kP2 ? -INFINITY : 0.f;
+      ws = 0.f;
+      if (qi < a.NQ) {
+        const size_t idx = size_t(bh) * a.NQ + qi;
+        const float l1 = a.lse1[idx];
+        na = -l1 * kLog2e;
+        ws = a.scale * a.dkl[idx];
+        nb = kP2 ? -a.lse2[idx] * kLog2e : -(l1 - a.lse2[idx] + a.kl[idx]);
+      }
+    };
+    float na, nb, ws;
+    if (n > 0) params(0, na, nb, ws);
     for (int i = 0; i < n; ++i) {
       const int q0 = (qt_lo + i) * kTile;
-      const int pb = i & 1;
-      const uint32_t par_bar = bar(L::B_PAR0 + 2 * wg + pb);
-      // per-query parameters of this tile (each warpgroup keeps its own copy)
-      {
-        float* P = par + pb * 3 * kTile;
-        const int qi = q0 + row;
-        float va = -INFINITY, vb = 0.f, vw = 0.f;
-        if (qi < a.NQ) {
-          const size_t idx = size_t(bh) * a.NQ + qi;
-          const float l1 = a.lse1[idx];
-          va = -l1 * kLog2e;
-          vw = a.scale * a.dkl[idx];  // s folded into dS: dK and dQ come out scaled
-          vb = kP2 ? -a.lse2[idx] * kLog2e : -(l1 - a.lse2[idx] + a.kl[idx]);
-        } else if (kP2) {
-          vb = -INFINITY;
-        }
-        P[row] = va;
-        P[kTile + row] = vb;
-        P[2 * kTile + row] = vw;
-        mbar_arrive(par_bar);
-      }
-      if (!mbar_wait_warp(par_bar, (i >> 1) & 1, ctl)) break;
+      const uint64_t NA = f2(na, na), NB = f2(nb, nb), WW = f2(ws, ws);
+      if (i + 1 < n) params(i + 1, na, nb, ws);  // used next tile: the loads overlap this one
       if (!mbar_wait_warp(bar(L::B_SFULL), i & 1, ctl)) break;
       tc_fence_after();
-      const float* P = par + pb * 3 * kTile;
+      // last visible key of this row, relative to the tile
+      const int lim = (a.causal ? min(q0 + row + off, a.NK - 1) : a.NK - 1) - k0;
       const bool need_mask = (k0 + kTile > a.NK) || (a.causal && q0 < k0 + kTile - 1 - off);
-      const int first_visible = !key_ok ? (1 << 30) : (a.causal ? kj - off - q0 : 0);
       uint32_t dsr[32];
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
@@ -269,10 +261,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (lane == 0) mbar_arrive(bar(L::B_SFREE));
         }
         if (need_mask)
-          ds_chunk<MODE, true>(x1, x2, P, P + kTile, P + 2 * kTile, c, a.scale, col, first_visible,
-                               dsr + ch * 16);
+          ds_chunk_row<MODE, true>(x1, x2, C, SS, NA, NB, WW, lim - col, dsr + ch * 16);
         else
-          ds_chunk<MODE, false>(x1, x2, P, P + kTile, P + 2 * kTile, c, a.scale, col, 0, dsr + ch * 16);
+          ds_chunk_row<MODE, false>(x1, x2, C, SS, NA, NB, WW, 0, dsr + ch * 16);
       }
       // the previous tile's products must be done reading dS before it is replaced
       if (!mbar_wait_warp(bar(L::B_DSEMPTY), (i & 1) ^ 1, ctl)) break;
@@ -548,28 +539,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(L::B_SFREE));
         }
-#pragma unroll
-        for (int k = 0; k < 32; k += 2) {
-          const uint64_t X1 = f2(__uint_as_float(x1[k]), __uint_as_float(x1[k + 1]));
-          const uint64_t X2 = f2(__uint_as_float(x2[k]), __uint_as_float(x2[k + 1]));
-          float ea, eb;
-          f2_split(f2_fma(X1, C, NA), ea, eb);
-          const uint64_t P1 = f2(ex2(ea), ex2(eb));
-          uint64_t D;
-          if (kP2) {
-            f2_split(f2_fma(X2, C, NB), ea, eb);
-            D = f2_mul(WW, f2_sub(f2(ex2(ea), ex2(eb)), P1));
-          } else {
-            D = f2_mul(f2_mul(WW, P1), f2_fma(f2_sub(X1, X2), SS, NB));
-          }
-          float da, db;
-          f2_split(D, da, db);
-          if (need_mask) {
-            if (ch * 32 + k > lim_rel) da = 0.f;
-            if (ch * 32 + k + 1 > lim_rel) db = 0.f;
-          }
-          dsr[ch * 16 + k / 2] = pack_bf16(da, db);
-        }
+        if (need_mask)
+          ds_chunk_row<MODE, true>(x1, x2, C, SS, NA, NB, WW, lim_rel - ch * 32, dsr + ch * 16);
+        else
+          ds_chunk_row<MODE, false>(x1, x2, C, SS, NA, NB, WW, 0, dsr + ch * 16);
       }
       if (!mbar_wait_warp(bar(L::B_DSEMPTY), (j & 1) ^ 1, ctl)) break;
       store_row_sw128(sb + L::oDS, row, dsr);

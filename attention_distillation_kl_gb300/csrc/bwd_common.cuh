@@ -41,49 +41,39 @@ __device__ __forceinline__ void store_half_row_sw128(uint32_t base, int r, int b
     st_shared_v4(rb + ((c ^ (r & 7)) << 4), v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
 }
 
-// dS for 32 consecutive query columns of one key row (thread), packed to
-// bf16 pairs.  pa/pb/pw: per-column parameters in shared memory:
-//   mode P2: pa = -LSE1 log2e, pb = -LSE2 log2e, pw = s dKL
-//   mode P1: pa = -LSE1 log2e, pb = -(LSE1 - LSE2 + KL), pw = s dKL
-// (the softmax scale s rides on dS, so dK = dS^T Q and dQ = dS K need no
-// further scaling)
-// Columns < first_visible (causal) or all columns when the key is past NK
-// (first_visible > 128) give 0.
+// dS for 32 consecutive key columns of one query row (thread), packed to
+// bf16 pairs.  Per-row parameters, each broadcast to both halves of a pair:
+//   mode P2: NA = -LSE1 log2e, NB = -LSE2 log2e, WW = s dKL
+//   mode P1: NA = -LSE1 log2e, NB = -(LSE1 - LSE2 + KL), WW = s dKL
+// with C = s log2e and SS = s (the softmax scale s rides on dS, so
+// dK = dS^T Q and dQ = dS K need no further scaling).  Columns k > lim_rel
+// (causal, or past NK) give 0.  A row past NQ has NA = -inf (and NB = -inf
+// in mode P2, WW = 0), so every product is an exact 0.
 template <int MODE, bool kMask>
-__device__ __forceinline__ void ds_chunk(const uint32_t (&x1u)[32], const uint32_t (&x2u)[32],
-                                         const float* pa, const float* pb, const float* pw, float c,
-                                         float s, int col0, int first_visible, uint32_t* out16) {
-  const uint64_t C = f2(c, c), S = f2(s, s);
+__device__ __forceinline__ void ds_chunk_row(const uint32_t (&x1u)[32], const uint32_t (&x2u)[32],
+                                             uint64_t C, uint64_t SS, uint64_t NA, uint64_t NB, uint64_t WW,
+                                             int lim_rel, uint32_t* out16) {
 #pragma unroll
-  for (int k = 0; k < 32; k += 4) {
-    const float4 A = *reinterpret_cast<const float4*>(pa + col0 + k);
-    const float4 Bv = *reinterpret_cast<const float4*>(pb + col0 + k);
-    const float4 W = *reinterpret_cast<const float4*>(pw + col0 + k);
-#pragma unroll
-    for (int e = 0; e < 4; e += 2) {
-      const uint64_t X1 = f2(__uint_as_float(x1u[k + e]), __uint_as_float(x1u[k + e + 1]));
-      const uint64_t X2 = f2(__uint_as_float(x2u[k + e]), __uint_as_float(x2u[k + e + 1]));
-      const uint64_t AA = e == 0 ? f2(A.x, A.y) : f2(A.z, A.w);
-      const uint64_t BB = e == 0 ? f2(Bv.x, Bv.y) : f2(Bv.z, Bv.w);
-      const uint64_t WW = e == 0 ? f2(W.x, W.y) : f2(W.z, W.w);
-      float ea, eb;
-      f2_split(f2_fma(X1, C, AA), ea, eb);
-      const uint64_t P1 = f2(ex2(ea), ex2(eb));
-      uint64_t D;
-      if (MODE == STREAMKL_GRAD_P2) {
-        f2_split(f2_fma(X2, C, BB), ea, eb);
-        D = f2_mul(WW, f2_sub(f2(ex2(ea), ex2(eb)), P1));
-      } else {
-        D = f2_mul(f2_mul(WW, P1), f2_fma(f2_sub(X1, X2), S, BB));
-      }
-      float da, db;
-      f2_split(D, da, db);
-      if (kMask) {
-        if (col0 + k + e < first_visible) da = 0.f;
-        if (col0 + k + e + 1 < first_visible) db = 0.f;
-      }
-      out16[(k + e) / 2] = pack_bf16(da, db);
+  for (int k = 0; k < 32; k += 2) {
+    const uint64_t X1 = f2(__uint_as_float(x1u[k]), __uint_as_float(x1u[k + 1]));
+    const uint64_t X2 = f2(__uint_as_float(x2u[k]), __uint_as_float(x2u[k + 1]));
+    float ea, eb;
+    f2_split(f2_fma(X1, C, NA), ea, eb);
+    const uint64_t P1 = f2(ex2(ea), ex2(eb));
+    uint64_t D;
+    if (MODE == STREAMKL_GRAD_P2) {
+      f2_split(f2_fma(X2, C, NB), ea, eb);
+      D = f2_mul(WW, f2_sub(f2(ex2(ea), ex2(eb)), P1));
+    } else {
+      D = f2_mul(f2_mul(WW, P1), f2_fma(f2_sub(X1, X2), SS, NB));
     }
+    float da, db;
+    f2_split(D, da, db);
+    if (kMask) {
+      if (k > lim_rel) da = 0.f;
+      if (k + 1 > lim_rel) db = 0.f;
+    }
+    out16[k / 2] = pack_bf16(da, db);
   }
 }
 

@@ -341,7 +341,6 @@ __device__ __forceinline__ void tmem_ld2x32(uint32_t ta, uint32_t tb, uint32_t (
       : "memory");
 }
 
-
 __device__ __forceinline__ void tmem_ld32(uint32_t ta, uint32_t (&a)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
