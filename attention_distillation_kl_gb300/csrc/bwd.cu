@@ -166,20 +166,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!mbar_wait_polled(bar(L::B_DSFULL), t & 1, ctl)) return false;
         if (a.write_dq && !mbar_wait_polled(bar(L::B_DQEMPTY), (t & 1) ^ 1, ctl)) return false;
         tc_fence_after();
-        const uint32_t qg = sb + L::oQg + (t & 1) * L::kQg;
+        const uint64_t dsm = sdesc_sw128(sb + L::oDS, kTile * 128, 1024);  // dS^T, M-major
+        const uint64_t qgn = sdesc_sw128(sb + L::oQg + (t & 1) * L::kQg, kTile * 128, 1024);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_bf16_ss(1u, t_dk, sdesc_sw128(sb + L::oDS + kk * 2048, kTile * 128, 1024),
-                      sdesc_sw128(qg + kk * 2048, kTile * 128, 1024), id_dk, (t > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16_ss(1u, t_dk, sdesc_add(dsm, kk * 2048), sdesc_add(qgn, kk * 2048), id_dk,
+                      (t > 0 || kk > 0) ? 1u : 0u);
         // Q_g(t) is free once dK has read it: its reload starts before dQ runs
         mma_commit(1u, bar(L::B_QGEMPTY0 + (t & 1)));
         if (a.write_dq) {
+          const uint64_t dsk = sdesc_sw128(sb + L::oDS, 16, 1024);  // dS, K-major
+          const uint64_t kgn = sdesc_sw128(sb + oKg, kTile * 128, 1024);
 #pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk) {
-            const uint32_t ao = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
-            mma_bf16_ss(1u, t_dq, sdesc_sw128(sb + L::oDS + ao, 16, 1024),
-                        sdesc_sw128(sb + oKg + kk * 2048, kTile * 128, 1024), id_dq, kk > 0 ? 1u : 0u);
-          }
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            mma_bf16_ss(1u, t_dq, sdesc_add(dsk, (kk >> 2) * (kTile * 128) + (kk & 3) * 32),
+                        sdesc_add(kgn, kk * 2048), id_dq, kk > 0 ? 1u : 0u);
         }
         mma_commit(1u, bar(L::B_DSEMPTY));
         if (a.write_dq) mma_commit(1u, bar(L::B_DQFULL));
@@ -190,10 +191,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t ks = sb + (side == 1 ? L::oK1 : L::oK2);
         const uint32_t d = side == 1 ? t_s1 : t_s2;
         const int steps = (side == 1 ? D1 : D2) / 16;
+        const uint64_t qd = sdesc_sw128(qs, 16, 1024), kd = sdesc_sw128(ks, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < steps; ++kk) {
           const uint32_t o = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
-          mma_bf16_ss(1u, d, sdesc_sw128(qs + o, 16, 1024), sdesc_sw128(ks + o, 16, 1024), id_s, kk > 0);
+          mma_bf16_ss(1u, d, sdesc_add(qd, o), sdesc_add(kd, o), id_s, kk > 0);
         }
       };
       bool ok = n > 0 && mbar_wait_polled(bar(L::B_KFULL), 0, ctl);

@@ -320,6 +320,11 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// The descriptor of the same operand `bytes` further on: the start address
+// field is the low 14 bits (address / 16), and shared-memory addresses stay
+// below 2^18, so a plain add never carries out of it.
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
+
 // Two 32-column loads (32 lanes x 32 bit, one row per thread) and the wait in
 // one statement, so no use of the registers can be scheduled before the wait.
 #define SKL_R8(a, o) "=r"(a[o + 0]), "=r"(a[o + 1]), "=r"(a[o + 2]), "=r"(a[o + 3]), \
