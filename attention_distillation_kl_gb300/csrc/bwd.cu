@@ -44,6 +44,7 @@
 namespace skl {
 
 constexpr int kBwdThreads = 448;
+constexpr int kDqBoxes = 4;  // dQ staging boxes per epilogue warp
 
 template <int D1, int D2, int MODE>
 struct BwdLayout {
@@ -53,8 +54,8 @@ struct BwdLayout {
   static constexpr uint32_t kK1 = kTile * D1 * 2, kK2 = kTile * D2 * 2;
   static constexpr uint32_t kQo = kTile * DO * 2, kQg = kTile * DG * 2;
   static constexpr uint32_t oDS = 0, oK1 = kDS, oK2 = oK1 + kK1, oQo = oK2 + kK2, oQg = oQo + kQo;
-  static constexpr uint32_t oStage = oQg + 2 * kQg;  // dQ staging: 4 warps x 3 x [32 rows][64 B]
-  static constexpr uint32_t oBar = oStage + 4 * 3 * 2048;
+  static constexpr uint32_t oStage = oQg + 2 * kQg;  // dQ staging: 4 warps x kDqBoxes x [32 rows][64 B]
+  static constexpr uint32_t oBar = oStage + 4 * kDqBoxes * 2048;
   enum {
     B_KFULL, B_QOFULL, B_QOEMPTY, B_QGFULL0, B_QGFULL1, B_QGEMPTY0, B_QGEMPTY1, B_SFULL, B_SFREE,
     B_DSFULL, B_DSEMPTY, B_DQFULL, B_DQEMPTY, B_DKFULL, B_DONE, kNumBars
@@ -280,10 +281,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int row = w4 * 32 + lane;
     const uint32_t lane_off = uint32_t(w4 * 32) << 16;
     if (a.write_dq) {
-      // Three 2 KB staging boxes per warp ([32 rows][16 fp32], 64-byte
+      // kDqBoxes 2 KB staging boxes per warp ([32 rows][16 fp32], 64-byte
       // swizzle: 16-byte chunk c of row r at chunk c ^ ((r / 2) % 4)), used
-      // round robin so up to three bulk reduce-adds are in flight.
-      const uint32_t stage = sb + L::oStage + w4 * (3 * 2048);
+      // round robin so up to kDqBoxes bulk reduce-adds are in flight.  The
+      // tile is read from TMEM 64 columns at a time; the second read
+      // releases the dQ accumulator before its boxes are staged, so the
+      // next dQ product does not wait for the reduce-adds.
+      const uint32_t stage = sb + L::oStage + w4 * (kDqBoxes * 2048);
       const uint32_t swz = (lane >> 1) & 3;
       int nred = 0;
       if (lane == 0) tma_prefetch_desc(&tdq);
@@ -292,28 +296,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_after();
         const int r0 = (qt_lo + i) * kTile + w4 * 32;  // first query row of this warp
 #pragma unroll
-        for (int ch = 0; ch < DG / 32; ++ch) {
-          uint32_t v[32];
-          tmem_ld32(t_dq + lane_off + ch * 32, v);
-          if (ch == DG / 32 - 1) {
+        for (int cp = 0; cp < DG / 64; ++cp) {
+          uint32_t v[2][32];
+          tmem_ld32(t_dq + lane_off + cp * 64, v[0]);
+          tmem_ld32(t_dq + lane_off + cp * 64 + 32, v[1]);
+          if (cp == DG / 64 - 1) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(L::B_DQEMPTY));
           }
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const uint32_t box = stage + (nred % 3) * 2048;
-            if (lane == 0) bulk_wait_read_le2();  // the box used three reduces ago has been read
+          for (int h = 0; h < 4; ++h) {
+            const uint32_t box = stage + (nred % kDqBoxes) * 2048;
+            // the box used kDqBoxes reduces ago has been read
+            if (lane == 0) bulk_wait_read_le<kDqBoxes - 1>();
             __syncwarp();
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-              const int e = h * 16 + 4 * c;
-              st_shared_v4(box + lane * 64 + ((c ^ swz) << 4), v[e], v[e + 1], v[e + 2], v[e + 3]);
+              const int e = (h & 1) * 16 + 4 * c;
+              st_shared_v4(box + lane * 64 + ((c ^ swz) << 4), v[h >> 1][e], v[h >> 1][e + 1], v[h >> 1][e + 2],
+                           v[h >> 1][e + 3]);
             }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0 && r0 < a.NQ) {  // a box starting past NQ has nothing to add
-              tma_reduce_add_3d(&tdq, box, ch * 32 + h * 16, r0, bh);
+              tma_reduce_add_3d(&tdq, box, cp * 64 + h * 16, r0, bh);
               bulk_commit();
             }
             ++nred;

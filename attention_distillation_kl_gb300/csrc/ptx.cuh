@@ -219,10 +219,11 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 __device__ __forceinline__ void bulk_wait_read_all() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
-// Waits until at most two committed bulk groups of this thread are still
+// Waits until at most N committed bulk groups of this thread are still
 // reading their shared-memory source.
-__device__ __forceinline__ void bulk_wait_read_le2() {
-  asm volatile("cp.async.bulk.wait_group.read 2;" ::: "memory");
+template <int N>
+__device__ __forceinline__ void bulk_wait_read_le() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
 }
 // Waits until every committed bulk group of this thread has completed.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
