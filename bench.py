@@ -40,8 +40,8 @@ UNIT = "TFLOP/s"
 # only while its source is unchanged (sha256 of the file it lives in).
 TRAFFIC = {
     # dram__bytes_read.sum + dram__bytes_write.sum of one full-size launch
-    "bwd_fused": {"bytes": 3296489472 + 2137337344, "src_sha": "0369387aa5f39747"},
-    "fwd": {"bytes": 2162542848 + 28695296, "src_sha": "cfd9153e8affce3f"},
+    "bwd_fused": {"bytes": 3295700480 + 2137939712, "src_sha": "d0e13631f6795f1a"},
+    "fwd": {"bytes": 2163079424 + 28846848, "src_sha": "468202db5f601fa5"},
 }
 
 
@@ -132,9 +132,17 @@ class Clocks:
                 "samples": len(sm)}
 
 
-def src_sha(name):
-    p = os.path.join(ROOT, "attention_distillation_kl_gb300", "csrc", name)
-    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+KERNEL_SOURCES = {"bwd_fused": ["bwd.cu", "bwd_common.cuh", "ptx.cuh", "kernels.cuh"],
+                  "fwd": ["fwd.cu", "ptx.cuh", "kernels.cuh"]}
+
+
+def src_sha(kernel):
+    """Hash of the sources a kernel is compiled from (its .cu and the headers
+    it includes): recorded traffic is only reported for the same sources."""
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kernel]:
+        h.update(open(os.path.join(ROOT, "attention_distillation_kl_gb300", "csrc", name), "rb").read())
+    return h.hexdigest()[:16]
 
 
 def cpu_sample(rows):
@@ -295,9 +303,10 @@ def run_mine(args, rank, world, local):
     bwd_tf = f_bwd / (bwd_ms * 1e-3) / 1e12
     fwd_tf = f_fwd / (fwd_ms * 1e-3) / 1e12
     dom = "bwd" if bwd_ms >= fwd_ms else "fwd"
-    tr = TRAFFIC.get("bwd_fused" if dom == "bwd" else "fwd")
+    kname = "bwd_fused" if dom == "bwd" else "fwd"
+    tr = TRAFFIC.get(kname)
     traffic = None
-    if tr and tr["src_sha"] == src_sha("bwd.cu" if dom == "bwd" else "fwd.cu"):
+    if tr and tr["src_sha"] == src_sha(kname):
         traffic = tr["bytes"]
     if skl.streamkl_get_device_status() != 0:
         raise RuntimeError("device status reported a timeout")
