@@ -11,15 +11,17 @@
 //
 // Fused kernel (article section "GPU kernel engineering": one visit per
 // query/key tile pair, dQ through atomics).  One CTA owns a 128-key tile and
-// walks the query tiles that can see it.  GB300 mapping, 14 warps:
+// walks the query tiles that can see it.  GB300 mapping, 15 warps:
 //   warp 12    TMA: K1, K2 once; per query tile Q_o (single buffer) and Q_g
 //              (double buffer; it is read again by the dK product)
-//   warp 13    TMEM owner, MMA issuer:
+//   warp 13    TMEM owner, S issuer:
 //                S1 = Q1 K1^T, S2 = Q2 K2^T      (M = queries, N = keys)
+//   warp 14    gradient issuer, one query tile behind:
 //                dK  += dS^T Q_g                   (accumulates in TMEM)
 //                dQ   = dS K_g                     (per query tile)
-//              with S of tile i+1 issued before the gradient products of
-//              tile i, so the tensor pipe stays busy while dS is formed
+//              Two issuing threads, so neither product waits behind the
+//              other's barriers; the tensor pipe runs S of tile i+1 while
+//              dS of tile i is formed.
 //   warps 0-7  thread = query row: P1/P2 and dS from S (TMEM) with the
 //              row's LSE/dKL/KL in registers (loaded one tile ahead);
 //              warps 0-3 take key columns 0-63, warps 4-7 columns 64-127
@@ -28,7 +30,7 @@
 //              128-byte-swizzled layout both products read: K-major A for
 //              dQ, M-major A (dS^T) for dK
 //   warps 8-11 dQ tile: TMEM -> registers (scaled) -> 32 x 16 fp32 boxes in
-//              swizzled shared memory (three per warp, round robin) -> TMA
+//              swizzled shared memory (four per warp, round robin) -> TMA
 //              bulk tensor reduce-add into global dQ (rows past NQ are
 //              clipped by the tensor map); finally dK (each CTA owns its
 //              keys: plain stores)
@@ -43,7 +45,7 @@
 
 namespace skl {
 
-constexpr int kBwdThreads = 448;
+constexpr int kBwdThreads = 480;
 constexpr int kDqBoxes = 4;  // dQ staging boxes per epilogue warp
 
 template <int D1, int D2, int MODE>
@@ -101,6 +103,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       uint32_t count = 1;  // TMA transaction barriers and tcgen05.commit targets
       if (b == L::B_SFREE || b == L::B_DSFULL) count = 8;  // one per dS warp
       if (b == L::B_DQEMPTY) count = 4;                    // one per epilogue warp
+      if (b == L::B_DONE) count = 2;                       // one per MMA issuer
       mbar_init(bar(b), count);
     }
     *abort_flag = 0;
@@ -156,37 +159,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     }
   } else if (warp == 13) {
-    // ---------------------------------------------------------------- MMA issuer
+    // ---------------------------------------------------------------- S issuer
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16(128, 128, 0, 0);
-      constexpr uint32_t id_dk = idesc_bf16(128, DG, 1, 1);  // A = dS^T M-major, B = Q_g N-major
-      constexpr uint32_t id_dq = idesc_bf16(128, DG, 0, 1);  // A = dS K-major,   B = K_g N-major
-      const uint32_t oKg = kP2 ? L::oK2 : L::oK1;
-      // gradient products of query tile t (dS(t) in shared memory)
-      auto grads = [&](int t) -> bool {
-        if (!mbar_wait_polled(bar(L::B_DSFULL), t & 1, ctl)) return false;
-        if (a.write_dq && !mbar_wait_polled(bar(L::B_DQEMPTY), (t & 1) ^ 1, ctl)) return false;
-        tc_fence_after();
-        const uint64_t dsm = sdesc_sw128(sb + L::oDS, kTile * 128, 1024);  // dS^T, M-major
-        const uint64_t qgn = sdesc_sw128(sb + L::oQg + (t & 1) * L::kQg, kTile * 128, 1024);
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_bf16_ss(1u, t_dk, sdesc_add(dsm, kk * 2048), sdesc_add(qgn, kk * 2048), id_dk,
-                      (t > 0 || kk > 0) ? 1u : 0u);
-        // Q_g(t) is free once dK has read it: its reload starts before dQ runs
-        mma_commit(1u, bar(L::B_QGEMPTY0 + (t & 1)));
-        if (a.write_dq) {
-          const uint64_t dsk = sdesc_sw128(sb + L::oDS, 16, 1024);  // dS, K-major
-          const uint64_t kgn = sdesc_sw128(sb + oKg, kTile * 128, 1024);
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_bf16_ss(1u, t_dq, sdesc_add(dsk, (kk >> 2) * (kTile * 128) + (kk & 3) * 32),
-                        sdesc_add(kgn, kk * 2048), id_dq, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(1u, bar(L::B_DSEMPTY));
-        if (a.write_dq) mma_commit(1u, bar(L::B_DQFULL));
-        return true;
-      };
       // S of one side for query tile i: Q tile (A, K-major) x K (B, K-major)
       auto s_product = [&](int side, uint32_t qs) {
         const uint32_t ks = sb + (side == 1 ? L::oK1 : L::oK2);
@@ -211,12 +186,43 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_after();
         s_product(kP2 ? 2 : 1, sb + L::oQg + (i & 1) * L::kQg);
         mma_commit(1u, bar(L::B_SFULL));
-        if (i > 0 && !grads(i - 1)) {
-          ok = false;
-          break;
+      }
+      mma_commit(1u, bar(L::B_DONE));
+      mbar_drain(bar(L::B_DONE), 0, 1000000000ull);
+    }
+  } else if (warp == 14) {
+    // ---------------------------------------------------------------- gradient issuer
+    if (lane == 0) {
+      constexpr uint32_t id_dk = idesc_bf16(128, DG, 1, 1);  // A = dS^T M-major, B = Q_g N-major
+      constexpr uint32_t id_dq = idesc_bf16(128, DG, 0, 1);  // A = dS K-major,   B = K_g N-major
+      const uint32_t oKg = kP2 ? L::oK2 : L::oK1;
+      const uint64_t dsm = sdesc_sw128(sb + L::oDS, kTile * 128, 1024);  // dS^T, M-major
+      const uint64_t dsk = sdesc_sw128(sb + L::oDS, 16, 1024);           // dS, K-major
+      const uint64_t kgn = sdesc_sw128(sb + oKg, kTile * 128, 1024);
+      int t = 0;
+      if (n > 0 && mbar_wait_polled(bar(L::B_KFULL), 0, ctl)) {
+        for (; t < n; ++t) {
+          if (!mbar_wait_polled(bar(L::B_DSFULL), t & 1, ctl)) break;
+          if (a.write_dq && !mbar_wait_polled(bar(L::B_DQEMPTY), (t & 1) ^ 1, ctl)) break;
+          tc_fence_after();
+          const uint64_t qgn = sdesc_sw128(sb + L::oQg + (t & 1) * L::kQg, kTile * 128, 1024);
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            mma_bf16_ss(1u, t_dk, sdesc_add(dsm, kk * 2048), sdesc_add(qgn, kk * 2048), id_dk,
+                        (t > 0 || kk > 0) ? 1u : 0u);
+          // Q_g(t) is free once dK has read it: its reload starts before dQ runs
+          mma_commit(1u, bar(L::B_QGEMPTY0 + (t & 1)));
+          if (a.write_dq) {
+#pragma unroll
+            for (int kk = 0; kk < kTile / 16; ++kk)
+              mma_bf16_ss(1u, t_dq, sdesc_add(dsk, (kk >> 2) * (kTile * 128) + (kk & 3) * 32),
+                          sdesc_add(kgn, kk * 2048), id_dq, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(1u, bar(L::B_DSEMPTY));
+          if (a.write_dq) mma_commit(1u, bar(L::B_DQFULL));
         }
       }
-      if (ok && n > 0 && !*abort_flag && grads(n - 1)) mma_commit(1u, bar(L::B_DKFULL));
+      if (n > 0 && t == n && !*abort_flag) mma_commit(1u, bar(L::B_DKFULL));
       mma_commit(1u, bar(L::B_DONE));
       mbar_drain(bar(L::B_DONE), 0, 1000000000ull);
     }
