@@ -11,17 +11,16 @@
 //
 // Fused kernel (article section "GPU kernel engineering": one visit per
 // query/key tile pair, dQ through atomics).  One CTA owns a 128-key tile and
-// walks the query tiles that can see it.  GB300 mapping, 15 warps:
+// walks the query tiles that can see it.  GB300 mapping, 15 or 16 warps:
 //   warp 12    TMA: K1, K2 once; per query tile Q_o (single buffer) and Q_g
 //              (double buffer; it is read again by the dK product)
 //   warp 13    TMEM owner, S issuer:
 //                S1 = Q1 K1^T, S2 = Q2 K2^T      (M = queries, N = keys)
-//   warp 14    gradient issuer, one query tile behind:
-//                dK  += dS^T Q_g                   (accumulates in TMEM)
-//                dQ   = dS K_g                     (per query tile)
-//              Two issuing threads, so neither product waits behind the
-//              other's barriers; the tensor pipe runs S of tile i+1 while
-//              dS of tile i is formed.
+//   warp 14    dK issuer:   dK += dS^T Q_g       (accumulates in TMEM)
+//              and, in mode P2, dQ = dS K_g      (per query tile)
+//   warp 15    mode P1 only: dQ issuer
+//              Separate issuing threads, so no product waits behind another's
+//              barriers (S of tile i+1 runs while dS of tile i is formed).
 //   warps 0-7  thread = query row: P1/P2 and dS from S (TMEM) with the
 //              row's LSE/dKL/KL in registers (loaded one tile ahead);
 //              warps 0-3 take key columns 0-63, warps 4-7 columns 64-127
@@ -45,13 +44,18 @@
 
 namespace skl {
 
-constexpr int kBwdThreads = 480;
+
 constexpr int kDqBoxes = 4;  // dQ staging boxes per epilogue warp
 
 template <int D1, int D2, int MODE>
 struct BwdLayout {
   static constexpr int DG = MODE == STREAMKL_GRAD_P2 ? D2 : D1;  // gradient side
   static constexpr int DO = MODE == STREAMKL_GRAD_P2 ? D1 : D2;  // other side
+  // Mode P1 forms dS with one ex2 per pair, so the MMA issue chain is what
+  // bounds it: dK and dQ then get an issuing thread each (16 warps).  In
+  // mode P2 the dS warps bound the tile and one thread issues both (15).
+  static constexpr bool kSplitIssue = MODE == STREAMKL_GRAD_P1;
+  static constexpr int kThreads = 32 * (kSplitIssue ? 16 : 15);
   static constexpr uint32_t kDS = kTile * kTile * 2;
   static constexpr uint32_t kK1 = kTile * D1 * 2, kK2 = kTile * D2 * 2;
   static constexpr uint32_t kQo = kTile * DO * 2, kQg = kTile * DG * 2;
@@ -69,7 +73,7 @@ struct BwdLayout {
 };
 
 template <int D1, int D2, int MODE>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
     bwd_fused_kernel(const __grid_constant__ CUtensorMap tq1, const __grid_constant__ CUtensorMap tk1,
                      const __grid_constant__ CUtensorMap tq2, const __grid_constant__ CUtensorMap tk2,
                      const __grid_constant__ CUtensorMap tdq, const BwdArgs a) {
@@ -103,7 +107,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       uint32_t count = 1;  // TMA transaction barriers and tcgen05.commit targets
       if (b == L::B_SFREE || b == L::B_DSFULL) count = 8;  // one per dS warp
       if (b == L::B_DQEMPTY) count = 4;                    // one per epilogue warp
-      if (b == L::B_DONE) count = 2;                       // one per MMA issuer
+      if (b == L::B_DSEMPTY) count = (L::kSplitIssue && a.write_dq) ? 2 : 1;  // dK (and dQ) issuers
+      if (b == L::B_DONE) count = L::kSplitIssue ? 3 : 2;  // one per MMA issuer
       mbar_init(bar(b), count);
     }
     *abort_flag = 0;
@@ -187,44 +192,64 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         s_product(kP2 ? 2 : 1, sb + L::oQg + (i & 1) * L::kQg);
         mma_commit(1u, bar(L::B_SFULL));
       }
+      // every MMA of every issuer has finished before TMEM is released
       mma_commit(1u, bar(L::B_DONE));
       mbar_drain(bar(L::B_DONE), 0, 1000000000ull);
     }
   } else if (warp == 14) {
-    // ---------------------------------------------------------------- gradient issuer
+    // ---------------------------------------------------------------- dK (and dQ) issuer
     if (lane == 0) {
+      constexpr bool kDq = !L::kSplitIssue;  // this thread also issues dQ
       constexpr uint32_t id_dk = idesc_bf16(128, DG, 1, 1);  // A = dS^T M-major, B = Q_g N-major
       constexpr uint32_t id_dq = idesc_bf16(128, DG, 0, 1);  // A = dS K-major,   B = K_g N-major
-      const uint32_t oKg = kP2 ? L::oK2 : L::oK1;
       const uint64_t dsm = sdesc_sw128(sb + L::oDS, kTile * 128, 1024);  // dS^T, M-major
       const uint64_t dsk = sdesc_sw128(sb + L::oDS, 16, 1024);           // dS, K-major
-      const uint64_t kgn = sdesc_sw128(sb + oKg, kTile * 128, 1024);
+      const uint64_t kgn = sdesc_sw128(sb + (kP2 ? L::oK2 : L::oK1), kTile * 128, 1024);
       int t = 0;
       if (n > 0 && mbar_wait_polled(bar(L::B_KFULL), 0, ctl)) {
         for (; t < n; ++t) {
           if (!mbar_wait_polled(bar(L::B_DSFULL), t & 1, ctl)) break;
-          if (a.write_dq && !mbar_wait_polled(bar(L::B_DQEMPTY), (t & 1) ^ 1, ctl)) break;
+          if (kDq && a.write_dq && !mbar_wait_polled(bar(L::B_DQEMPTY), (t & 1) ^ 1, ctl)) break;
           tc_fence_after();
           const uint64_t qgn = sdesc_sw128(sb + L::oQg + (t & 1) * L::kQg, kTile * 128, 1024);
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk)
             mma_bf16_ss(1u, t_dk, sdesc_add(dsm, kk * 2048), sdesc_add(qgn, kk * 2048), id_dk,
                         (t > 0 || kk > 0) ? 1u : 0u);
-          // Q_g(t) is free once dK has read it: its reload starts before dQ runs
-          mma_commit(1u, bar(L::B_QGEMPTY0 + (t & 1)));
-          if (a.write_dq) {
+          mma_commit(1u, bar(L::B_QGEMPTY0 + (t & 1)));  // Q_g(t) may be reloaded
+          if (kDq && a.write_dq) {
 #pragma unroll
             for (int kk = 0; kk < kTile / 16; ++kk)
               mma_bf16_ss(1u, t_dq, sdesc_add(dsk, (kk >> 2) * (kTile * 128) + (kk & 3) * 32),
                           sdesc_add(kgn, kk * 2048), id_dq, kk > 0 ? 1u : 0u);
           }
           mma_commit(1u, bar(L::B_DSEMPTY));
-          if (a.write_dq) mma_commit(1u, bar(L::B_DQFULL));
+          if (kDq && a.write_dq) mma_commit(1u, bar(L::B_DQFULL));
         }
       }
       if (n > 0 && t == n && !*abort_flag) mma_commit(1u, bar(L::B_DKFULL));
-      mma_commit(1u, bar(L::B_DONE));
-      mbar_drain(bar(L::B_DONE), 0, 1000000000ull);
+      mma_commit(1u, bar(L::B_DONE));  // the TMEM owner drains it before releasing TMEM
+    }
+  } else if (L::kSplitIssue && warp == 15) {
+    // ---------------------------------------------------------------- dQ issuer (mode P1)
+    if (lane == 0) {
+      constexpr uint32_t id_dq = idesc_bf16(128, DG, 0, 1);  // A = dS K-major, B = K_g N-major
+      const uint64_t dsk = sdesc_sw128(sb + L::oDS, 16, 1024);  // dS, K-major
+      const uint64_t kgn = sdesc_sw128(sb + (kP2 ? L::oK2 : L::oK1), kTile * 128, 1024);
+      if (a.write_dq && n > 0 && mbar_wait_polled(bar(L::B_KFULL), 0, ctl)) {
+        for (int t = 0; t < n; ++t) {
+          if (!mbar_wait_polled(bar(L::B_DSFULL), t & 1, ctl)) break;
+          if (!mbar_wait_polled(bar(L::B_DQEMPTY), (t & 1) ^ 1, ctl)) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            mma_bf16_ss(1u, t_dq, sdesc_add(dsk, (kk >> 2) * (kTile * 128) + (kk & 3) * 32),
+                        sdesc_add(kgn, kk * 2048), id_dq, kk > 0 ? 1u : 0u);
+          mma_commit(1u, bar(L::B_DSEMPTY));
+          mma_commit(1u, bar(L::B_DQFULL));
+        }
+      }
+      mma_commit(1u, bar(L::B_DONE));  // the TMEM owner drains it before releasing TMEM
     }
   } else if (warp < 8) {
     // ---------------------------------------------------------------- dS (thread = query row)
@@ -598,7 +623,7 @@ static int launch_fused_t(const TMaps& m, const BwdArgs& a, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
   dim3 grid((a.NK + kTile - 1) / kTile, a.BH);
-  kern<<<grid, kBwdThreads, L::kAlloc, st>>>(m.q1, m.k1, m.q2, m.k2, m.dq, a);
+  kern<<<grid, L::kThreads, L::kAlloc, st>>>(m.q1, m.k1, m.q2, m.k2, m.dq, a);
   return cudaGetLastError();
 }
 
