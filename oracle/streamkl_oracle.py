@@ -14,12 +14,15 @@ Sources (the pages this restates; no code was printed on them):
         Attention Distillation", arXiv 2606.20005 listing: abstract (row-wise
         KL between two attention distributions, tile-by-tile recompute).
 
-Notation (the pages' own): S1 = s*Q1 K1^T, S2 = s*Q2 K2^T, P1 = softmax(S1),
+Notation (the pages' own): S1 = s1*Q1 K1^T, S2 = s2*Q2 K2^T, P1 = softmax(S1),
 P2 = softmax(S2) row-wise over the visible keys, KL_i = sum_j P1_ij
 log(P1_ij / P2_ij), LSE_k = log sum_j exp(S_k,ij).
 
 Readings taken where the pages are silent (each is listed in the design doc):
-  * one softmax scale ``s`` multiplies both logit matrices;
+  * one softmax scale ``s`` multiplies both logit matrices by default; a
+    second scale (``scale2``) may be given for the S2 side, e.g. a student
+    with another head dimension (every function takes ``scale2=None``,
+    meaning s2 = s1 = ``scale``);
   * the causal mask is bottom-right aligned: key j is visible to query i iff
     j <= i + (NK - NQ); causal with NQ > NK is rejected (every row keeps at
     least one key);
@@ -75,7 +78,7 @@ def _logsumexp_rows(s, vis):
 
 
 @_quiet
-def _head_rows(q1, k1, q2, k2, scale, causal, rows):
+def _head_rows(q1, k1, q2, k2, s1, s2, causal, rows):
     """Materialise S, log P and P for the given query rows of one head.
 
     [AGI] "Why attention distillation matters": the loss compares the two
@@ -84,8 +87,7 @@ def _head_rows(q1, k1, q2, k2, scale, causal, rows):
     """
     nq, nk = q1.shape[0], k1.shape[0]
     vis = visible_mask(nq, nk, causal, rows)
-    s1 = scale * (q1[rows] @ k1.T)
-    s2 = scale * (q2[rows] @ k2.T)
+    s1, s2 = s1 * (q1[rows] @ k1.T), s2 * (q2[rows] @ k2.T)
     lse1 = _logsumexp_rows(s1, vis)
     lse2 = _logsumexp_rows(s2, vis)
     # log-domain probabilities: P itself may underflow, log P never does
@@ -99,43 +101,49 @@ def _head_rows(q1, k1, q2, k2, scale, causal, rows):
                 logp1=logp1, logp2=logp2, p1=p1, p2=p2, kl=kl)
 
 
+def _scales(scale, scale2):
+    """(s1, s2): the S1-side and S2-side softmax scales."""
+    return scale, (scale if scale2 is None else scale2)
+
+
 def _row_blocks(n, block):
     for r0 in range(0, n, block):
         yield np.arange(r0, min(n, r0 + block))
 
 
-def forward_head(q1, k1, q2, k2, scale, causal, row_block=256):
+def forward_head(q1, k1, q2, k2, scale, causal, row_block=256, scale2=None):
     """KL, LSE1, LSE2 for every query row of one head (float64 [NQ] each)."""
+    s1, s2 = _scales(scale, scale2)
     nq = q1.shape[0]
     kl = np.empty(nq)
     lse1 = np.empty(nq)
     lse2 = np.empty(nq)
     for rows in _row_blocks(nq, row_block):
-        r = _head_rows(q1, k1, q2, k2, scale, causal, rows)
+        r = _head_rows(q1, k1, q2, k2, s1, s2, causal, rows)
         kl[rows], lse1[rows], lse2[rows] = r["kl"], r["lse1"], r["lse2"]
     return kl, lse1, lse2
 
 
-def forward(q1, k1, q2, k2, scale, causal, row_block=256):
+def forward(q1, k1, q2, k2, scale, causal, row_block=256, scale2=None):
     """Batched forward over [B, H, N, d] inputs -> (kl, lse1, lse2) [B, H, NQ]."""
     b_, h_, nq = q1.shape[:3]
     out = [np.empty((b_, h_, nq)) for _ in range(3)]
     for b in range(b_):
         for h in range(h_):
-            res = forward_head(q1[b, h], k1[b, h], q2[b, h], k2[b, h], scale, causal, row_block)
+            res = forward_head(q1[b, h], k1[b, h], q2[b, h], k2[b, h], scale, causal, row_block, scale2)
             for o, v in zip(out, res):
                 o[b, h] = v
     return tuple(out)
 
 
-def forward_rows(q1, k1, q2, k2, scale, causal, rows):
+def forward_rows(q1, k1, q2, k2, scale, causal, rows, scale2=None):
     """Forward for selected query rows of one head (each row is independent)."""
-    r = _head_rows(q1, k1, q2, k2, scale, causal, np.asarray(rows))
+    r = _head_rows(q1, k1, q2, k2, *_scales(scale, scale2), causal, np.asarray(rows))
     return r["kl"], r["lse1"], r["lse2"]
 
 
 @_quiet
-def forward_online(q1, k1, q2, k2, scale, causal, key_tile=64, row_block=256):
+def forward_online(q1, k1, q2, k2, scale, causal, key_tile=64, row_block=256, scale2=None):
     """The pages' online coupled-KL recurrence, run in float64 ([AGI] "Online
     formula" and "Forward").
 
@@ -146,6 +154,7 @@ def forward_online(q1, k1, q2, k2, scale, causal, key_tile=64, row_block=256):
     At the end LSE = m + log l and KL = acc / l1 + LSE2 - LSE1.
     Only the logit tiles of one key tile exist at a time.
     """
+    sc1, sc2 = _scales(scale, scale2)
     nq, nk = q1.shape[0], k1.shape[0]
     kl = np.empty(nq)
     lse1 = np.empty(nq)
@@ -160,8 +169,8 @@ def forward_online(q1, k1, q2, k2, scale, causal, key_tile=64, row_block=256):
         for k0 in range(0, nk, key_tile):
             keys = np.arange(k0, min(nk, k0 + key_tile))
             vis = visible_mask(nq, nk, causal, rows)[:, keys]
-            s1 = scale * (q1[rows] @ k1[keys].T)
-            s2 = scale * (q2[rows] @ k2[keys].T)
+            s1 = sc1 * (q1[rows] @ k1[keys].T)
+            s2 = sc2 * (q2[rows] @ k2[keys].T)
             t1 = np.where(vis, s1, -np.inf).max(axis=1)
             t2 = np.where(vis, s2, -np.inf).max(axis=1)
             m1_new = np.maximum(m1, t1)
@@ -184,12 +193,13 @@ def forward_online(q1, k1, q2, k2, scale, causal, key_tile=64, row_block=256):
 
 
 @_quiet
-def forward_two_pass(q1, k1, q2, k2, scale, causal, key_tile=64, row_block=256):
+def forward_two_pass(q1, k1, q2, k2, scale, causal, key_tile=64, row_block=256, scale2=None):
     """The two-pass streaming alternative ([AGI] "Why FlashAttention does not
     carry over"): pass 1 streams keys for LSE1 and LSE2, pass 2 streams them
     again for sum_j P1 (S1 - S2); then KL = that sum - LSE1 + LSE2 (because
     log P1 - log P2 = S1 - S2 - LSE1 + LSE2 and P1 sums to one).
     """
+    sc1, sc2 = _scales(scale, scale2)
     nq, nk = q1.shape[0], k1.shape[0]
     kl = np.empty(nq)
     lse1 = np.empty(nq)
@@ -202,8 +212,8 @@ def forward_two_pass(q1, k1, q2, k2, scale, causal, key_tile=64, row_block=256):
         b = np.full(rows.shape[0], -np.inf)
         for keys in tiles:
             vis = vis_all[:, keys]
-            s1 = np.where(vis, scale * (q1[rows] @ k1[keys].T), -np.inf)
-            s2 = np.where(vis, scale * (q2[rows] @ k2[keys].T), -np.inf)
+            s1 = np.where(vis, sc1 * (q1[rows] @ k1[keys].T), -np.inf)
+            s2 = np.where(vis, sc2 * (q2[rows] @ k2[keys].T), -np.inf)
             for dst, s in ((0, s1), (1, s2)):
                 t = s.max(axis=1)
                 tt = np.where(np.isfinite(t), t, 0.0)
@@ -217,8 +227,8 @@ def forward_two_pass(q1, k1, q2, k2, scale, causal, key_tile=64, row_block=256):
         w = np.zeros(rows.shape[0])
         for keys in tiles:
             vis = vis_all[:, keys]
-            s1 = scale * (q1[rows] @ k1[keys].T)
-            s2 = scale * (q2[rows] @ k2[keys].T)
+            s1 = sc1 * (q1[rows] @ k1[keys].T)
+            s2 = sc2 * (q2[rows] @ k2[keys].T)
             p1 = np.where(vis, np.exp(np.where(vis, s1, 0.0) - a[:, None]), 0.0)
             w += np.sum(np.where(vis, p1 * (s1 - s2), 0.0), axis=1)
         lse1[rows], lse2[rows] = a, b
@@ -250,25 +260,27 @@ def _grad_scores(r, dkl_rows, mode):
     return np.where(vis, ds, 0.0)
 
 
-def backward_head(q1, k1, q2, k2, scale, causal, dkl, mode, row_block=256):
+def backward_head(q1, k1, q2, k2, scale, causal, dkl, mode, row_block=256, scale2=None):
     """(dQ, dK) of L = sum_i dKL_i KL_i for one head, on the gradient side.
 
     Mode P2 returns (dQ2 [NQ, d2], dK2 [NK, d2]); mode P1 returns (dQ1, dK1).
-    With S = s Q K^T: dQ = s dS K and dK = s dS^T Q.
+    With S = s Q K^T on the gradient side: dQ = s dS K and dK = s dS^T Q.
     """
+    s1, s2 = _scales(scale, scale2)
     nq, nk = q1.shape[0], k1.shape[0]
     qg, kg = (q2, k2) if mode == MODE_P2 else (q1, k1)
+    sg = s2 if mode == MODE_P2 else s1
     dq = np.zeros((nq, qg.shape[1]))
     dk = np.zeros((nk, kg.shape[1]))
     for rows in _row_blocks(nq, row_block):
-        r = _head_rows(q1, k1, q2, k2, scale, causal, rows)
+        r = _head_rows(q1, k1, q2, k2, s1, s2, causal, rows)
         ds = _grad_scores(r, dkl[rows], mode)
-        dq[rows] = scale * (ds @ kg)
-        dk += scale * (ds.T @ qg[rows])
+        dq[rows] = sg * (ds @ kg)
+        dk += sg * (ds.T @ qg[rows])
     return dq, dk
 
 
-def backward(q1, k1, q2, k2, scale, causal, dkl, mode, row_block=256):
+def backward(q1, k1, q2, k2, scale, causal, dkl, mode, row_block=256, scale2=None):
     """Batched backward over [B, H, N, d] inputs; dkl is [B, H, NQ]."""
     b_, h_, nq = q1.shape[:3]
     nk = k1.shape[2]
@@ -278,20 +290,21 @@ def backward(q1, k1, q2, k2, scale, causal, dkl, mode, row_block=256):
     for b in range(b_):
         for h in range(h_):
             dq[b, h], dk[b, h] = backward_head(q1[b, h], k1[b, h], q2[b, h], k2[b, h],
-                                               scale, causal, dkl[b, h], mode, row_block)
+                                               scale, causal, dkl[b, h], mode, row_block, scale2)
     return dq, dk
 
 
-def backward_dq_rows(q1, k1, q2, k2, scale, causal, dkl, mode, rows):
+def backward_dq_rows(q1, k1, q2, k2, scale, causal, dkl, mode, rows, scale2=None):
     """dQ for selected query rows of one head (a row's dS needs only that row)."""
+    s1, s2 = _scales(scale, scale2)
     rows = np.asarray(rows)
-    r = _head_rows(q1, k1, q2, k2, scale, causal, rows)
+    r = _head_rows(q1, k1, q2, k2, s1, s2, causal, rows)
     ds = _grad_scores(r, dkl[rows], mode)
-    kg = k2 if mode == MODE_P2 else k1
-    return scale * (ds @ kg)
+    kg, sg = (k2, s2) if mode == MODE_P2 else (k1, s1)
+    return sg * (ds @ kg)
 
 
-def backward_dk_keys(q1, k1, q2, k2, scale, causal, dkl, mode, keys, row_block=256, first_row=0):
+def backward_dk_keys(q1, k1, q2, k2, scale, causal, dkl, mode, keys, row_block=256, first_row=0, scale2=None):
     """dK for selected keys of one head: dK_j = s sum_i dS_ij Q_i over all rows.
 
     ``first_row`` skips rows that see none of ``keys`` under the causal mask
@@ -301,19 +314,21 @@ def backward_dk_keys(q1, k1, q2, k2, scale, causal, dkl, mode, keys, row_block=2
     nq, nk = q1.shape[0], k1.shape[0]
     if first_row > 0 and (not causal or first_row > keys.min() - (nk - nq)):
         raise ValueError("first_row would skip rows that see the requested keys")
+    s1, s2 = _scales(scale, scale2)
     qg, kg = (q2, k2) if mode == MODE_P2 else (q1, k1)
+    sg = s2 if mode == MODE_P2 else s1
     dk = np.zeros((keys.shape[0], kg.shape[1]))
     for rows in _row_blocks(nq, row_block):
         rows = rows[rows >= first_row]
         if rows.shape[0] == 0:
             continue
-        r = _head_rows(q1, k1, q2, k2, scale, causal, rows)
+        r = _head_rows(q1, k1, q2, k2, s1, s2, causal, rows)
         ds = _grad_scores(r, dkl[rows], mode)[:, keys]
-        dk += scale * (ds.T @ qg[rows])
+        dk += sg * (ds.T @ qg[rows])
     return dk
 
 
-def loss(q1, k1, q2, k2, scale, causal, dkl):
+def loss(q1, k1, q2, k2, scale, causal, dkl, scale2=None):
     """Scalar L = sum dKL * KL over all rows, for finite-difference checks."""
-    kl, _, _ = forward(q1, k1, q2, k2, scale, causal)
+    kl, _, _ = forward(q1, k1, q2, k2, scale, causal, scale2=scale2)
     return float(np.sum(dkl * kl))

@@ -22,7 +22,10 @@ MUTANTS = {
     "kl weight P2 instead of P1": ("p1 * (logp1 - logp2), 0.0), axis=1)", "p2 * (logp1 - logp2), 0.0), axis=1)"),
     "kl log ratio flipped": ("p1 * (logp1 - logp2), 0.0), axis=1)", "p1 * (logp2 - logp1), 0.0), axis=1)"),
     "lse without max shift back": ("return m + np.log(", "return np.log("),
-    "scale dropped on S2": ("s2 = scale * (q2[rows] @ k2.T)", "s2 = (q2[rows] @ k2.T)"),
+    "scale dropped on S2": ("s2 * (q2[rows] @ k2.T)", "(q2[rows] @ k2.T)"),
+    "S2 takes the S1 scale": ("s2 * (q2[rows] @ k2.T)", "s1 * (q2[rows] @ k2.T)"),
+    "online S2 takes the S1 scale": ("s2 = sc2 * (q2[rows] @ k2[keys].T)\n            t1", "s2 = sc1 * (q2[rows] @ k2[keys].T)\n            t1"),
+    "gradient scale of the other side": ("sg = s2 if mode == MODE_P2 else s1\n    dq = np.zeros", "sg = s1 if mode == MODE_P2 else s2\n    dq = np.zeros"),
     "top-left causal alignment": ("return j <= rows[:, None] + (nk - nq)", "return j <= rows[:, None]"),
     "strict causal mask": ("return j <= rows[:, None] + (nk - nq)", "return j < rows[:, None] + (nk - nq)"),
     "online acc not rescaled": ("acc = a1 * acc + ", "acc = acc + "),
@@ -33,10 +36,10 @@ MUTANTS = {
     "mode P1 drops KL": ('(ratio - r["kl"][:, None])', '(ratio)'),
     "mode P1 weight P2": ('ds = dkl_rows[:, None] * r["p1"] * (ratio', 'ds = dkl_rows[:, None] * r["p2"] * (ratio'),
     "dkl ignored": ('ds = dkl_rows[:, None] * (r["p2"] - r["p1"])', 'ds = (r["p2"] - r["p1"])'),
-    "dq scale dropped": ("dq[rows] = scale * (ds @ kg)", "dq[rows] = (ds @ kg)"),
-    "dk uses other side": ("dk += scale * (ds.T @ qg[rows])", "dk += scale * (ds.T @ (q1 if mode == MODE_P2 else q2)[rows][:, :qg.shape[1]])"),
-    "sampled dq wrong side": ("kg = k2 if mode == MODE_P2 else k1\n    return", "kg = k1 if mode == MODE_P2 else k2\n    return"),
-    "sampled dk missing scale": ("dk += scale * (ds.T @ qg[rows])\n    return dk\n\n\ndef loss", "dk += (ds.T @ qg[rows])\n    return dk\n\n\ndef loss"),
+    "dq scale dropped": ("dq[rows] = sg * (ds @ kg)", "dq[rows] = (ds @ kg)"),
+    "dk uses other side": ("dk += sg * (ds.T @ qg[rows])", "dk += sg * (ds.T @ (q1 if mode == MODE_P2 else q2)[rows][:, :qg.shape[1]])"),
+    "sampled dq wrong side": ("kg, sg = (k2, s2) if mode == MODE_P2 else (k1, s1)", "kg, sg = (k1, s2) if mode == MODE_P2 else (k2, s1)"),
+    "sampled dk missing scale": ("dk += sg * (ds.T @ qg[rows])\n    return dk\n\n\ndef loss", "dk += (ds.T @ qg[rows])\n    return dk\n\n\ndef loss"),
 }
 
 

@@ -13,7 +13,11 @@ copies of the oracle with planted mistakes.  What each pin rests on:
 * independent library routines: torch.nn.functional.kl_div / log_softmax,
   scipy.special.logsumexp, CPU float64 torch autograd;
 * central finite differences of sum(dKL * KL) for both gradient modes;
-* the online recurrence and the two-pass form agreeing with the direct one.
+* the online recurrence and the two-pass form agreeing with the direct one;
+* a second softmax scale for the S2 side: s2 = 0 gives the uniform-student
+  closed form, a power-of-two rescale of Q2 against s2 changes nothing, and
+  per-side results equal single-scale results with Q2 pre-multiplied by
+  s2/s1 (gradients by the chain rule), plus finite differences.
 """
 
 import math
@@ -188,13 +192,13 @@ def pin_online_and_two_pass(o):
                 np.testing.assert_allclose(b2, b, rtol=1e-13, atol=1e-13)
 
 
-def _fd_grad(o, q1, k1, q2, k2, s, causal, dkl, mode, h=1e-6):
+def _fd_grad(o, q1, k1, q2, k2, s, causal, dkl, mode, h=1e-6, s2=None):
     """Central differences of L = sum(dkl * KL) w.r.t. the gradient side."""
     args = [q1.copy(), k1.copy(), q2.copy(), k2.copy()]
     iq, ik = (2, 3) if mode == O.MODE_P2 else (0, 1)
 
     def L():
-        return o.loss(*(x[None, None] for x in args), s, causal, dkl[None, None])
+        return o.loss(*(x[None, None] for x in args), s, causal, dkl[None, None], scale2=s2)
 
     out = []
     for idx in (iq, ik):
@@ -297,6 +301,72 @@ def pin_underflow_is_finite(o):
         dq, dk = o.backward(q1[None, None], k1[None, None], q2[None, None], k2[None, None],
                             1.0, False, np.ones((1, 1, nq)), mode)
         assert np.all(np.isfinite(dq)) and np.all(np.isfinite(dk))
+
+
+def pin_per_side_scale_uniform_student(o):
+    """s2 = 0 makes P2 uniform whatever Q2 is: KL_i = log|A_i| - H(P1_i)."""
+    rng = np.random.default_rng(17)
+    nq, nk = 10, 14
+    for causal in (False, True):
+        q1, k1, q2, k2 = _head(rng, nq, nk, 5, 4)
+        kl, _, lse2 = o.forward_head(q1, k1, q2, k2, 0.7, causal, scale2=0.0)
+        for i in range(nq):
+            n_vis = nk if not causal else i + (nk - nq) + 1
+            p1 = scipy.special.softmax(0.7 * (q1[i] @ k1[:n_vis].T))
+            assert abs(kl[i] - (math.log(n_vis) - scipy.stats.entropy(p1))) < 1e-12
+            assert abs(lse2[i] - math.log(n_vis)) < 1e-12
+
+
+def pin_per_side_scale_matches_prescaled_student(o):
+    """(s1, s2) on (Q1, Q2) is s1 on (Q1, (s2/s1) Q2): forward equal; the
+    gradient w.r.t. Q2 picks up the factor s2/s1 by the chain rule, w.r.t.
+    K2 (and on the P1 side) it is unchanged.  A power-of-two rescale of Q2
+    against s2 is exact."""
+    rng = np.random.default_rng(18)
+    s1, s2 = 0.8, 0.45
+    for causal in (False, True):
+        q1, k1, q2, k2 = _head(rng, 13, 17, 6, 4, sd=1.2)
+        dkl = rng.uniform(0.5, 1.5, 13)
+        b = lambda x: x[None, None]
+        got = o.forward(b(q1), b(k1), b(q2), b(k2), s1, causal, scale2=s2)
+        want = o.forward(b(q1), b(k1), b(q2 * (s2 / s1)), b(k2), s1, causal)
+        for g, w in zip(got, want):
+            np.testing.assert_allclose(g, w, rtol=1e-12, atol=1e-13)
+        exact = o.forward(b(q1), b(k1), b(q2 * 4.0), b(k2), s1, causal, scale2=s2 / 4.0)
+        for g, w in zip(got, exact):
+            assert np.array_equal(g, w)
+        for mode in (O.MODE_P2, O.MODE_P1):
+            dq, dk = o.backward(b(q1), b(k1), b(q2), b(k2), s1, causal, b(dkl), mode, scale2=s2)
+            dq0, dk0 = o.backward(b(q1), b(k1), b(q2 * (s2 / s1)), b(k2), s1, causal, b(dkl), mode)
+            fq = s2 / s1 if mode == O.MODE_P2 else 1.0
+            np.testing.assert_allclose(dq, fq * dq0, rtol=1e-11, atol=1e-14)
+            np.testing.assert_allclose(dk, dk0, rtol=1e-11, atol=1e-14)
+
+
+def pin_per_side_scale_finite_differences(o):
+    rng = np.random.default_rng(19)
+    for causal, nq, nk, d1, d2 in ((False, 5, 6, 3, 4), (True, 5, 7, 4, 2)):
+        q1, k1, q2, k2 = _head(rng, nq, nk, d1, d2, sd=1.2)
+        dkl = rng.uniform(0.5, 1.5, nq)
+        for mode in (O.MODE_P2, O.MODE_P1):
+            dq, dk = o.backward(q1[None, None], k1[None, None], q2[None, None], k2[None, None],
+                                0.9, causal, dkl[None, None], mode, scale2=0.55)
+            gq, gk = _fd_grad(o, q1, k1, q2, k2, 0.9, causal, dkl, mode, s2=0.55)
+            for got, want in ((dq[0, 0], gq), (dk[0, 0], gk)):
+                err = np.abs(got - want).max() / max(1e-12, np.abs(want).max())
+                assert err < 1e-7, (causal, mode, err)
+
+
+def pin_per_side_scale_online(o):
+    rng = np.random.default_rng(20)
+    q1, k1, q2, k2 = _head(rng, 29, 41, 6, 4, sd=1.3)
+    for causal in (False, True):
+        kl, a, b = o.forward_head(q1, k1, q2, k2, 0.9, causal, scale2=0.4)
+        for fn in (o.forward_online, o.forward_two_pass):
+            kl2, a2, b2 = fn(q1, k1, q2, k2, 0.9, causal, key_tile=8, row_block=6, scale2=0.4)
+            np.testing.assert_allclose(kl2, kl, rtol=1e-12, atol=1e-13)
+            np.testing.assert_allclose(a2, a, rtol=1e-13, atol=1e-13)
+            np.testing.assert_allclose(b2, b, rtol=1e-13, atol=1e-13)
 
 
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
