@@ -49,6 +49,11 @@ _SIGS = {
     "streamkl_suggest_splits": (_I, [_I, _I, _I, _I, _I]),
     "streamkl_bwd": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P, _P, _I, _I,
                           _P, _P, _P]),
+    "streamkl_fwd_scaled": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _F, _I, _P, _P, _P, _P]),
+    "streamkl_fwd_splitk_scaled": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _F, _I, _I, _P, _SZ,
+                                        _P, _P, _P, _P]),
+    "streamkl_bwd_scaled": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _F, _I, _P, _P, _P, _P, _I,
+                                 _I, _P, _P, _P]),
     "streamkl_status_string": (ctypes.c_char_p, [_I]),
     "streamkl_get_device_status": (_I, []),
     "streamkl_probe_ex2": (_I, [_P, _I, _I, _P]),
@@ -203,6 +208,56 @@ def streamkl_bwd(q1, k1, q2, k2, scale, causal, kl, lse1, lse2, dkl, mode=STREAM
                               int(mode), int(bool(deterministic)), dq.data_ptr(), dk.data_ptr(),
                               _stream(stream)),
            "streamkl_bwd")
+    return dq, dk
+
+
+def streamkl_fwd_scaled(q1, k1, q2, k2, scale1, scale2, causal, kl=None, lse1=None, lse2=None, stream=None):
+    """streamkl_fwd with S1 = scale1 Q1 K1^T and S2 = scale2 Q2 K2^T."""
+    B, H, NQ, NK, d1, d2 = _dims(q1, k1, q2, k2)
+    kl = _out(kl, (B, H, NQ), q1.device, "kl")
+    lse1 = _out(lse1, (B, H, NQ), q1.device, "lse1")
+    lse2 = _out(lse2, (B, H, NQ), q1.device, "lse2")
+    _check(lib().streamkl_fwd_scaled(q1.data_ptr(), k1.data_ptr(), q2.data_ptr(), k2.data_ptr(),
+                                     B, H, NQ, NK, d1, d2, float(scale1), float(scale2), int(bool(causal)),
+                                     kl.data_ptr(), lse1.data_ptr(), lse2.data_ptr(), _stream(stream)),
+           "streamkl_fwd_scaled")
+    return kl, lse1, lse2
+
+
+def streamkl_fwd_splitk_scaled(q1, k1, q2, k2, scale1, scale2, causal, num_splits, workspace=None,
+                               kl=None, lse1=None, lse2=None, stream=None):
+    """streamkl_fwd_splitk with a softmax scale per side."""
+    B, H, NQ, NK, d1, d2 = _dims(q1, k1, q2, k2)
+    need = streamkl_fwd_splitk_workspace_bytes(B, H, NQ, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q1.device)
+    kl = _out(kl, (B, H, NQ), q1.device, "kl")
+    lse1 = _out(lse1, (B, H, NQ), q1.device, "lse1")
+    lse2 = _out(lse2, (B, H, NQ), q1.device, "lse2")
+    _check(lib().streamkl_fwd_splitk_scaled(q1.data_ptr(), k1.data_ptr(), q2.data_ptr(), k2.data_ptr(),
+                                            B, H, NQ, NK, d1, d2, float(scale1), float(scale2),
+                                            int(bool(causal)), int(num_splits), workspace.data_ptr(),
+                                            workspace.numel() * workspace.element_size(),
+                                            kl.data_ptr(), lse1.data_ptr(), lse2.data_ptr(), _stream(stream)),
+           "streamkl_fwd_splitk_scaled")
+    return kl, lse1, lse2
+
+
+def streamkl_bwd_scaled(q1, k1, q2, k2, scale1, scale2, causal, kl, lse1, lse2, dkl, mode=STREAMKL_GRAD_P2,
+                        deterministic=False, dq=None, dk=None, stream=None):
+    """streamkl_bwd with a softmax scale per side (kl/lse from streamkl_fwd_scaled)."""
+    B, H, NQ, NK, d1, d2 = _dims(q1, k1, q2, k2)
+    dg = d2 if mode == STREAMKL_GRAD_P2 else d1
+    for name, t in (("kl", kl), ("lse1", lse1), ("lse2", lse2), ("dkl", dkl)):
+        _out(t, (B, H, NQ), q1.device, name)
+    dq = _out(dq, (B, H, NQ, dg), q1.device, "dq")
+    dk = _out(dk, (B, H, NK, dg), q1.device, "dk")
+    _check(lib().streamkl_bwd_scaled(q1.data_ptr(), k1.data_ptr(), q2.data_ptr(), k2.data_ptr(),
+                                     B, H, NQ, NK, d1, d2, float(scale1), float(scale2), int(bool(causal)),
+                                     kl.data_ptr(), lse1.data_ptr(), lse2.data_ptr(), dkl.data_ptr(),
+                                     int(mode), int(bool(deterministic)), dq.data_ptr(), dk.data_ptr(),
+                                     _stream(stream)),
+           "streamkl_bwd_scaled")
     return dq, dk
 
 

@@ -65,6 +65,8 @@ bool make_map_dq(CUtensorMap* m, void* ptr, long long BH, long long NQ, int dg) 
   return r == CUDA_SUCCESS;
 }
 
+bool scale_ok(float s) { return std::isfinite(s) && s > 0.f && s <= 1.0e4f; }
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool head_dim_ok(int d) { return d == 64 || d == 128; }
@@ -75,7 +77,7 @@ int check_problem(const void* q1, const void* k1, const void* q2, const void* k2
                   int NQ, int NK, int d1, int d2, float scale, int causal, bool* empty) {
   *empty = false;
   if (B < 0 || H < 0 || NQ < 0 || NK < 0) return STREAMKL_INVALID_ARG;
-  if (!std::isfinite(scale) || !(scale > 0.f) || scale > 1.0e4f) return STREAMKL_INVALID_ARG;
+  if (!scale_ok(scale)) return STREAMKL_INVALID_ARG;
   if (causal != 0 && causal != 1) return STREAMKL_INVALID_ARG;
   if (!head_dim_ok(d1) || !head_dim_ok(d2)) return STREAMKL_UNSUPPORTED;
   if (causal && NQ > NK) return STREAMKL_INVALID_ARG;
@@ -117,11 +119,12 @@ int as_status(int cuda_err) { return cuda_err == 0 ? STREAMKL_OK : STREAMKL_CUDA
 
 extern "C" {
 
-int streamkl_fwd(const void* q1, const void* k1, const void* q2, const void* k2, int B, int H,
-                 int NQ, int NK, int d1, int d2, float scale, int causal, float* kl, float* lse1,
-                 float* lse2, streamkl_stream_t stream) {
+int streamkl_fwd_scaled(const void* q1, const void* k1, const void* q2, const void* k2, int B, int H,
+                        int NQ, int NK, int d1, int d2, float scale1, float scale2, int causal, float* kl,
+                        float* lse1, float* lse2, streamkl_stream_t stream) {
   bool empty = false;
-  int s = check_problem(q1, k1, q2, k2, B, H, NQ, NK, d1, d2, scale, causal, &empty);
+  int s = check_problem(q1, k1, q2, k2, B, H, NQ, NK, d1, d2, scale1, causal, &empty);
+  if (s == STREAMKL_OK && !scale_ok(scale2)) s = STREAMKL_INVALID_ARG;
   if (s != STREAMKL_OK || empty) return s;
   if (!kl || !lse1 || !lse2 || !aligned16(kl) || !aligned16(lse1) || !aligned16(lse2))
     return STREAMKL_INVALID_ARG;
@@ -130,8 +133,15 @@ int streamkl_fwd(const void* q1, const void* k1, const void* q2, const void* k2,
   if ((s = make_maps(&m, q1, k1, q2, k2, B * H, NQ, NK, d1, d2)) != STREAMKL_OK) return s;
   int* st = status_ptr();
   if (!st) return STREAMKL_CUDA_ERROR;
-  skl::FwdArgs a{B * H, NQ, NK, causal, 1, scale, kl, lse1, lse2, nullptr, st};
+  skl::FwdArgs a{B * H, NQ, NK, causal, 1, scale1, scale2, kl, lse1, lse2, nullptr, st};
   return as_status(skl::launch_fwd(m, d1, d2, a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int streamkl_fwd(const void* q1, const void* k1, const void* q2, const void* k2, int B, int H,
+                 int NQ, int NK, int d1, int d2, float scale, int causal, float* kl, float* lse1,
+                 float* lse2, streamkl_stream_t stream) {
+  return streamkl_fwd_scaled(q1, k1, q2, k2, B, H, NQ, NK, d1, d2, scale, scale, causal, kl, lse1, lse2,
+                             stream);
 }
 
 size_t streamkl_fwd_splitk_workspace_bytes(int B, int H, int NQ, int num_splits) {
@@ -139,12 +149,13 @@ size_t streamkl_fwd_splitk_workspace_bytes(int B, int H, int NQ, int num_splits)
   return size_t(5) * 4 * size_t(num_splits) * size_t(B) * size_t(H) * size_t(NQ);
 }
 
-int streamkl_fwd_splitk(const void* q1, const void* k1, const void* q2, const void* k2, int B, int H,
-                        int NQ, int NK, int d1, int d2, float scale, int causal, int num_splits,
-                        void* workspace, size_t workspace_bytes, float* kl, float* lse1, float* lse2,
-                        streamkl_stream_t stream) {
+int streamkl_fwd_splitk_scaled(const void* q1, const void* k1, const void* q2, const void* k2, int B,
+                               int H, int NQ, int NK, int d1, int d2, float scale1, float scale2, int causal,
+                               int num_splits, void* workspace, size_t workspace_bytes, float* kl,
+                               float* lse1, float* lse2, streamkl_stream_t stream) {
   bool empty = false;
-  int s = check_problem(q1, k1, q2, k2, B, H, NQ, NK, d1, d2, scale, causal, &empty);
+  int s = check_problem(q1, k1, q2, k2, B, H, NQ, NK, d1, d2, scale1, causal, &empty);
+  if (s == STREAMKL_OK && !scale_ok(scale2)) s = STREAMKL_INVALID_ARG;
   if (s != STREAMKL_OK) return s;
   if (num_splits < 1 || num_splits > 1024) return STREAMKL_INVALID_ARG;
   if (empty) return STREAMKL_OK;
@@ -159,10 +170,18 @@ int streamkl_fwd_splitk(const void* q1, const void* k1, const void* q2, const vo
   if (!st) return STREAMKL_CUDA_ERROR;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   float* part = static_cast<float*>(workspace);
-  skl::FwdArgs a{B * H, NQ, NK, causal, num_splits, scale, kl, lse1, lse2, part, st};
+  skl::FwdArgs a{B * H, NQ, NK, causal, num_splits, scale1, scale2, kl, lse1, lse2, part, st};
   int e = skl::launch_fwd(m, d1, d2, a, cs);
   if (e != 0) return STREAMKL_CUDA_ERROR;
   return as_status(skl::launch_splitk_reduce(part, B * H * NQ, num_splits, kl, lse1, lse2, cs));
+}
+
+int streamkl_fwd_splitk(const void* q1, const void* k1, const void* q2, const void* k2, int B, int H,
+                        int NQ, int NK, int d1, int d2, float scale, int causal, int num_splits,
+                        void* workspace, size_t workspace_bytes, float* kl, float* lse1, float* lse2,
+                        streamkl_stream_t stream) {
+  return streamkl_fwd_splitk_scaled(q1, k1, q2, k2, B, H, NQ, NK, d1, d2, scale, scale, causal, num_splits,
+                                    workspace, workspace_bytes, kl, lse1, lse2, stream);
 }
 
 int streamkl_suggest_splits(int B, int H, int NQ, int NK, int causal) {
@@ -177,12 +196,13 @@ int streamkl_suggest_splits(int B, int H, int NQ, int NK, int causal) {
   return s;
 }
 
-int streamkl_bwd(const void* q1, const void* k1, const void* q2, const void* k2, int B, int H,
-                 int NQ, int NK, int d1, int d2, float scale, int causal, const float* kl,
-                 const float* lse1, const float* lse2, const float* dkl, int mode, int deterministic,
-                 float* dq, float* dk, streamkl_stream_t stream) {
+int streamkl_bwd_scaled(const void* q1, const void* k1, const void* q2, const void* k2, int B, int H,
+                        int NQ, int NK, int d1, int d2, float scale1, float scale2, int causal,
+                        const float* kl, const float* lse1, const float* lse2, const float* dkl, int mode,
+                        int deterministic, float* dq, float* dk, streamkl_stream_t stream) {
   bool empty = false;
-  int s = check_problem(q1, k1, q2, k2, B, H, NQ, NK, d1, d2, scale, causal, &empty);
+  int s = check_problem(q1, k1, q2, k2, B, H, NQ, NK, d1, d2, scale1, causal, &empty);
+  if (s == STREAMKL_OK && !scale_ok(scale2)) s = STREAMKL_INVALID_ARG;
   if (s != STREAMKL_OK) return s;
   if (mode != STREAMKL_GRAD_P2 && mode != STREAMKL_GRAD_P1) return STREAMKL_INVALID_ARG;
   if (deterministic != 0 && deterministic != 1) return STREAMKL_INVALID_ARG;
@@ -204,7 +224,7 @@ int streamkl_bwd(const void* q1, const void* k1, const void* q2, const void* k2,
   if ((s = make_maps(&m, q1, k1, q2, k2, B * H, NQ, NK, d1, d2)) != STREAMKL_OK) return s;
   int* st = status_ptr();
   if (!st) return STREAMKL_CUDA_ERROR;
-  skl::BwdArgs a{B * H, NQ, NK, causal, mode, scale, kl, lse1, lse2, dkl, dq, dk, st, 1};
+  skl::BwdArgs a{B * H, NQ, NK, causal, mode, scale1, scale2, kl, lse1, lse2, dkl, dq, dk, st, 1};
   if (!deterministic) {
     const size_t dq_bytes = size_t(B) * H * NQ * dg * 4;
     if (!make_map_dq(&m.dq, dq, (long long)B * H, NQ, dg)) return STREAMKL_CUDA_ERROR;
@@ -215,6 +235,14 @@ int streamkl_bwd(const void* q1, const void* k1, const void* q2, const void* k2,
   int e = skl::launch_bwd_fused(m, d1, d2, a, cs);
   if (e != 0) return STREAMKL_CUDA_ERROR;
   return as_status(skl::launch_bwd_dq(m, d1, d2, a, cs));
+}
+
+int streamkl_bwd(const void* q1, const void* k1, const void* q2, const void* k2, int B, int H,
+                 int NQ, int NK, int d1, int d2, float scale, int causal, const float* kl,
+                 const float* lse1, const float* lse2, const float* dkl, int mode, int deterministic,
+                 float* dq, float* dk, streamkl_stream_t stream) {
+  return streamkl_bwd_scaled(q1, k1, q2, k2, B, H, NQ, NK, d1, d2, scale, scale, causal, kl, lse1, lse2, dkl,
+                             mode, deterministic, dq, dk, stream);
 }
 
 const char* streamkl_status_string(int status) {

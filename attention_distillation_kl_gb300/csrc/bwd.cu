@@ -257,7 +257,9 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
     const int wg = warp >> 2;
     const int row = (warp & 3) * 32 + lane;
     const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
-    const uint64_t C = f2(a.scale * kLog2e, a.scale * kLog2e), SS = f2(a.scale, a.scale);
+    const float c1 = a.scale1 * kLog2e, c2 = a.scale2 * kLog2e, nr = -a.scale2 / a.scale1;
+    const uint64_t C1 = f2(c1, c1), C2 = f2(c2, c2), S1 = f2(a.scale1, a.scale1), NR = f2(nr, nr);
+    const float sg = kP2 ? a.scale2 : a.scale1;  // softmax scale of the gradient side
     // per-row parameters of query tile i (see ds_chunk_row)
     auto params = [&](int i, float& na, float& nb, float& ws) {
       const int qi = (qt_lo + i) * kTile + row;
@@ -268,7 +270,7 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
         const size_t idx = size_t(bh) * a.NQ + qi;
         const float l1 = a.lse1[idx];
         na = -l1 * kLog2e;
-        ws = a.scale * a.dkl[idx];
+        ws = sg * a.dkl[idx];
         nb = kP2 ? -a.lse2[idx] * kLog2e : -(l1 - a.lse2[idx] + a.kl[idx]);
       }
     };
@@ -295,9 +297,9 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
           if (lane == 0) mbar_arrive(bar(L::B_SFREE));
         }
         if (need_mask)
-          ds_chunk_row<MODE, true>(x1, x2, C, SS, NA, NB, WW, lim - col, dsr + ch * 16);
+          ds_chunk_row<MODE, true>(x1, x2, C1, C2, S1, NR, NA, NB, WW, lim - col, dsr + ch * 16);
         else
-          ds_chunk_row<MODE, false>(x1, x2, C, SS, NA, NB, WW, 0, dsr + ch * 16);
+          ds_chunk_row<MODE, false>(x1, x2, C1, C2, S1, NR, NA, NB, WW, 0, dsr + ch * 16);
       }
       // the previous tile's products must be done reading dS before it is replaced
       if (!mbar_wait_warp(bar(L::B_DSEMPTY), (i & 1) ^ 1, ctl)) break;
@@ -550,7 +552,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     // ---------------------------------------------------------------- dS (thread = query row)
     const int row = warp * 32 + lane;
     const int qi = q0 + row;
-    const float c = a.scale * kLog2e;
+    const float c1 = a.scale1 * kLog2e, c2 = a.scale2 * kLog2e, nr = -a.scale2 / a.scale1;
     const uint32_t lane_off = uint32_t(warp * 32) << 16;
     const int lim = a.causal ? min(qi + off, a.NK - 1) : a.NK - 1;  // last visible key
     float na = -INFINITY, nb = kP2 ? -INFINITY : 0.f, w = 0.f;
@@ -561,8 +563,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       w = a.dkl[idx];
       nb = kP2 ? -a.lse2[idx] * kLog2e : -(l1 - a.lse2[idx] + a.kl[idx]);
     }
-    const float ws = a.scale * w;  // s folded into dS
-    const uint64_t C = f2(c, c), SS = f2(a.scale, a.scale), NA = f2(na, na), NB = f2(nb, nb), WW = f2(ws, ws);
+    const float ws = (kP2 ? a.scale2 : a.scale1) * w;  // the gradient side's s folded into dS
+    const uint64_t C1 = f2(c1, c1), C2 = f2(c2, c2), S1 = f2(a.scale1, a.scale1), NR = f2(nr, nr);
+    const uint64_t NA = f2(na, na), NB = f2(nb, nb), WW = f2(ws, ws);
     for (int j = 0; j < nkt; ++j) {
       if (!mbar_wait_warp(bar(L::B_SFULL), j & 1, ctl)) break;
       tc_fence_after();
@@ -580,9 +583,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           if (lane == 0) mbar_arrive(bar(L::B_SFREE));
         }
         if (need_mask)
-          ds_chunk_row<MODE, true>(x1, x2, C, SS, NA, NB, WW, lim_rel - ch * 32, dsr + ch * 16);
+          ds_chunk_row<MODE, true>(x1, x2, C1, C2, S1, NR, NA, NB, WW, lim_rel - ch * 32, dsr + ch * 16);
         else
-          ds_chunk_row<MODE, false>(x1, x2, C, SS, NA, NB, WW, 0, dsr + ch * 16);
+          ds_chunk_row<MODE, false>(x1, x2, C1, C2, S1, NR, NA, NB, WW, 0, dsr + ch * 16);
       }
       if (!mbar_wait_warp(bar(L::B_DSEMPTY), (j & 1) ^ 1, ctl)) break;
       store_row_sw128(sb + L::oDS, row, dsr);

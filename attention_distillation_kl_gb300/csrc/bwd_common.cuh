@@ -43,29 +43,31 @@ __device__ __forceinline__ void store_half_row_sw128(uint32_t base, int r, int b
 
 // dS for 32 consecutive key columns of one query row (thread), packed to
 // bf16 pairs.  Per-row parameters, each broadcast to both halves of a pair:
-//   mode P2: NA = -LSE1 log2e, NB = -LSE2 log2e, WW = s dKL
-//   mode P1: NA = -LSE1 log2e, NB = -(LSE1 - LSE2 + KL), WW = s dKL
-// with C = s log2e and SS = s (the softmax scale s rides on dS, so
-// dK = dS^T Q and dQ = dS K need no further scaling).  Columns k > lim_rel
-// (causal, or past NK) give 0.  A row past NQ has NA = -inf (and NB = -inf
-// in mode P2, WW = 0), so every product is an exact 0.
+//   mode P2: NA = -LSE1 log2e, NB = -LSE2 log2e, WW = s2 dKL
+//   mode P1: NA = -LSE1 log2e, NB = -(LSE1 - LSE2 + KL), WW = s1 dKL
+// and per-launch constants C1 = s1 log2e, C2 = s2 log2e, S1 = s1,
+// NR = -s2 / s1 (the gradient side's softmax scale rides on dS, so
+// dK = dS^T Q and dQ = dS K need no further scaling; in mode P1 the
+// log-ratio S1 - S2 - LSE1 + LSE2 is s1 (x1 - (s2/s1) x2) + LSE2 - LSE1).
+// Columns k > lim_rel (causal, or past NK) give 0.  A row past NQ has
+// NA = -inf (and NB = -inf in mode P2, WW = 0), so every product is an exact 0.
 template <int MODE, bool kMask>
 __device__ __forceinline__ void ds_chunk_row(const uint32_t (&x1u)[32], const uint32_t (&x2u)[32],
-                                             uint64_t C, uint64_t SS, uint64_t NA, uint64_t NB, uint64_t WW,
-                                             int lim_rel, uint32_t* out16) {
+                                             uint64_t C1, uint64_t C2, uint64_t S1, uint64_t NR, uint64_t NA,
+                                             uint64_t NB, uint64_t WW, int lim_rel, uint32_t* out16) {
 #pragma unroll
   for (int k = 0; k < 32; k += 2) {
     const uint64_t X1 = f2(__uint_as_float(x1u[k]), __uint_as_float(x1u[k + 1]));
     const uint64_t X2 = f2(__uint_as_float(x2u[k]), __uint_as_float(x2u[k + 1]));
     float ea, eb;
-    f2_split(f2_fma(X1, C, NA), ea, eb);
+    f2_split(f2_fma(X1, C1, NA), ea, eb);
     const uint64_t P1 = f2(ex2(ea), ex2(eb));
     uint64_t D;
     if (MODE == STREAMKL_GRAD_P2) {
-      f2_split(f2_fma(X2, C, NB), ea, eb);
+      f2_split(f2_fma(X2, C2, NB), ea, eb);
       D = f2_mul(WW, f2_sub(f2(ex2(ea), ex2(eb)), P1));
     } else {
-      D = f2_mul(f2_mul(WW, P1), f2_fma(f2_sub(X1, X2), SS, NB));
+      D = f2_mul(f2_mul(WW, P1), f2_fma(f2_fma(X2, NR, X1), S1, NB));
     }
     float da, db;
     f2_split(D, da, db);

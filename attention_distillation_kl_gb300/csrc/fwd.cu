@@ -2,11 +2,13 @@
 // tile and keeps the coupled online statistics of the StreamKL article
 // ("Online formula", "Forward") in registers:
 //   m1, m2   running maxima of the raw logits q.k
-//   l1, l2   running sums of 2^(c (x - m))        (c = scale * log2 e)
-//   acc      running sum of 2^(c (x1 - m1)) (x1 - x2)
-// When m1 moves, l1 and acc are multiplied by 2^(c (m1_old - m1_new)) -- a
+//   l1, l2   running sums of 2^(c (x - m))        (c = s log2 e of that side)
+//   acc      running sum of 2^(c1 (x1 - m1)) (x1 - rho x2),  rho = s2 / s1
+// When m1 moves, l1 and acc are multiplied by 2^(c1 (m1_old - m1_new)) -- a
 // vector rescale per row, never a B_Q x d matrix.  At the end
-//   LSE = s m + ln l,  KL = s acc / l1 + LSE2 - LSE1.
+//   LSE = s m + ln l,  KL = s1 acc / l1 + LSE2 - LSE1
+// (s1 (x1 - rho x2) = S1 - S2, so s1 acc / l1 is the P1-weighted mean of
+// S1 - S2).
 //
 // GB300 mapping (10 warps, 1 CTA per SM):
 //   warp 8      TMA producer: Q1/Q2 once, then K1_j/K2_j into a ring of stages
@@ -67,9 +69,12 @@ struct RowStats {
 // Folds 32 consecutive key columns into the running state.  Columns k with
 // k > lim_rel are masked (causal or past NK): they neither move the maxima
 // nor add to the sums.  Pairs of columns go through the packed FP32 pipe.
+// c1, c2: s log2 e of each side; nrho = -s2 / s1 (x1 - rho x2 is one fma,
+// exactly x1 - x2 when the scales are equal).
 template <bool kMask>
 __device__ __forceinline__ void fold_chunk(RowStats& st, const uint32_t (&x1u)[32],
-                                           const uint32_t (&x2u)[32], float c, int lim_rel) {
+                                           const uint32_t (&x2u)[32], float c1, float c2, float nrho,
+                                           int lim_rel) {
   float t1 = st.m1, t2 = st.m2;
 #pragma unroll
   for (int k = 0; k < 32; k += 2) {
@@ -77,19 +82,20 @@ __device__ __forceinline__ void fold_chunk(RowStats& st, const uint32_t (&x1u)[3
     t1 = max3(t1, oa ? __uint_as_float(x1u[k]) : kNegBig, ob ? __uint_as_float(x1u[k + 1]) : kNegBig);
     t2 = max3(t2, oa ? __uint_as_float(x2u[k]) : kNegBig, ob ? __uint_as_float(x2u[k + 1]) : kNegBig);
   }
-  const float a1 = ex2((st.m1 - t1) * c);
-  const float a2 = ex2((st.m2 - t2) * c);
+  const float a1 = ex2((st.m1 - t1) * c1);
+  const float a2 = ex2((st.m2 - t2) * c2);
   st.m1 = t1;
   st.m2 = t2;
-  const uint64_t C = f2(c, c), NB1 = f2(-t1 * c, -t1 * c), NB2 = f2(-t2 * c, -t2 * c);
+  const uint64_t C1 = f2(c1, c1), C2 = f2(c2, c2), NR = f2(nrho, nrho);
+  const uint64_t NB1 = f2(-t1 * c1, -t1 * c1), NB2 = f2(-t2 * c2, -t2 * c2);
   uint64_t L1 = f2(0.f, 0.f), L2 = L1, ACC = L1;
 #pragma unroll
   for (int k = 0; k < 32; k += 2) {
     const uint64_t X1 = f2(__uint_as_float(x1u[k]), __uint_as_float(x1u[k + 1]));
     const uint64_t X2 = f2(__uint_as_float(x2u[k]), __uint_as_float(x2u[k + 1]));
     float e1a, e1b, e2a, e2b;
-    f2_split(f2_fma(X1, C, NB1), e1a, e1b);
-    f2_split(f2_fma(X2, C, NB2), e2a, e2b);
+    f2_split(f2_fma(X1, C1, NB1), e1a, e1b);
+    f2_split(f2_fma(X2, C2, NB2), e2a, e2b);
     float p1a = ex2(e1a), p1b = ex2(e1b), p2a = ex2(e2a), p2b = ex2(e2b);
     if (kMask) {
       if (k > lim_rel) { p1a = 0.f; p2a = 0.f; }
@@ -98,7 +104,7 @@ __device__ __forceinline__ void fold_chunk(RowStats& st, const uint32_t (&x1u)[3
     const uint64_t P1 = f2(p1a, p1b);
     L1 = f2_add(L1, P1);
     L2 = f2_add(L2, f2(p2a, p2b));
-    ACC = f2_fma(P1, f2_sub(X1, X2), ACC);
+    ACC = f2_fma(P1, f2_fma(X2, NR, X1), ACC);
   }
   float l1a, l1b, l2a, l2b, aca, acb;
   f2_split(L1, l1a, l1b);
@@ -242,7 +248,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const int wg = warp >> 2;
     const int row = (warp & 3) * 32 + lane;
     const int grow = q0 + row;
-    const float c = a.scale * kLog2e;
+    const float c1 = a.scale1 * kLog2e, c2 = a.scale2 * kLog2e, nrho = -a.scale2 / a.scale1;
     const int lim = a.causal ? min(grow + off, a.NK - 1) : a.NK - 1;  // last visible key
     const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
     RowStats st{kNegBig, kNegBig, 0.f, 0.f, 0.f};
@@ -265,9 +271,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           if (lane == 0) mbar_arrive(bar_sempty(b));
         }
         if (need_mask)
-          fold_chunk<true>(st, x1, x2, c, lim - (k0 + col));
+          fold_chunk<true>(st, x1, x2, c1, c2, nrho, lim - (k0 + col));
         else
-          fold_chunk<false>(st, x1, x2, c, 0);
+          fold_chunk<false>(st, x1, x2, c1, c2, nrho, 0);
       }
     }
     // merge the column shares of every row (warpgroups 1.. -> warpgroup 0)
@@ -289,31 +295,31 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         M1 = fmaxf(M1, mg[w * kTile * 5 + row * 5 + 0]);
         M2 = fmaxf(M2, mg[w * kTile * 5 + row * 5 + 3]);
       }
-      const float e1 = ex2((st.m1 - M1) * c), e2 = ex2((st.m2 - M2) * c);
+      const float e1 = ex2((st.m1 - M1) * c1), e2 = ex2((st.m2 - M2) * c2);
       float L1 = st.l1 * e1, A = st.acc * e1, L2 = st.l2 * e2;
 #pragma unroll
       for (int w = 0; w < kStatWGs - 1; ++w) {
         const float* o = mg + w * kTile * 5 + row * 5;
-        const float f1 = ex2((o[0] - M1) * c), f2 = ex2((o[3] - M2) * c);
-        L1 = fmaf(o[1], f1, L1);
-        A = fmaf(o[2], f1, A);
-        L2 = fmaf(o[4], f2, L2);
+        const float g1 = ex2((o[0] - M1) * c1), g2 = ex2((o[3] - M2) * c2);
+        L1 = fmaf(o[1], g1, L1);
+        A = fmaf(o[2], g1, A);
+        L2 = fmaf(o[4], g2, L2);
       }
       const size_t rows = size_t(a.BH) * a.NQ;
       const size_t idx = size_t(bh) * a.NQ + grow;
       if (a.partial != nullptr) {
         float* p = a.partial + size_t(split) * 5 * rows + idx;
-        p[0 * rows] = a.scale * M1;
+        p[0 * rows] = a.scale1 * M1;
         p[1 * rows] = L1;
-        p[2 * rows] = a.scale * A;
-        p[3 * rows] = a.scale * M2;
+        p[2 * rows] = a.scale1 * A;
+        p[3 * rows] = a.scale2 * M2;
         p[4 * rows] = L2;
       } else {
-        const float lse1 = a.scale * M1 + logf(L1);
-        const float lse2 = a.scale * M2 + logf(L2);
+        const float lse1 = a.scale1 * M1 + logf(L1);
+        const float lse2 = a.scale2 * M2 + logf(L2);
         a.lse1[idx] = lse1;
         a.lse2[idx] = lse2;
-        a.kl[idx] = a.scale * A / L1 + lse2 - lse1;
+        a.kl[idx] = a.scale1 * A / L1 + lse2 - lse1;
       }
     }
   }

@@ -17,7 +17,7 @@ struct TMaps {
 
 struct FwdArgs {
   int BH, NQ, NK, causal, num_splits;
-  float scale;
+  float scale1, scale2;  // S1 = scale1 Q1 K1^T, S2 = scale2 Q2 K2^T
   float* kl;
   float* lse1;
   float* lse2;
@@ -27,7 +27,7 @@ struct FwdArgs {
 
 struct BwdArgs {
   int BH, NQ, NK, causal, mode;
-  float scale;
+  float scale1, scale2;
   const float* kl;
   const float* lse1;
   const float* lse2;

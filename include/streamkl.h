@@ -28,7 +28,8 @@
  * Streams: every call is asynchronous and stream-ordered on `stream`
  *   (a cudaStream_t; NULL = legacy default stream).  Errors detected on the
  *   host return before anything is enqueued.
- * Scale: 0 < scale <= 1e4 and finite; S = scale * Q K^T on both sides.
+ * Scale: 0 < scale <= 1e4 and finite; S = scale * Q K^T on both sides (the
+ *   *_scaled calls take one scale per side, each under the same rule).
  * Causal: key j is visible to query i iff j <= i + (NK - NQ) (bottom-right
  *   aligned; j <= i when NQ == NK).  causal with NQ > NK is INVALID_ARG.
  * Head dims: d1, d2 in {64, 128}, independently (UNSUPPORTED otherwise).
@@ -144,6 +145,30 @@ int streamkl_bwd(const void* q1, const void* k1, const void* q2, const void* k2,
                  int B, int H, int NQ, int NK, int d1, int d2, float scale, int causal,
                  const float* kl, const float* lse1, const float* lse2, const float* dkl,
                  int mode, int deterministic, float* dq, float* dk, streamkl_stream_t stream);
+
+/*
+ * Per-side softmax scales: S1 = scale1 * Q1 K1^T and S2 = scale2 * Q2 K2^T,
+ * for a student whose head dimension or temperature differs from the
+ * teacher's.  (The pages use one scale; a second one is a widening of the
+ * method, taken as the plain reading: each softmax keeps its own logits.)
+ * Arguments, layout, ownership and errors are those of the single-scale
+ * calls, which are these with scale1 = scale2 = scale.  In the backward the
+ * gradient side's scale multiplies dQ and dK (s2 in mode P2, s1 in mode P1);
+ * kl, lse1, lse2 must come from a forward with the same two scales.
+ */
+int streamkl_fwd_scaled(const void* q1, const void* k1, const void* q2, const void* k2,
+                        int B, int H, int NQ, int NK, int d1, int d2, float scale1, float scale2,
+                        int causal, float* kl, float* lse1, float* lse2, streamkl_stream_t stream);
+int streamkl_fwd_splitk_scaled(const void* q1, const void* k1, const void* q2, const void* k2,
+                               int B, int H, int NQ, int NK, int d1, int d2, float scale1,
+                               float scale2, int causal, int num_splits, void* workspace,
+                               size_t workspace_bytes, float* kl, float* lse1, float* lse2,
+                               streamkl_stream_t stream);
+int streamkl_bwd_scaled(const void* q1, const void* k1, const void* q2, const void* k2,
+                        int B, int H, int NQ, int NK, int d1, int d2, float scale1, float scale2,
+                        int causal, const float* kl, const float* lse1, const float* lse2,
+                        const float* dkl, int mode, int deterministic, float* dq, float* dk,
+                        streamkl_stream_t stream);
 
 /* Static, NUL-terminated description of a status value. */
 const char* streamkl_status_string(int status);

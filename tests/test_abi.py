@@ -132,3 +132,20 @@ def test_noalloc_constant_and_host_refusal(L):
     assert f(A, A, A, A, 1, 16, 2048, 128, 64, 64, 0.125, 0, 1024, A, A, A, None) == skl.STREAMKL_INVALID_ARG
     assert f(A, A, A, A, 1, 1, 128, 128, 64, 64, 0.125, 0, 0, A, A, A, None) == skl.STREAMKL_INVALID_ARG
     assert f(0, 0, 0, 0, 1, 1, 0, 128, 64, 64, 0.125, 0, 2, 0, 0, 0, None) == skl.STREAMKL_OK  # no rows
+
+
+@pytest.mark.parametrize("s1,s2", [(0.125, 0.0), (0.125, -1.0), (0.125, float("nan")), (0.125, 2e4),
+                                   (0.0, 0.125), (float("inf"), 0.125)])
+def test_scaled_calls_validate_both_scales(L, s1, s2):
+    out = (A, A, A)
+    assert L.streamkl_fwd_scaled(A, A, A, A, 1, 1, 128, 128, 64, 64, s1, s2, 0, *out, None) == \
+        skl.STREAMKL_INVALID_ARG
+    need = skl.streamkl_fwd_splitk_workspace_bytes(1, 1, 128, 2)
+    assert L.streamkl_fwd_splitk_scaled(A, A, A, A, 1, 1, 128, 128, 64, 64, s1, s2, 0, 2, A, need,
+                                        *out, None) == skl.STREAMKL_INVALID_ARG
+    assert L.streamkl_bwd_scaled(A, A, A, A, 1, 1, 128, 128, 64, 64, s1, s2, 0, A, A, A, A, 0, 0, A, A,
+                                 None) == skl.STREAMKL_INVALID_ARG
+
+
+def test_scaled_calls_empty_problem_is_noop(L):
+    assert L.streamkl_fwd_scaled(0, 0, 0, 0, 1, 1, 0, 128, 64, 64, 0.1, 0.2, 0, 0, 0, 0, None) == skl.STREAMKL_OK
