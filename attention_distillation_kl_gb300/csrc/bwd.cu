@@ -209,7 +209,6 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
       if (n > 0 && mbar_wait_polled(bar(L::B_KFULL), 0, ctl)) {
         for (; t < n; ++t) {
           if (!mbar_wait_polled(bar(L::B_DSFULL), t & 1, ctl)) break;
-          if (kDq && a.write_dq && !mbar_wait_polled(bar(L::B_DQEMPTY), (t & 1) ^ 1, ctl)) break;
           tc_fence_after();
           const uint64_t qgn = sdesc_sw128(sb + L::oQg + (t & 1) * L::kQg, kTile * 128, 1024);
 #pragma unroll
@@ -218,6 +217,9 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
                         (t > 0 || kk > 0) ? 1u : 0u);
           mma_commit(1u, bar(L::B_QGEMPTY0 + (t & 1)));  // Q_g(t) may be reloaded
           if (kDq && a.write_dq) {
+            // dK and the Q_g release above did not wait for the dQ accumulator
+            if (!mbar_wait_polled(bar(L::B_DQEMPTY), (t & 1) ^ 1, ctl)) break;
+            tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < kTile / 16; ++kk)
               mma_bf16_ss(1u, t_dq, sdesc_add(dsk, (kk >> 2) * (kTile * 128) + (kk & 3) * 32),
