@@ -205,6 +205,47 @@ def ex2_rate(skl):
     return blocks * 256 * iters * 8 / best
 
 
+def key_split_timing(skl, stream):
+    w = WORKLOADS["c5"]
+    dev = [t.cuda() for t in generate(w)]
+    kl = torch.empty(w.B, w.H, w.NQ, device="cuda")
+    l1, l2 = torch.empty_like(kl), torch.empty_like(kl)
+    dq = torch.empty(w.B, w.H, w.NQ, w.d2, device="cuda")
+    dk = torch.empty(w.B, w.H, w.NK, w.d2, device="cuda")
+    dkl = torch.ones(w.B, w.H, w.NQ, device="cuda")
+    heur = skl.streamkl_suggest_splits(w.B, w.H, w.NQ, w.NK, w.causal)
+    ws = torch.empty(skl.streamkl_fwd_splitk_workspace_bytes(w.B, w.H, w.NQ, max(8, heur)), dtype=torch.uint8,
+                     device="cuda")
+
+    def timed(fn, reps=4):
+        fn()
+        ts = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return float(np.median(ts))
+
+    f_fwd, f_bwd = flops(w)
+    out = {"workload": f"c5: B={w.B} H={w.H} NQ=NK={w.NQ} d1={w.d1} d2={w.d2} causal"}
+    out["fwd_ms"] = timed(lambda: skl.streamkl_fwd(*dev, w.scale, w.causal, kl, l1, l2))
+    out["fwd_splitk8_ms"] = timed(lambda: skl.streamkl_fwd_splitk(*dev, w.scale, w.causal, 8, ws, kl, l1, l2))
+    out["suggested_splits"] = heur
+    out["fwd_splitk_suggested_ms"] = timed(lambda: skl.streamkl_fwd_splitk(*dev, w.scale, w.causal, heur, ws, kl,
+                                                                           l1, l2))
+    out["bwd_p2_ms"] = timed(lambda: skl.streamkl_bwd(*dev, w.scale, w.causal, kl, l1, l2, dkl,
+                                                      skl.STREAMKL_GRAD_P2, False, dq, dk))
+    out["fwd_tflops"] = f_fwd / (out["fwd_ms"] * 1e-3) / 1e12
+    out["fwd_splitk8_tflops"] = f_fwd / (out["fwd_splitk8_ms"] * 1e-3) / 1e12
+    out["bwd_p2_tflops"] = f_bwd / (out["bwd_p2_ms"] * 1e-3) / 1e12
+    del dev, dq, dk, ws
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_mine(args, rank, world, local):
     import attention_distillation_kl_gb300 as skl  # raises if the CUDA library is missing
     torch.cuda.set_device(local)
@@ -328,6 +369,11 @@ def run_mine(args, rank, world, local):
     extra_bytes = free0 - torch.cuda.mem_get_info()[0]
     f_p1 = (2 * (w.d1 + w.d2) + 4 * w.d1) * w.pairs
 
+    # key-split forward (and the d2 = 64 backward) on the 131K-token,
+    # 4-head workload, timed on their own after the step loop: forced 8
+    # splits, the heuristic's choice, and the plain forward for comparison
+    c5 = key_split_timing(skl, stream) if rank == 0 and world == 1 and not args.no_cpu_baseline else None
+
     rate = ex2_rate(skl)
     burst, sustained, _hbm, src = peaks()
     pairs = w.pairs
@@ -361,6 +407,7 @@ def run_mine(args, rank, world, local):
             "bwd_p1_ms": p1_ms, "bwd_p1_tflops": f_p1 / (p1_ms * 1e-3) / 1e12,
             "bwd_p1_roofline_frac": max(f_p1 / (sustained * 1e12), pairs / rate) / (p1_ms * 1e-3),
             "extra_device_bytes": extra_bytes,
+            "key_split_131k": c5,
             "ex2_per_s": rate,
             "roofline": {"bound": "tensor", "achieved": bwd_tf if dom == "bwd" else fwd_tf,
                          "peak": sustained, "unit": "TFLOP/s",
