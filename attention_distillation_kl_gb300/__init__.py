@@ -54,6 +54,8 @@ _SIGS = {
                                         _P, _P, _P, _P]),
     "streamkl_bwd_scaled": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _F, _I, _P, _P, _P, _P, _I,
                                  _I, _P, _P, _P]),
+    "streamkl_bwd_both": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _F, _I, _P, _P, _P, _P, _I,
+                               _P, _P, _P, _P, _P]),
     "streamkl_status_string": (ctypes.c_char_p, [_I]),
     "streamkl_get_device_status": (_I, []),
     "streamkl_probe_ex2": (_I, [_P, _I, _I, _P]),
@@ -259,6 +261,25 @@ def streamkl_bwd_scaled(q1, k1, q2, k2, scale1, scale2, causal, kl, lse1, lse2, 
                                      _stream(stream)),
            "streamkl_bwd_scaled")
     return dq, dk
+
+
+def streamkl_bwd_both(q1, k1, q2, k2, scale1, scale2, causal, kl, lse1, lse2, dkl, deterministic=False,
+                      dq1=None, dk1=None, dq2=None, dk2=None, stream=None):
+    """(dQ1, dK1, dQ2, dK2) fp32: the gradients of sum(dkl * KL) on both sides."""
+    B, H, NQ, NK, d1, d2 = _dims(q1, k1, q2, k2)
+    for name, t in (("kl", kl), ("lse1", lse1), ("lse2", lse2), ("dkl", dkl)):
+        _out(t, (B, H, NQ), q1.device, name)
+    dq1 = _out(dq1, (B, H, NQ, d1), q1.device, "dq1")
+    dk1 = _out(dk1, (B, H, NK, d1), q1.device, "dk1")
+    dq2 = _out(dq2, (B, H, NQ, d2), q1.device, "dq2")
+    dk2 = _out(dk2, (B, H, NK, d2), q1.device, "dk2")
+    _check(lib().streamkl_bwd_both(q1.data_ptr(), k1.data_ptr(), q2.data_ptr(), k2.data_ptr(),
+                                   B, H, NQ, NK, d1, d2, float(scale1), float(scale2), int(bool(causal)),
+                                   kl.data_ptr(), lse1.data_ptr(), lse2.data_ptr(), dkl.data_ptr(),
+                                   int(bool(deterministic)), dq1.data_ptr(), dk1.data_ptr(), dq2.data_ptr(),
+                                   dk2.data_ptr(), _stream(stream)),
+           "streamkl_bwd_both")
+    return dq1, dk1, dq2, dk2
 
 
 def streamkl_get_device_status():

@@ -15,7 +15,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libstreamkl.so")
-SOURCES = ["api.cu", "fwd.cu", "bwd.cu", "static_ws.cu"]
+SOURCES = ["api.cu", "fwd.cu", "bwd.cu", "bwd_both.cu", "static_ws.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

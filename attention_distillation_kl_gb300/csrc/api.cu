@@ -245,6 +245,43 @@ int streamkl_bwd(const void* q1, const void* k1, const void* q2, const void* k2,
                              mode, deterministic, dq, dk, stream);
 }
 
+int streamkl_bwd_both(const void* q1, const void* k1, const void* q2, const void* k2, int B, int H, int NQ,
+                      int NK, int d1, int d2, float scale1, float scale2, int causal, const float* kl,
+                      const float* lse1, const float* lse2, const float* dkl, int deterministic, float* dq1,
+                      float* dk1, float* dq2, float* dk2, streamkl_stream_t stream) {
+  bool empty = false;
+  int s = check_problem(q1, k1, q2, k2, B, H, NQ, NK, d1, d2, scale1, causal, &empty);
+  if (s == STREAMKL_OK && !scale_ok(scale2)) s = STREAMKL_INVALID_ARG;
+  if (s != STREAMKL_OK) return s;
+  if (deterministic != 0 && deterministic != 1) return STREAMKL_INVALID_ARG;
+  if (d1 != 64 || d2 != 64 || deterministic || empty) {
+    // one recompute per side (the single-side kernels; they also handle empty problems)
+    s = streamkl_bwd_scaled(q1, k1, q2, k2, B, H, NQ, NK, d1, d2, scale1, scale2, causal, kl, lse1, lse2,
+                            dkl, STREAMKL_GRAD_P2, deterministic, dq2, dk2, stream);
+    if (s != STREAMKL_OK) return s;
+    return streamkl_bwd_scaled(q1, k1, q2, k2, B, H, NQ, NK, d1, d2, scale1, scale2, causal, kl, lse1, lse2,
+                               dkl, STREAMKL_GRAD_P1, deterministic, dq1, dk1, stream);
+  }
+  if (!kl || !lse1 || !lse2 || !dkl || !dq1 || !dk1 || !dq2 || !dk2) return STREAMKL_INVALID_ARG;
+  if (!aligned16(kl) || !aligned16(lse1) || !aligned16(lse2) || !aligned16(dkl) || !aligned16(dq1) ||
+      !aligned16(dk1) || !aligned16(dq2) || !aligned16(dk2))
+    return STREAMKL_INVALID_ARG;
+  if ((s = device_ok()) != STREAMKL_OK) return s;
+  skl::TMaps m{};
+  if ((s = make_maps(&m, q1, k1, q2, k2, B * H, NQ, NK, d1, d2)) != STREAMKL_OK) return s;
+  if (!make_map_dq(&m.dq, dq1, (long long)B * H, NQ, 64) || !make_map_dq(&m.dq2, dq2, (long long)B * H, NQ, 64))
+    return STREAMKL_CUDA_ERROR;
+  int* st = status_ptr();
+  if (!st) return STREAMKL_CUDA_ERROR;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const size_t dq_bytes = size_t(B) * H * NQ * 64 * 4;
+  if (cudaMemsetAsync(dq1, 0, dq_bytes, cs) != cudaSuccess || cudaMemsetAsync(dq2, 0, dq_bytes, cs) != cudaSuccess)
+    return STREAMKL_CUDA_ERROR;
+  skl::BwdArgs a{B * H, NQ, NK, causal, STREAMKL_GRAD_P2, scale1, scale2, kl, lse1, lse2, dkl, dq1, dk1, st, 1,
+                 dq2, dk2};
+  return as_status(skl::launch_bwd_both(m, a, cs));
+}
+
 const char* streamkl_status_string(int status) {
   switch (status) {
     case STREAMKL_OK: return "ok";

@@ -79,4 +79,47 @@ __device__ __forceinline__ void ds_chunk_row(const uint32_t (&x1u)[32], const ui
   }
 }
 
+// Writes 32 bf16 columns [col, col + 32) (col a multiple of 32) of row r of
+// such an operand from 16 packed registers.
+__device__ __forceinline__ void store_cols32_sw128(uint32_t base, int r, int col, const uint32_t (&v)[16]) {
+  const uint32_t rb = base + (col >> 6) * (kTile * 128) + (r >> 3) * 1024 + (r & 7) * 128;
+  const int c0 = (col & 63) >> 3;  // first 16-byte chunk of the 32 columns
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    st_shared_v4(rb + (((c0 + k) ^ (r & 7)) << 4), v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+}
+
+// Both gradient sides from one pair of exponentials: for 32 key columns of
+// one query row, dS2 = s2 dKL (P2 - P1) into out2 and dS1 = s1 dKL P1 (r - KL)
+// into out1 (packed bf16 pairs).  Per-row parameters as in ds_chunk_row:
+// NA = -LSE1 log2e, NB2 = -LSE2 log2e, NB1 = -(LSE1 - LSE2 + KL),
+// W2 = s2 dKL, W1 = s1 dKL; constants C1, C2, S1, NR as there.
+template <bool kMask>
+__device__ __forceinline__ void ds_chunk_row_both(const uint32_t (&x1u)[32], const uint32_t (&x2u)[32],
+                                                  uint64_t C1, uint64_t C2, uint64_t S1, uint64_t NR,
+                                                  uint64_t NA, uint64_t NB2, uint64_t NB1, uint64_t W2,
+                                                  uint64_t W1, int lim_rel, uint32_t (&out1)[16],
+                                                  uint32_t (&out2)[16]) {
+#pragma unroll
+  for (int k = 0; k < 32; k += 2) {
+    const uint64_t X1 = f2(__uint_as_float(x1u[k]), __uint_as_float(x1u[k + 1]));
+    const uint64_t X2 = f2(__uint_as_float(x2u[k]), __uint_as_float(x2u[k + 1]));
+    float ea, eb;
+    f2_split(f2_fma(X1, C1, NA), ea, eb);
+    const uint64_t P1 = f2(ex2(ea), ex2(eb));
+    f2_split(f2_fma(X2, C2, NB2), ea, eb);
+    const uint64_t D2 = f2_mul(W2, f2_sub(f2(ex2(ea), ex2(eb)), P1));
+    const uint64_t D1 = f2_mul(f2_mul(W1, P1), f2_fma(f2_fma(X2, NR, X1), S1, NB1));
+    float a1, b1, a2, b2;
+    f2_split(D1, a1, b1);
+    f2_split(D2, a2, b2);
+    if (kMask) {
+      if (k > lim_rel) a1 = a2 = 0.f;
+      if (k + 1 > lim_rel) b1 = b2 = 0.f;
+    }
+    out1[k / 2] = pack_bf16(a1, b1);
+    out2[k / 2] = pack_bf16(a2, b2);
+  }
+}
+
 }  // namespace skl

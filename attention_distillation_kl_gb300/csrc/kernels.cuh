@@ -13,6 +13,7 @@ constexpr int kTile = 128;  // query and key tile: 128 rows = 128 TMEM lanes
 struct TMaps {
   CUtensorMap q1, k1, q2, k2;  // [BH][N][d] bf16, boxes of 64 x 128, 128-byte swizzle
   CUtensorMap dq;              // [BH][NQ][dg] fp32, boxes of 16 x 32, 64-byte swizzle (fused backward)
+  CUtensorMap dq2;             // the second side's dQ (both-sides backward)
 };
 
 struct FwdArgs {
@@ -36,6 +37,8 @@ struct BwdArgs {
   float* dk;  // fp32 [BH][NK][dg]
   int* status;
   int write_dq;  // 0: skip the dQ product (deterministic two-pass uses its own dQ kernel)
+  float* dq2;    // both-sides backward: dQ2, dK2 (dq, dk then hold dQ1, dK1)
+  float* dk2;
 };
 
 // Each returns a cudaError_t value (cudaSuccess = 0).
@@ -44,6 +47,7 @@ int launch_splitk_reduce(const float* partial, int rows, int num_splits, float* 
                          float* lse2, cudaStream_t st);
 int launch_bwd_fused(const TMaps& m, int d1, int d2, const BwdArgs& a, cudaStream_t st);
 int launch_bwd_dq(const TMaps& m, int d1, int d2, const BwdArgs& a, cudaStream_t st);
+int launch_bwd_both(const TMaps& m, const BwdArgs& a, cudaStream_t st);  // d1 = d2 = 64
 int launch_ex2_probe(float* out, int blocks, int iters, cudaStream_t st);
 int launch_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t st);
 

@@ -170,6 +170,24 @@ int streamkl_bwd_scaled(const void* q1, const void* k1, const void* q2, const vo
                         const float* dkl, int mode, int deterministic, float* dq, float* dk,
                         streamkl_stream_t stream);
 
+/*
+ * Both-sides backward: the gradients of sum_i dkl_i * KL_i with respect to
+ * both distributions (dq1, dk1 with head dim d1; dq2, dk2 with d2; fp32,
+ * fully overwritten), from one recompute of S1 and S2 per tile pair when
+ * d1 = d2 = 64 and deterministic = 0.  (A widening of the method: the
+ * article's two modes share P1 and P2.)  Other head dimensions, where the
+ * four accumulators do not fit beside S1 and S2 in tensor memory, and the
+ * deterministic mode run the single-side backward twice (mode P2, then mode
+ * P1) and return what those return.  Arguments, ownership and errors are
+ * otherwise those of streamkl_bwd_scaled; kl, lse1, lse2 must come from a
+ * forward with the same two scales.
+ */
+int streamkl_bwd_both(const void* q1, const void* k1, const void* q2, const void* k2,
+                      int B, int H, int NQ, int NK, int d1, int d2, float scale1, float scale2,
+                      int causal, const float* kl, const float* lse1, const float* lse2,
+                      const float* dkl, int deterministic, float* dq1, float* dk1, float* dq2,
+                      float* dk2, streamkl_stream_t stream);
+
 /* Static, NUL-terminated description of a status value. */
 const char* streamkl_status_string(int status);
 

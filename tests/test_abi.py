@@ -149,3 +149,14 @@ def test_scaled_calls_validate_both_scales(L, s1, s2):
 
 def test_scaled_calls_empty_problem_is_noop(L):
     assert L.streamkl_fwd_scaled(0, 0, 0, 0, 1, 1, 0, 128, 64, 64, 0.1, 0.2, 0, 0, 0, 0, None) == skl.STREAMKL_OK
+
+
+def test_bwd_both_validation(L):
+    f = L.streamkl_bwd_both
+    base = (A, A, A, A, 1, 1, 128, 128, 64, 64)
+    tail = (A, A, A, A)
+    assert f(*base, 0.125, 0.0, 0, *tail, 0, A, A, A, A, None) == skl.STREAMKL_INVALID_ARG     # scale2
+    assert f(*base, 0.125, 0.125, 0, *tail, 2, A, A, A, A, None) == skl.STREAMKL_INVALID_ARG   # deterministic flag
+    assert f(*base, 0.125, 0.125, 0, *tail, 0, A, A, 0, A, None) == skl.STREAMKL_INVALID_ARG   # null dq2
+    assert f(*base, 0.125, 0.125, 0, *tail, 0, A, A, A, A + 4, None) == skl.STREAMKL_INVALID_ARG  # misaligned dk2
+    assert f(A, A, A, A, 1, 1, 128, 128, 96, 64, 0.1, 0.1, 0, *tail, 0, A, A, A, A, None) == skl.STREAMKL_UNSUPPORTED
