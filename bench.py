@@ -246,6 +246,41 @@ def key_split_timing(skl, stream):
     return out
 
 
+def both_sides_timing(skl, stream):
+    """Both-sides backward in one pass against the two single-side passes,
+    on a d = 64 problem (16K tokens x 32 heads, causal)."""
+    from attention_distillation_kl_gb300.workloads import Workload
+    w = Workload("both-d64", 1, 32, 16384, 16384, 64, 64, True, 0.125, "independent", 0.0, 1.0, 1006)
+    dev = [t.cuda() for t in generate(w)]
+    kl, l1, l2 = skl.streamkl_fwd(*dev, w.scale, w.causal)
+    dkl = torch.ones_like(kl)
+    bufs = [torch.empty(w.B, w.H, n, 64, device="cuda") for n in (w.NQ, w.NK, w.NQ, w.NK)]
+
+    def timed(fn, reps=4):
+        fn()
+        ts = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return float(np.median(ts))
+
+    out = {"workload": f"B={w.B} H={w.H} NQ=NK={w.NQ} d1=d2=64 causal"}
+    out["bwd_p2_ms"] = timed(lambda: skl.streamkl_bwd(*dev, w.scale, w.causal, kl, l1, l2, dkl,
+                                                      skl.STREAMKL_GRAD_P2, False, bufs[2], bufs[3]))
+    out["bwd_p1_ms"] = timed(lambda: skl.streamkl_bwd(*dev, w.scale, w.causal, kl, l1, l2, dkl,
+                                                      skl.STREAMKL_GRAD_P1, False, bufs[0], bufs[1]))
+    out["bwd_both_ms"] = timed(lambda: skl.streamkl_bwd_both(*dev, w.scale, w.scale, w.causal, kl, l1, l2, dkl,
+                                                             False, *bufs))
+    out["bwd_both_tflops"] = (2 * 128 + 4 * 64 * 2) * w.pairs / (out["bwd_both_ms"] * 1e-3) / 1e12
+    del dev, bufs
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_mine(args, rank, world, local):
     import attention_distillation_kl_gb300 as skl  # raises if the CUDA library is missing
     torch.cuda.set_device(local)
@@ -373,6 +408,7 @@ def run_mine(args, rank, world, local):
     # 4-head workload, timed on their own after the step loop: forced 8
     # splits, the heuristic's choice, and the plain forward for comparison
     c5 = key_split_timing(skl, stream) if rank == 0 and world == 1 and not args.no_cpu_baseline else None
+    both = both_sides_timing(skl, stream) if rank == 0 and world == 1 and not args.no_cpu_baseline else None
 
     rate = ex2_rate(skl)
     burst, sustained, _hbm, src = peaks()
@@ -408,6 +444,7 @@ def run_mine(args, rank, world, local):
             "bwd_p1_roofline_frac": max(f_p1 / (sustained * 1e12), pairs / rate) / (p1_ms * 1e-3),
             "extra_device_bytes": extra_bytes,
             "key_split_131k": c5,
+            "both_sides_d64": both,
             "ex2_per_s": rate,
             "roofline": {"bound": "tensor", "achieved": bwd_tf if dom == "bwd" else fwd_tf,
                          "peak": sustained, "unit": "TFLOP/s",
