@@ -18,7 +18,7 @@ Notation (the pages' own): S1 = s1*Q1 K1^T, S2 = s2*Q2 K2^T, P1 = softmax(S1),
 P2 = softmax(S2) row-wise over the visible keys, KL_i = sum_j P1_ij
 log(P1_ij / P2_ij), LSE_k = log sum_j exp(S_k,ij).
 
-Readings taken where the pages are silent (each is listed in the design doc):
+Readings taken where the pages are silent:
   * one softmax scale ``s`` multiplies both logit matrices by default; a
     second scale (``scale2``) may be given for the S2 side, e.g. a student
     with another head dimension (every function takes ``scale2=None``,
