@@ -119,10 +119,16 @@ def generate(w: Workload, heads=None):
 
 def generate_dkl(w: Workload, kind: str = "ones", seed: int = 0) -> torch.Tensor:
     """Upstream gradient dL/dKL, fp32 [B, H, NQ]: all ones (the gradient of
-    sum(KL)), or U(0.5, 1.5) to exercise per-row indexing."""
+    sum(KL)), U(0.5, 1.5) to exercise per-row indexing ("uniform"), or
+    U(-1.5, 1.5) with every fifth row exactly 0 ("signed": a loss that weights
+    some rows negatively or not at all)."""
     if kind == "ones":
         return torch.ones((w.B, w.H, w.NQ), dtype=torch.float32)
     g = np.random.Generator(np.random.PCG64([w.seed, 7919, seed]))
+    if kind == "signed":
+        v = g.uniform(-1.5, 1.5, size=(w.B, w.H, w.NQ))
+        v[..., ::5] = 0.0
+        return torch.from_numpy(v.astype(np.float32))
     return torch.from_numpy(g.uniform(0.5, 1.5, size=(w.B, w.H, w.NQ)).astype(np.float32))
 
 

@@ -65,3 +65,21 @@ def test_one_pass_agrees_with_the_two_single_side_calls():
     for got, want in ((dq1, sq1), (dk1, sk1), (dq2, sq2), (dk2, sk2)):
         g, r = np_(got), np_(want)
         assert np.linalg.norm(g - r) <= 1e-5 * np.linalg.norm(r) + 1e-30
+
+
+def test_both_sides_with_signed_upstream_gradient():
+    w = Workload("both", 1, 2, 300, 300, 64, 64, True, 0.125, "independent", 0.0, 1.2, 97)
+    host, dev = inputs(w)
+    dkl = generate_dkl(w, "signed")
+    kl, l1, l2 = skl.streamkl_fwd(*dev, w.scale, w.causal)
+    got = skl.streamkl_bwd_both(*dev, w.scale, w.scale, w.causal, kl, l1, l2, dkl.cuda())
+    torch.cuda.synchronize()
+    f64 = [to_f64(t) for t in host]
+    d64 = to_f64(dkl)
+    r1 = oracle.backward(*f64, w.scale, w.causal, d64, oracle.MODE_P1)
+    r2 = oracle.backward(*f64, w.scale, w.causal, d64, oracle.MODE_P2)
+    for out, want, g in ((got[:2], r1, 0), (got[2:], r2, 2)):
+        for h in range(w.H):
+            fl = grad_floor(w.scale, d64[0, h], f64[g][0, h], f64[g + 1][0, h])
+            grad_close(np_(out[0])[0, h], want[0][0, h], fl)
+            grad_close(np_(out[1])[0, h], want[1][0, h], fl)

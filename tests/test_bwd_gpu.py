@@ -140,3 +140,14 @@ def test_large_workload_sampled(name, mode):
         first = 0
     rdk = oracle.backward_dk_keys(*f, w.scale, w.causal, dk_all[b, h], omode, keys, first_row=first)
     assert frob_rel(gdk[b, h, keys], rdk) <= GRAD_RTOL, (name, "dk")
+
+
+@pytest.mark.parametrize("det", [False, True], ids=["fused", "deterministic"])
+@pytest.mark.parametrize("mode", MODES, ids=["P2", "P1"])
+@pytest.mark.parametrize("shape", [(1, 2, 300, 300, 128, 128, True), (2, 1, 200, 333, 64, 128, False)],
+                         ids=["300-causal", "200x333"])
+def test_signed_upstream_gradient(shape, mode, det):
+    """dKL may be negative or zero on some rows (any loss that weights rows)."""
+    B, H, NQ, NK, d1, d2, causal = shape
+    w = Workload("signed", B, H, NQ, NK, d1, d2, causal, 1.0 / np.sqrt(d1), "independent", 0.0, 1.2, 81)
+    check_full(w, mode, det, "signed")
