@@ -35,17 +35,21 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// [BH][N][d] bf16 viewed as a 3-D tensor; boxes of 64 elements x 128 rows x 1,
-// 128-byte swizzle.  Rows past N read as zeros.
+// [BH][N][d] bf16 viewed as a 3-D tensor; boxes of 64 elements x 128 rows x 1
+// with the 128-byte swizzle, or for d = 32 one box of 32 elements x 128 rows
+// x 1 with the 64-byte swizzle (the layouts the kernels' operand tiles
+// expect).  Rows past N read as zeros.
 bool make_map(CUtensorMap* m, const void* ptr, long long BH, long long N, int d) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[3] = {cuuint64_t(d), cuuint64_t(N), cuuint64_t(BH)};
   cuuint64_t strides[2] = {cuuint64_t(d) * 2, cuuint64_t(N) * d * 2};
-  cuuint32_t box[3] = {64, cuuint32_t(skl::kTile), 1};
+  const bool narrow = d < 64;
+  cuuint32_t box[3] = {narrow ? 32u : 64u, cuuint32_t(skl::kTile), 1};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
-                  es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  narrow ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -69,7 +73,7 @@ bool scale_ok(float s) { return std::isfinite(s) && s > 0.f && s <= 1.0e4f; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-bool head_dim_ok(int d) { return d == 64 || d == 128; }
+bool head_dim_ok(int d) { return d == 32 || d == 64 || d == 128; }
 
 // Shared validation of the problem description.  Returns STREAMKL_OK, or the
 // status to report.  Sets *empty when there is no row to compute.

@@ -41,6 +41,7 @@
 #include "bwd_common.cuh"
 #include "kernels.cuh"
 #include "ptx.cuh"
+#include "tiles.cuh"
 
 namespace skl {
 
@@ -80,6 +81,10 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
   using L = BwdLayout<D1, D2, MODE>;
   constexpr int DG = L::DG, DO = L::DO;
   constexpr bool kP2 = MODE == STREAMKL_GRAD_P2;
+  using T1 = OpTile<D1>;
+  using T2 = OpTile<D2>;
+  using TO = OpTile<DO>;
+  using TG = OpTile<DG>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -132,27 +137,18 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
       tma_prefetch_desc(&tq2);
       tma_prefetch_desc(&tk2);
       mbar_arrive_expect_tx(bar(L::B_KFULL), L::kK1 + L::kK2);
-#pragma unroll
-      for (int c = 0; c < D1 / 64; ++c)
-        tma_load_3d(sb + L::oK1 + c * (kTile * 128), &tk1, bar(L::B_KFULL), c * 64, k0, bh);
-#pragma unroll
-      for (int c = 0; c < D2 / 64; ++c)
-        tma_load_3d(sb + L::oK2 + c * (kTile * 128), &tk2, bar(L::B_KFULL), c * 64, k0, bh);
+      T1::load(sb + L::oK1, &tk1, bar(L::B_KFULL), k0, bh);
+      T2::load(sb + L::oK2, &tk2, bar(L::B_KFULL), k0, bh);
       int issued = 0;
       for (int i = 0; i < n; ++i) {
         const int q0 = (qt_lo + i) * kTile;
         if (!mbar_wait_polled(bar(L::B_QOEMPTY), (i & 1) ^ 1, ctl)) break;
         mbar_arrive_expect_tx(bar(L::B_QOFULL), L::kQo);
-#pragma unroll
-        for (int c = 0; c < DO / 64; ++c)
-          tma_load_3d(sb + L::oQo + c * (kTile * 128), tqo, bar(L::B_QOFULL), c * 64, q0, bh);
+        TO::load(sb + L::oQo, tqo, bar(L::B_QOFULL), q0, bh);
         const int g = i & 1;
         if (!mbar_wait_polled(bar(L::B_QGEMPTY0 + g), ((i >> 1) & 1) ^ 1, ctl)) break;
         mbar_arrive_expect_tx(bar(L::B_QGFULL0 + g), L::kQg);
-#pragma unroll
-        for (int c = 0; c < DG / 64; ++c)
-          tma_load_3d(sb + L::oQg + g * L::kQg + c * (kTile * 128), tqg, bar(L::B_QGFULL0 + g), c * 64,
-                      q0, bh);
+        TG::load(sb + L::oQg + g * L::kQg, tqg, bar(L::B_QGFULL0 + g), q0, bh);
         issued = i + 1;
       }
       if (*abort_flag) {  // let the copies already started land before the CTA exits
@@ -168,14 +164,12 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16(128, 128, 0, 0);
       // S of one side for query tile i: Q tile (A, K-major) x K (B, K-major)
-      auto s_product = [&](int side, uint32_t qs) {
-        const uint32_t ks = sb + (side == 1 ? L::oK1 : L::oK2);
-        const uint32_t d = side == 1 ? t_s1 : t_s2;
-        const int steps = (side == 1 ? D1 : D2) / 16;
-        const uint64_t qd = sdesc_sw128(qs, 16, 1024), kd = sdesc_sw128(ks, 16, 1024);
+      auto s_product = [&](auto tile, uint32_t d, uint32_t qs, uint32_t ks) {
+        using T = decltype(tile);
+        const uint64_t qd = T::desc_k(qs), kd = T::desc_k(ks);
 #pragma unroll
-        for (int kk = 0; kk < steps; ++kk) {
-          const uint32_t o = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
+        for (int kk = 0; kk < T::kD / 16; ++kk) {
+          const uint32_t o = T::off_k(kk);
           mma_bf16_ss(1u, d, sdesc_add(qd, o), sdesc_add(kd, o), id_s, kk > 0);
         }
       };
@@ -185,11 +179,13 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
         if (!mbar_wait_polled(bar(L::B_QOFULL), i & 1, ctl)) break;
         tc_fence_after();
         // the other side first: its single Q buffer is released as early as possible
-        s_product(kP2 ? 1 : 2, sb + L::oQo);
+        if constexpr (kP2) s_product(T1{}, t_s1, sb + L::oQo, sb + L::oK1);
+        else s_product(T2{}, t_s2, sb + L::oQo, sb + L::oK2);
         mma_commit(1u, bar(L::B_QOEMPTY));
         if (!mbar_wait_polled(bar(L::B_QGFULL0 + (i & 1)), (i >> 1) & 1, ctl)) break;
         tc_fence_after();
-        s_product(kP2 ? 2 : 1, sb + L::oQg + (i & 1) * L::kQg);
+        if constexpr (kP2) s_product(T2{}, t_s2, sb + L::oQg + (i & 1) * L::kQg, sb + L::oK2);
+        else s_product(T1{}, t_s1, sb + L::oQg + (i & 1) * L::kQg, sb + L::oK1);
         mma_commit(1u, bar(L::B_SFULL));
       }
       // every MMA of every issuer has finished before TMEM is released
@@ -204,16 +200,16 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
       constexpr uint32_t id_dq = idesc_bf16(128, DG, 0, 1);  // A = dS K-major,   B = K_g N-major
       const uint64_t dsm = sdesc_sw128(sb + L::oDS, kTile * 128, 1024);  // dS^T, M-major
       const uint64_t dsk = sdesc_sw128(sb + L::oDS, 16, 1024);           // dS, K-major
-      const uint64_t kgn = sdesc_sw128(sb + (kP2 ? L::oK2 : L::oK1), kTile * 128, 1024);
+      const uint64_t kgn = TG::desc_n(sb + (kP2 ? L::oK2 : L::oK1));
       int t = 0;
       if (n > 0 && mbar_wait_polled(bar(L::B_KFULL), 0, ctl)) {
         for (; t < n; ++t) {
           if (!mbar_wait_polled(bar(L::B_DSFULL), t & 1, ctl)) break;
           tc_fence_after();
-          const uint64_t qgn = sdesc_sw128(sb + L::oQg + (t & 1) * L::kQg, kTile * 128, 1024);
+          const uint64_t qgn = TG::desc_n(sb + L::oQg + (t & 1) * L::kQg);
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_bf16_ss(1u, t_dk, sdesc_add(dsm, kk * 2048), sdesc_add(qgn, kk * 2048), id_dk,
+            mma_bf16_ss(1u, t_dk, sdesc_add(dsm, kk * 2048), sdesc_add(qgn, TG::off_n(kk)), id_dk,
                         (t > 0 || kk > 0) ? 1u : 0u);
           mma_commit(1u, bar(L::B_QGEMPTY0 + (t & 1)));  // Q_g(t) may be reloaded
           if (kDq && a.write_dq) {
@@ -223,7 +219,7 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < kTile / 16; ++kk)
               mma_bf16_ss(1u, t_dq, sdesc_add(dsk, (kk >> 2) * (kTile * 128) + (kk & 3) * 32),
-                          sdesc_add(kgn, kk * 2048), id_dq, kk > 0 ? 1u : 0u);
+                          sdesc_add(kgn, TG::off_n(kk)), id_dq, kk > 0 ? 1u : 0u);
           }
           mma_commit(1u, bar(L::B_DSEMPTY));
           if (kDq && a.write_dq) mma_commit(1u, bar(L::B_DQFULL));
@@ -237,7 +233,7 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t id_dq = idesc_bf16(128, DG, 0, 1);  // A = dS K-major, B = K_g N-major
       const uint64_t dsk = sdesc_sw128(sb + L::oDS, 16, 1024);  // dS, K-major
-      const uint64_t kgn = sdesc_sw128(sb + (kP2 ? L::oK2 : L::oK1), kTile * 128, 1024);
+      const uint64_t kgn = TG::desc_n(sb + (kP2 ? L::oK2 : L::oK1));
       if (a.write_dq && n > 0 && mbar_wait_polled(bar(L::B_KFULL), 0, ctl)) {
         for (int t = 0; t < n; ++t) {
           if (!mbar_wait_polled(bar(L::B_DSFULL), t & 1, ctl)) break;
@@ -246,7 +242,7 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk)
             mma_bf16_ss(1u, t_dq, sdesc_add(dsk, (kk >> 2) * (kTile * 128) + (kk & 3) * 32),
-                        sdesc_add(kgn, kk * 2048), id_dq, kk > 0 ? 1u : 0u);
+                        sdesc_add(kgn, TG::off_n(kk)), id_dq, kk > 0 ? 1u : 0u);
           mma_commit(1u, bar(L::B_DSEMPTY));
           mma_commit(1u, bar(L::B_DQFULL));
         }
@@ -319,9 +315,10 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
       // kDqBoxes 2 KB staging boxes per warp ([32 rows][16 fp32], 64-byte
       // swizzle: 16-byte chunk c of row r at chunk c ^ ((r / 2) % 4)), used
       // round robin so up to kDqBoxes bulk reduce-adds are in flight.  The
-      // tile is read from TMEM 64 columns at a time; the second read
+      // tile is read from TMEM kRead columns at a time; the last read
       // releases the dQ accumulator before its boxes are staged, so the
       // next dQ product does not wait for the reduce-adds.
+      constexpr int kHalves = DG >= 64 ? 2 : 1, kRead = 32 * kHalves;
       const uint32_t stage = sb + L::oStage + w4 * (kDqBoxes * 2048);
       const uint32_t swz = (lane >> 1) & 3;
       int nred = 0;
@@ -331,17 +328,17 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
         tc_fence_after();
         const int r0 = (qt_lo + i) * kTile + w4 * 32;  // first query row of this warp
 #pragma unroll
-        for (int cp = 0; cp < DG / 64; ++cp) {
-          uint32_t v[2][32];
-          tmem_ld32(t_dq + lane_off + cp * 64, v[0]);
-          tmem_ld32(t_dq + lane_off + cp * 64 + 32, v[1]);
-          if (cp == DG / 64 - 1) {
+        for (int cp = 0; cp < DG / kRead; ++cp) {
+          uint32_t v[kHalves][32];
+#pragma unroll
+          for (int x = 0; x < kHalves; ++x) tmem_ld32(t_dq + lane_off + cp * kRead + 32 * x, v[x]);
+          if (cp == DG / kRead - 1) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(L::B_DQEMPTY));
           }
 #pragma unroll
-          for (int h = 0; h < 4; ++h) {
+          for (int h = 0; h < 2 * kHalves; ++h) {
             const uint32_t box = stage + (nred % kDqBoxes) * 2048;
             // the box used kDqBoxes reduces ago has been read
             if (lane == 0) bulk_wait_read_le<kDqBoxes - 1>();
@@ -355,7 +352,7 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0 && r0 < a.NQ) {  // a box starting past NQ has nothing to add
-              tma_reduce_add_3d(&tdq, box, cp * 64 + h * 16, r0, bh);
+              tma_reduce_add_3d(&tdq, box, cp * kRead + h * 16, r0, bh);
               bulk_commit();
             }
             ++nred;
@@ -436,6 +433,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                   const BwdArgs a) {
   using L = DqLayout<D1, D2, MODE>;
   constexpr int DG = L::DG;
+  using T1 = OpTile<D1>;
+  using T2 = OpTile<D2>;
+  using TG = OpTile<DG>;
   constexpr bool kP2 = MODE == STREAMKL_GRAD_P2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -476,24 +476,16 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
       mbar_arrive_expect_tx(bar(L::B_QFULL), L::kQ1 + L::kQ2);
-#pragma unroll
-      for (int c = 0; c < D1 / 64; ++c)
-        tma_load_3d(sb + L::oQ1 + c * (kTile * 128), &tq1, bar(L::B_QFULL), c * 64, q0, bh);
-#pragma unroll
-      for (int c = 0; c < D2 / 64; ++c)
-        tma_load_3d(sb + L::oQ2 + c * (kTile * 128), &tq2, bar(L::B_QFULL), c * 64, q0, bh);
+      T1::load(sb + L::oQ1, &tq1, bar(L::B_QFULL), q0, bh);
+      T2::load(sb + L::oQ2, &tq2, bar(L::B_QFULL), q0, bh);
       int issued = 0;
       for (int j = 0; j < nkt; ++j) {
         const int s = j & 1;
         if (!mbar_wait_polled(bar(L::B_KEMPTY0 + s), ((j >> 1) & 1) ^ 1, ctl)) break;
         mbar_arrive_expect_tx(bar(L::B_KFULL0 + s), L::kStage);
         const uint32_t st = sb + L::oK + s * L::kStage;
-#pragma unroll
-        for (int c = 0; c < D1 / 64; ++c)
-          tma_load_3d(st + c * (kTile * 128), &tk1, bar(L::B_KFULL0 + s), c * 64, j * kTile, bh);
-#pragma unroll
-        for (int c = 0; c < D2 / 64; ++c)
-          tma_load_3d(st + L::kK1 + c * (kTile * 128), &tk2, bar(L::B_KFULL0 + s), c * 64, j * kTile, bh);
+        T1::load(st, &tk1, bar(L::B_KFULL0 + s), j * kTile, bh);
+        T2::load(st + L::kK1, &tk2, bar(L::B_KFULL0 + s), j * kTile, bh);
         issued = j + 1;
       }
       if (*abort_flag) {
@@ -515,7 +507,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         for (int kk = 0; kk < kTile / 16; ++kk) {
           const uint32_t ao = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
           mma_bf16_ss(1u, t_dq, sdesc_sw128(sb + L::oDS + ao, 16, 1024),
-                      sdesc_sw128(kg + kk * 2048, kTile * 128, 1024), id_dq, (t > 0 || kk > 0) ? 1u : 0u);
+                      TG::desc_n(kg + TG::off_n(kk)), id_dq, (t > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(1u, bar(L::B_DSEMPTY));
         mma_commit(1u, bar(L::B_KEMPTY0 + (t & 1)));
@@ -530,15 +522,13 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         const uint32_t k1s = sb + L::oK + s * L::kStage, k2s = k1s + L::kK1;
 #pragma unroll
         for (int kk = 0; kk < D1 / 16; ++kk) {
-          const uint32_t o = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
-          mma_bf16_ss(1u, t_s1, sdesc_sw128(sb + L::oQ1 + o, 16, 1024), sdesc_sw128(k1s + o, 16, 1024), id_s,
-                      kk > 0);
+          const uint32_t o = T1::off_k(kk);
+          mma_bf16_ss(1u, t_s1, T1::desc_k(sb + L::oQ1 + o), T1::desc_k(k1s + o), id_s, kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < D2 / 16; ++kk) {
-          const uint32_t o = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
-          mma_bf16_ss(1u, t_s2, sdesc_sw128(sb + L::oQ2 + o, 16, 1024), sdesc_sw128(k2s + o, 16, 1024), id_s,
-                      kk > 0);
+          const uint32_t o = T2::off_k(kk);
+          mma_bf16_ss(1u, t_s2, T2::desc_k(sb + L::oQ2 + o), T2::desc_k(k2s + o), id_s, kk > 0);
         }
         mma_commit(1u, bar(L::B_SFULL));
         if (j > 0 && !dq_product(j - 1)) {
@@ -643,14 +633,15 @@ static int launch_dq_t(const TMaps& m, const BwdArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-#define SKL_DISPATCH(FN)                                                                    \
-  do {                                                                                      \
-    const bool p2 = a.mode == STREAMKL_GRAD_P2;                                             \
-    if (d1 == 128 && d2 == 128) return p2 ? FN<128, 128, 0>(m, a, st) : FN<128, 128, 1>(m, a, st); \
-    if (d1 == 128 && d2 == 64) return p2 ? FN<128, 64, 0>(m, a, st) : FN<128, 64, 1>(m, a, st);    \
-    if (d1 == 64 && d2 == 128) return p2 ? FN<64, 128, 0>(m, a, st) : FN<64, 128, 1>(m, a, st);    \
-    if (d1 == 64 && d2 == 64) return p2 ? FN<64, 64, 0>(m, a, st) : FN<64, 64, 1>(m, a, st);       \
-    return cudaErrorInvalidValue;                                                           \
+#define SKL_DISPATCH_CASE(FN, A, B) \
+  if (d1 == A && d2 == B) return p2 ? FN<A, B, 0>(m, a, st) : FN<A, B, 1>(m, a, st);
+#define SKL_DISPATCH(FN)                                                                     \
+  do {                                                                                       \
+    const bool p2 = a.mode == STREAMKL_GRAD_P2;                                              \
+    SKL_DISPATCH_CASE(FN, 128, 128) SKL_DISPATCH_CASE(FN, 128, 64) SKL_DISPATCH_CASE(FN, 128, 32) \
+    SKL_DISPATCH_CASE(FN, 64, 128) SKL_DISPATCH_CASE(FN, 64, 64) SKL_DISPATCH_CASE(FN, 64, 32)    \
+    SKL_DISPATCH_CASE(FN, 32, 128) SKL_DISPATCH_CASE(FN, 32, 64) SKL_DISPATCH_CASE(FN, 32, 32)    \
+    return cudaErrorInvalidValue;                                                            \
   } while (0)
 
 int launch_bwd_fused(const TMaps& m, int d1, int d2, const BwdArgs& a, cudaStream_t st) {

@@ -29,6 +29,7 @@
 // instead of the final values; splitk_reduce_kernel merges them.
 #include "kernels.cuh"
 #include "ptx.cuh"
+#include "tiles.cuh"
 
 namespace skl {
 
@@ -121,6 +122,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                const __grid_constant__ CUtensorMap tq2, const __grid_constant__ CUtensorMap tk2,
                const FwdArgs a) {
   using L = FwdLayout<D1, D2>;
+  using T1 = OpTile<D1>;
+  using T2 = OpTile<D2>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -180,12 +183,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tma_prefetch_desc(&tq2);
       tma_prefetch_desc(&tk2);
       mbar_arrive_expect_tx(bar_q, L::kQ1 + L::kQ2);
-#pragma unroll
-      for (int c = 0; c < D1 / 64; ++c)
-        tma_load_3d(sb + L::oQ1 + c * (kTile * 128), &tq1, bar_q, c * 64, q0, bh);
-#pragma unroll
-      for (int c = 0; c < D2 / 64; ++c)
-        tma_load_3d(sb + L::oQ2 + c * (kTile * 128), &tq2, bar_q, c * 64, q0, bh);
+      T1::load(sb + L::oQ1, &tq1, bar_q, q0, bh);
+      T2::load(sb + L::oQ2, &tq2, bar_q, q0, bh);
       int issued = 0;
       for (int j = 0; j < nkt; ++j) {
         const int s = j % L::kStages;
@@ -194,12 +193,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         mbar_arrive_expect_tx(bar_kfull(s), L::kStage);
         const int k0 = (kt_lo + j) * kTile;
         const uint32_t st = sb + L::oK + s * L::kStage;
-#pragma unroll
-        for (int c = 0; c < D1 / 64; ++c)
-          tma_load_3d(st + c * (kTile * 128), &tk1, bar_kfull(s), c * 64, k0, bh);
-#pragma unroll
-        for (int c = 0; c < D2 / 64; ++c)
-          tma_load_3d(st + L::kK1 + c * (kTile * 128), &tk2, bar_kfull(s), c * 64, k0, bh);
+        T1::load(st, &tk1, bar_kfull(s), k0, bh);
+        T2::load(st + L::kK1, &tk2, bar_kfull(s), k0, bh);
         issued = j + 1;
       }
       if (*abort_flag) {  // let the copies already started land before the CTA exits
@@ -226,15 +221,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const uint32_t k1s = sb + L::oK + s * L::kStage, k2s = k1s + L::kK1;
 #pragma unroll
         for (int kk = 0; kk < D1 / 16; ++kk) {
-          const uint32_t o = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
-          mma_bf16_ss(leader, d1, sdesc_sw128(sb + L::oQ1 + o, 16, 1024), sdesc_sw128(k1s + o, 16, 1024),
-                      idesc, kk > 0);
+          const uint32_t o = T1::off_k(kk);
+          mma_bf16_ss(leader, d1, T1::desc_k(sb + L::oQ1 + o), T1::desc_k(k1s + o), idesc, kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < D2 / 16; ++kk) {
-          const uint32_t o = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
-          mma_bf16_ss(leader, d2, sdesc_sw128(sb + L::oQ2 + o, 16, 1024), sdesc_sw128(k2s + o, 16, 1024),
-                      idesc, kk > 0);
+          const uint32_t o = T2::off_k(kk);
+          mma_bf16_ss(leader, d2, T2::desc_k(sb + L::oQ2 + o), T2::desc_k(k2s + o), idesc, kk > 0);
         }
         mma_commit(leader, bar_kempty(s));
         mma_commit(leader, bar_sfull(b));
@@ -408,10 +401,12 @@ static int launch_fwd_t(const TMaps& m, const FwdArgs& a, cudaStream_t st) {
 }
 
 int launch_fwd(const TMaps& m, int d1, int d2, const FwdArgs& a, cudaStream_t st) {
-  if (d1 == 128 && d2 == 128) return launch_fwd_t<128, 128>(m, a, st);
-  if (d1 == 128 && d2 == 64) return launch_fwd_t<128, 64>(m, a, st);
-  if (d1 == 64 && d2 == 128) return launch_fwd_t<64, 128>(m, a, st);
-  if (d1 == 64 && d2 == 64) return launch_fwd_t<64, 64>(m, a, st);
+#define SKL_FWD_CASE(A, B) \
+  if (d1 == A && d2 == B) return launch_fwd_t<A, B>(m, a, st);
+  SKL_FWD_CASE(128, 128) SKL_FWD_CASE(128, 64) SKL_FWD_CASE(128, 32)
+  SKL_FWD_CASE(64, 128) SKL_FWD_CASE(64, 64) SKL_FWD_CASE(64, 32)
+  SKL_FWD_CASE(32, 128) SKL_FWD_CASE(32, 64) SKL_FWD_CASE(32, 32)
+#undef SKL_FWD_CASE
   return cudaErrorInvalidValue;
 }
 

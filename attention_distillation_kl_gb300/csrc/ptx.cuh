@@ -316,6 +316,20 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// The same descriptor for the 64-byte swizzle (layout 4): K-major operand
+// stored as [rows][32 bf16] (64-byte rows): SBO = 512 (8-row group stride);
+// MN-major operand stored as [K rows][32 bf16 of MN]: SBO = 512 between
+// groups of 8 K rows, LBO = stride between 32-element MN blocks.
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= uint64_t((saddr >> 4) & 0x3FFFu);
+  d |= uint64_t((lbo >> 4) & 0x3FFFu) << 16;
+  d |= uint64_t((sbo >> 4) & 0x3FFFu) << 32;
+  d |= uint64_t(1) << 46;
+  d |= uint64_t(4) << 61;
+  return d;
+}
+
 // The descriptor of the same operand `bytes` further on: the start address
 // field is the low 14 bits (address / 16), and shared-memory addresses stay
 // below 2^18, so a plain add never carries out of it.

@@ -132,8 +132,8 @@ class Clocks:
                 "samples": len(sm)}
 
 
-KERNEL_SOURCES = {"bwd_fused": ["bwd.cu", "bwd_common.cuh", "ptx.cuh", "kernels.cuh"],
-                  "fwd": ["fwd.cu", "ptx.cuh", "kernels.cuh"]}
+KERNEL_SOURCES = {"bwd_fused": ["bwd.cu", "bwd_common.cuh", "ptx.cuh", "kernels.cuh", "tiles.cuh"],
+                  "fwd": ["fwd.cu", "ptx.cuh", "kernels.cuh", "tiles.cuh"]}
 
 
 def src_sha(kernel):

@@ -32,7 +32,7 @@
  *   *_scaled calls take one scale per side, each under the same rule).
  * Causal: key j is visible to query i iff j <= i + (NK - NQ) (bottom-right
  *   aligned; j <= i when NQ == NK).  causal with NQ > NK is INVALID_ARG.
- * Head dims: d1, d2 in {64, 128}, independently (UNSUPPORTED otherwise).
+ * Head dims: d1, d2 in {32, 64, 128}, independently (UNSUPPORTED otherwise).
  * Empty problems: B*H*NQ == 0 is a no-op that returns OK (the backward then
  *   zeroes dk); NK == 0 with NQ > 0 is INVALID_ARG (rows without keys).
  * Return: a streamkl_status value; C++ exceptions never cross this ABI.

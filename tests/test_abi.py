@@ -74,7 +74,9 @@ def fwd(L, q=(A, A, A, A), B=1, H=1, NQ=128, NK=128, d1=64, d2=64, scale=0.125, 
     (dict(scale=float("inf")), skl.STREAMKL_INVALID_ARG),
     (dict(causal=2), skl.STREAMKL_INVALID_ARG),
     (dict(d1=96), skl.STREAMKL_UNSUPPORTED),
-    (dict(d2=32), skl.STREAMKL_UNSUPPORTED),
+    (dict(d2=48), skl.STREAMKL_UNSUPPORTED),
+    (dict(d1=16), skl.STREAMKL_UNSUPPORTED),
+    (dict(d2=256), skl.STREAMKL_UNSUPPORTED),
     (dict(NQ=256, NK=128, causal=1), skl.STREAMKL_INVALID_ARG),
     (dict(NK=0), skl.STREAMKL_INVALID_ARG),
     (dict(B=-1), skl.STREAMKL_INVALID_ARG),
