@@ -258,7 +258,7 @@ int streamkl_bwd_both(const void* q1, const void* k1, const void* q2, const void
   if (s == STREAMKL_OK && !scale_ok(scale2)) s = STREAMKL_INVALID_ARG;
   if (s != STREAMKL_OK) return s;
   if (deterministic != 0 && deterministic != 1) return STREAMKL_INVALID_ARG;
-  if (d1 != 64 || d2 != 64 || deterministic || empty) {
+  if (d1 != d2 || (d1 != 64 && d1 != 32) || deterministic || empty) {
     // one recompute per side (the single-side kernels; they also handle empty problems)
     s = streamkl_bwd_scaled(q1, k1, q2, k2, B, H, NQ, NK, d1, d2, scale1, scale2, causal, kl, lse1, lse2,
                             dkl, STREAMKL_GRAD_P2, deterministic, dq2, dk2, stream);
@@ -273,17 +273,17 @@ int streamkl_bwd_both(const void* q1, const void* k1, const void* q2, const void
   if ((s = device_ok()) != STREAMKL_OK) return s;
   skl::TMaps m{};
   if ((s = make_maps(&m, q1, k1, q2, k2, B * H, NQ, NK, d1, d2)) != STREAMKL_OK) return s;
-  if (!make_map_dq(&m.dq, dq1, (long long)B * H, NQ, 64) || !make_map_dq(&m.dq2, dq2, (long long)B * H, NQ, 64))
+  if (!make_map_dq(&m.dq, dq1, (long long)B * H, NQ, d1) || !make_map_dq(&m.dq2, dq2, (long long)B * H, NQ, d1))
     return STREAMKL_CUDA_ERROR;
   int* st = status_ptr();
   if (!st) return STREAMKL_CUDA_ERROR;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  const size_t dq_bytes = size_t(B) * H * NQ * 64 * 4;
+  const size_t dq_bytes = size_t(B) * H * NQ * d1 * 4;
   if (cudaMemsetAsync(dq1, 0, dq_bytes, cs) != cudaSuccess || cudaMemsetAsync(dq2, 0, dq_bytes, cs) != cudaSuccess)
     return STREAMKL_CUDA_ERROR;
   skl::BwdArgs a{B * H, NQ, NK, causal, STREAMKL_GRAD_P2, scale1, scale2, kl, lse1, lse2, dkl, dq1, dk1, st, 1,
                  dq2, dk2};
-  return as_status(skl::launch_bwd_both(m, a, cs));
+  return as_status(skl::launch_bwd_both(m, d1, a, cs));
 }
 
 const char* streamkl_status_string(int status) {

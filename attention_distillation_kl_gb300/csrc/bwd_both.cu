@@ -4,9 +4,10 @@
 // pass is a widening of the method, not a mode the pages name):
 //   dS2 = dKL (P2 - P1)                 -> dQ2 = s2 dS2 K2, dK2 = s2 dS2^T Q2
 //   dS1 = dKL P1 (r - KL), r from logits -> dQ1 = s1 dS1 K1, dK1 = s1 dS1^T Q1
-// Built for d1 = d2 = 64, where the four accumulators fit next to S1 and S2
-// in the 512 TMEM columns:
-//   S1 [0,128)  S2 [128,256)  dK1 [256,320)  dK2 [320,384)  dQ1 [384,448)  dQ2 [448,512)
+// Built for d1 = d2 = D with D = 64 or 32, where the four accumulators fit
+// next to S1 and S2 in the 512 TMEM columns (each takes D columns of a
+// 64-column slot):
+//   S1 [0,128)  S2 [128,256)  dK1 256  dK2 320  dQ1 384  dQ2 448
 // One CTA owns a 128-key tile and walks the query tiles that see it, like the
 // single-side fused kernel.  16 warps:
 //   warps 0-7   thread = query row: P1, P2 once, then dS1 and dS2 (bf16, two
@@ -20,6 +21,7 @@
 #include "bwd_common.cuh"
 #include "kernels.cuh"
 #include "ptx.cuh"
+#include "tiles.cuh"
 
 namespace skl {
 
@@ -28,8 +30,9 @@ namespace {
 constexpr int kBothThreads = 512;
 constexpr int kBothBoxes = 4;  // dQ staging boxes per epilogue warp
 
+template <int D_>
 struct BothLayout {
-  static constexpr int D = 64;
+  static constexpr int D = D_;
   static constexpr uint32_t kDS = kTile * kTile * 2;  // one bf16 dS tile
   static constexpr uint32_t kK = kTile * D * 2, kQ = kTile * D * 2;
   static constexpr uint32_t oDS1 = 0, oDS2 = kDS, oK1 = 2 * kDS, oK2 = oK1 + kK;
@@ -46,12 +49,14 @@ struct BothLayout {
   static_assert(kAlloc <= 232448, "over the 227 KB shared memory limit");
 };
 
+template <int D_>
 __global__ void __launch_bounds__(kBothThreads, 1)
     bwd_both_kernel(const __grid_constant__ CUtensorMap tq1, const __grid_constant__ CUtensorMap tk1,
                     const __grid_constant__ CUtensorMap tq2, const __grid_constant__ CUtensorMap tk2,
                     const __grid_constant__ CUtensorMap tdq1, const __grid_constant__ CUtensorMap tdq2,
                     const BwdArgs a) {
-  using L = BothLayout;
+  using L = BothLayout<D_>;
+  using T = OpTile<D_>;
   constexpr int D = L::D;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -102,16 +107,16 @@ __global__ void __launch_bounds__(kBothThreads, 1)
       tma_prefetch_desc(&tq2);
       tma_prefetch_desc(&tk2);
       mbar_arrive_expect_tx(bar(L::B_KFULL), 2 * L::kK);
-      tma_load_3d(sb + L::oK1, &tk1, bar(L::B_KFULL), 0, k0, bh);
-      tma_load_3d(sb + L::oK2, &tk2, bar(L::B_KFULL), 0, k0, bh);
+      T::load(sb + L::oK1, &tk1, bar(L::B_KFULL), k0, bh);
+      T::load(sb + L::oK2, &tk2, bar(L::B_KFULL), k0, bh);
       int issued = 0;
       for (int i = 0; i < n; ++i) {
         const int g = i & 1;
         if (!mbar_wait_polled(bar(L::B_QEMPTY0 + g), ((i >> 1) & 1) ^ 1, ctl)) break;
         mbar_arrive_expect_tx(bar(L::B_QFULL0 + g), 2 * L::kQ);
         const int q0 = (qt_lo + i) * kTile;
-        tma_load_3d(sb + L::oQ1 + g * L::kQ, &tq1, bar(L::B_QFULL0 + g), 0, q0, bh);
-        tma_load_3d(sb + L::oQ2 + g * L::kQ, &tq2, bar(L::B_QFULL0 + g), 0, q0, bh);
+        T::load(sb + L::oQ1 + g * L::kQ, &tq1, bar(L::B_QFULL0 + g), q0, bh);
+        T::load(sb + L::oQ2 + g * L::kQ, &tq2, bar(L::B_QFULL0 + g), q0, bh);
         issued = i + 1;
       }
       if (*abort_flag) {  // let the copies already started land before the CTA exits
@@ -125,21 +130,21 @@ __global__ void __launch_bounds__(kBothThreads, 1)
     // ---------------------------------------------------------------- S issuer
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16(128, 128, 0, 0);
-      const uint64_t k1d = sdesc_sw128(sb + L::oK1, 16, 1024), k2d = sdesc_sw128(sb + L::oK2, 16, 1024);
+      const uint64_t k1d = T::desc_k(sb + L::oK1), k2d = T::desc_k(sb + L::oK2);
       bool ok = n > 0 && mbar_wait_polled(bar(L::B_KFULL), 0, ctl);
       for (int i = 0; ok && i < n; ++i) {
         const int g = i & 1;
         if (!mbar_wait_polled(bar(L::B_SFREE), (i & 1) ^ 1, ctl)) break;
         if (!mbar_wait_polled(bar(L::B_QFULL0 + g), (i >> 1) & 1, ctl)) break;
         tc_fence_after();
-        const uint64_t q1d = sdesc_sw128(sb + L::oQ1 + g * L::kQ, 16, 1024);
-        const uint64_t q2d = sdesc_sw128(sb + L::oQ2 + g * L::kQ, 16, 1024);
+        const uint64_t q1d = T::desc_k(sb + L::oQ1 + g * L::kQ);
+        const uint64_t q2d = T::desc_k(sb + L::oQ2 + g * L::kQ);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_bf16_ss(1u, t_s1, sdesc_add(q1d, kk * 32), sdesc_add(k1d, kk * 32), id_s, kk > 0);
+          mma_bf16_ss(1u, t_s1, sdesc_add(q1d, T::off_k(kk)), sdesc_add(k1d, T::off_k(kk)), id_s, kk > 0);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_bf16_ss(1u, t_s2, sdesc_add(q2d, kk * 32), sdesc_add(k2d, kk * 32), id_s, kk > 0);
+          mma_bf16_ss(1u, t_s2, sdesc_add(q2d, T::off_k(kk)), sdesc_add(k2d, T::off_k(kk)), id_s, kk > 0);
         mma_commit(1u, bar(L::B_SFULL));
       }
       // every MMA of every issuer has finished before TMEM is released
@@ -158,15 +163,15 @@ __global__ void __launch_bounds__(kBothThreads, 1)
           if (!mbar_wait_polled(bar(L::B_DSFULL), t & 1, ctl)) break;
           tc_fence_after();
           const int g = t & 1;
-          const uint64_t q1n = sdesc_sw128(sb + L::oQ1 + g * L::kQ, kTile * 128, 1024);
-          const uint64_t q2n = sdesc_sw128(sb + L::oQ2 + g * L::kQ, kTile * 128, 1024);
+          const uint64_t q1n = T::desc_n(sb + L::oQ1 + g * L::kQ);
+          const uint64_t q2n = T::desc_n(sb + L::oQ2 + g * L::kQ);
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_bf16_ss(1u, t_dk1, sdesc_add(ds1, kk * 2048), sdesc_add(q1n, kk * 2048), id_dk,
+            mma_bf16_ss(1u, t_dk1, sdesc_add(ds1, kk * 2048), sdesc_add(q1n, T::off_n(kk)), id_dk,
                         (t > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_bf16_ss(1u, t_dk2, sdesc_add(ds2, kk * 2048), sdesc_add(q2n, kk * 2048), id_dk,
+            mma_bf16_ss(1u, t_dk2, sdesc_add(ds2, kk * 2048), sdesc_add(q2n, T::off_n(kk)), id_dk,
                         (t > 0 || kk > 0) ? 1u : 0u);
           mma_commit(1u, bar(L::B_QEMPTY0 + g));  // S and dK are done with Q1, Q2 of tile t
           mma_commit(1u, bar(L::B_DSEMPTY));
@@ -180,8 +185,8 @@ __global__ void __launch_bounds__(kBothThreads, 1)
     if (lane == 0) {
       constexpr uint32_t id_dq = idesc_bf16(128, D, 0, 1);  // A = dS K-major, B = K N-major
       const uint64_t ds1 = sdesc_sw128(sb + L::oDS1, 16, 1024), ds2 = sdesc_sw128(sb + L::oDS2, 16, 1024);
-      const uint64_t k1n = sdesc_sw128(sb + L::oK1, kTile * 128, 1024);
-      const uint64_t k2n = sdesc_sw128(sb + L::oK2, kTile * 128, 1024);
+      const uint64_t k1n = T::desc_n(sb + L::oK1);
+      const uint64_t k2n = T::desc_n(sb + L::oK2);
       if (n > 0 && mbar_wait_polled(bar(L::B_KFULL), 0, ctl)) {
         for (int t = 0; t < n; ++t) {
           if (!mbar_wait_polled(bar(L::B_DSFULL), t & 1, ctl)) break;
@@ -190,12 +195,12 @@ __global__ void __launch_bounds__(kBothThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk) {
             const uint32_t ao = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
-            mma_bf16_ss(1u, t_dq, sdesc_add(ds1, ao), sdesc_add(k1n, kk * 2048), id_dq, kk > 0 ? 1u : 0u);
+            mma_bf16_ss(1u, t_dq, sdesc_add(ds1, ao), sdesc_add(k1n, T::off_n(kk)), id_dq, kk > 0 ? 1u : 0u);
           }
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk) {
             const uint32_t ao = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
-            mma_bf16_ss(1u, t_dq + D, sdesc_add(ds2, ao), sdesc_add(k2n, kk * 2048), id_dq, kk > 0 ? 1u : 0u);
+            mma_bf16_ss(1u, t_dq + 64, sdesc_add(ds2, ao), sdesc_add(k2n, T::off_n(kk)), id_dq, kk > 0 ? 1u : 0u);
           }
           mma_commit(1u, bar(L::B_DSEMPTY));
           mma_commit(1u, bar(L::B_DQFULL));
@@ -274,6 +279,7 @@ __global__ void __launch_bounds__(kBothThreads, 1)
     // swizzle: 16-byte chunk c of row r at chunk c ^ ((r / 2) % 4)), round
     // robin; dQ1 is read first, dQ2 second, and the accumulator is released
     // after the second read, before that side is staged.
+    constexpr int kHalves = D / 32;
     const uint32_t stage = sb + L::oStage + w4 * (kBothBoxes * 2048);
     const uint32_t swz = (lane >> 1) & 3;
     int nred = 0;
@@ -287,16 +293,16 @@ __global__ void __launch_bounds__(kBothThreads, 1)
       const int r0 = (qt_lo + i) * kTile + w4 * 32;  // first query row of this warp
 #pragma unroll
       for (int side = 0; side < 2; ++side) {
-        uint32_t v[2][32];
-        tmem_ld32(t_dq + lane_off + side * D, v[0]);
-        tmem_ld32(t_dq + lane_off + side * D + 32, v[1]);
+        uint32_t v[kHalves][32];
+#pragma unroll
+        for (int x = 0; x < kHalves; ++x) tmem_ld32(t_dq + lane_off + side * 64 + 32 * x, v[x]);
         if (side == 1) {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(L::B_DQEMPTY));
         }
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
+        for (int h = 0; h < 2 * kHalves; ++h) {
           const uint32_t box = stage + (nred % kBothBoxes) * 2048;
           if (lane == 0) bulk_wait_read_le<kBothBoxes - 1>();  // the box used kBothBoxes reduces ago was read
           __syncwarp();
@@ -355,13 +361,21 @@ __global__ void __launch_bounds__(kBothThreads, 1)
 
 }  // namespace
 
-int launch_bwd_both(const TMaps& m, const BwdArgs& a, cudaStream_t st) {
-  using L = BothLayout;
-  cudaError_t e = cudaFuncSetAttribute(bwd_both_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+template <int D>
+static int launch_bwd_both_t(const TMaps& m, const BwdArgs& a, cudaStream_t st) {
+  using L = BothLayout<D>;
+  auto kern = bwd_both_kernel<D>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
   dim3 grid((a.NK + kTile - 1) / kTile, a.BH);
-  bwd_both_kernel<<<grid, kBothThreads, L::kAlloc, st>>>(m.q1, m.k1, m.q2, m.k2, m.dq, m.dq2, a);
+  kern<<<grid, kBothThreads, L::kAlloc, st>>>(m.q1, m.k1, m.q2, m.k2, m.dq, m.dq2, a);
   return cudaGetLastError();
+}
+
+int launch_bwd_both(const TMaps& m, int d, const BwdArgs& a, cudaStream_t st) {
+  if (d == 64) return launch_bwd_both_t<64>(m, a, st);
+  if (d == 32) return launch_bwd_both_t<32>(m, a, st);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace skl

@@ -47,7 +47,7 @@ int launch_splitk_reduce(const float* partial, int rows, int num_splits, float* 
                          float* lse2, cudaStream_t st);
 int launch_bwd_fused(const TMaps& m, int d1, int d2, const BwdArgs& a, cudaStream_t st);
 int launch_bwd_dq(const TMaps& m, int d1, int d2, const BwdArgs& a, cudaStream_t st);
-int launch_bwd_both(const TMaps& m, const BwdArgs& a, cudaStream_t st);  // d1 = d2 = 64
+int launch_bwd_both(const TMaps& m, int d, const BwdArgs& a, cudaStream_t st);  // d1 = d2 = d, 32 or 64
 int launch_ex2_probe(float* out, int blocks, int iters, cudaStream_t st);
 int launch_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t st);
 

@@ -246,15 +246,15 @@ def key_split_timing(skl, stream):
     return out
 
 
-def both_sides_timing(skl, stream):
+def both_sides_timing(skl, stream, d=64):
     """Both-sides backward in one pass against the two single-side passes,
-    on a d = 64 problem (16K tokens x 32 heads, causal)."""
+    on a d1 = d2 = d problem (16K tokens x 32 heads, causal)."""
     from attention_distillation_kl_gb300.workloads import Workload
-    w = Workload("both-d64", 1, 32, 16384, 16384, 64, 64, True, 0.125, "independent", 0.0, 1.0, 1006)
+    w = Workload(f"both-d{d}", 1, 32, 16384, 16384, d, d, True, 1 / np.sqrt(d), "independent", 0.0, 1.0, 1006)
     dev = [t.cuda() for t in generate(w)]
     kl, l1, l2 = skl.streamkl_fwd(*dev, w.scale, w.causal)
     dkl = torch.ones_like(kl)
-    bufs = [torch.empty(w.B, w.H, n, 64, device="cuda") for n in (w.NQ, w.NK, w.NQ, w.NK)]
+    bufs = [torch.empty(w.B, w.H, n, d, device="cuda") for n in (w.NQ, w.NK, w.NQ, w.NK)]
 
     def timed(fn, reps=4):
         fn()
@@ -268,14 +268,15 @@ def both_sides_timing(skl, stream):
             ts.append(a.elapsed_time(b))
         return float(np.median(ts))
 
-    out = {"workload": f"B={w.B} H={w.H} NQ=NK={w.NQ} d1=d2=64 causal"}
+    out = {"workload": f"B={w.B} H={w.H} NQ=NK={w.NQ} d1=d2={d} causal"}
     out["bwd_p2_ms"] = timed(lambda: skl.streamkl_bwd(*dev, w.scale, w.causal, kl, l1, l2, dkl,
                                                       skl.STREAMKL_GRAD_P2, False, bufs[2], bufs[3]))
     out["bwd_p1_ms"] = timed(lambda: skl.streamkl_bwd(*dev, w.scale, w.causal, kl, l1, l2, dkl,
                                                       skl.STREAMKL_GRAD_P1, False, bufs[0], bufs[1]))
     out["bwd_both_ms"] = timed(lambda: skl.streamkl_bwd_both(*dev, w.scale, w.scale, w.causal, kl, l1, l2, dkl,
                                                              False, *bufs))
-    out["bwd_both_tflops"] = (2 * 128 + 4 * 64 * 2) * w.pairs / (out["bwd_both_ms"] * 1e-3) / 1e12
+    # two S products and four gradient products, 2 d flops each per pair
+    out["bwd_both_tflops"] = 12 * d * w.pairs / (out["bwd_both_ms"] * 1e-3) / 1e12
     del dev, bufs
     torch.cuda.empty_cache()
     return out
@@ -409,6 +410,7 @@ def run_mine(args, rank, world, local):
     # splits, the heuristic's choice, and the plain forward for comparison
     c5 = key_split_timing(skl, stream) if rank == 0 and world == 1 and not args.no_cpu_baseline else None
     both = both_sides_timing(skl, stream) if rank == 0 and world == 1 and not args.no_cpu_baseline else None
+    both32 = both_sides_timing(skl, stream, 32) if both is not None else None
 
     rate = ex2_rate(skl)
     burst, sustained, _hbm, src = peaks()
@@ -445,6 +447,7 @@ def run_mine(args, rank, world, local):
             "extra_device_bytes": extra_bytes,
             "key_split_131k": c5,
             "both_sides_d64": both,
+            "both_sides_d32": both32,
             "ex2_per_s": rate,
             "roofline": {"bound": "tensor", "achieved": bwd_tf if dom == "bwd" else fwd_tf,
                          "peak": sustained, "unit": "TFLOP/s",

@@ -1,6 +1,7 @@
 """Both-sides backward (streamkl_bwd_both): dQ1, dK1, dQ2, dK2 against the
-float64 oracle's two gradient modes on the same inputs.  d1 = d2 = 64 runs
-the one-recompute kernel; other head dimensions and the deterministic mode
+float64 oracle's two gradient modes on the same inputs.  d1 = d2 = 64 and
+d1 = d2 = 32 run the one-recompute kernel; other head dimensions and the
+deterministic mode
 run the single-side backward twice; both must match the oracle with the
 single-side tolerances."""
 
@@ -25,7 +26,12 @@ CASES = [
     (1, 1, 700, 200, 64, 64, False, 0.125, 0.125, False),
     (1, 1, 5, 333, 64, 64, True, 0.125, 0.125, False),
     (1, 2, 257, 257, 64, 64, True, 0.125, 0.125, True),
+    (1, 2, 300, 300, 32, 32, True, 1 / np.sqrt(32), 0.15, False),
+    (2, 1, 130, 390, 32, 32, False, 0.2, 1 / np.sqrt(32), False),
+    (1, 1, 1000, 1000, 32, 32, True, 1 / np.sqrt(32), 1 / np.sqrt(32), False),
+    (1, 1, 700, 200, 32, 32, False, 0.15, 0.15, False),
     (1, 2, 300, 300, 128, 64, True, 1 / np.sqrt(128), 1 / np.sqrt(64), False),
+    (1, 2, 300, 300, 64, 32, True, 1 / np.sqrt(64), 1 / np.sqrt(32), False),
     (1, 1, 384, 384, 128, 128, False, 1 / np.sqrt(128), 1 / np.sqrt(128), False),
 ]
 IDS = ["x".join(f"{v:.3g}" if isinstance(v, float) else str(v) for v in c) for c in CASES]
@@ -53,8 +59,9 @@ def test_both_sides_match_the_oracle(c):
                 grad_close(np_(got[1])[b, h], want[1][b, h], fl)
 
 
-def test_one_pass_agrees_with_the_two_single_side_calls():
-    w = Workload("both", 1, 4, 1536, 1536, 64, 64, True, 0.125, "independent", 0.0, 1.2, 96)
+@pytest.mark.parametrize("d", [64, 32])
+def test_one_pass_agrees_with_the_two_single_side_calls(d):
+    w = Workload("both", 1, 4, 1536, 1536, d, d, True, 1 / np.sqrt(d), "independent", 0.0, 1.2, 96)
     host, dev = inputs(w)
     dkl = generate_dkl(w, "uniform").cuda()
     kl, l1, l2 = skl.streamkl_fwd(*dev, w.scale, w.causal)
