@@ -35,16 +35,21 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+// The kernels' tile width for head dim d (a multiple of 16 up to 128): 32,
+// 64 or 128.  Columns past d in a tile are zero-filled by the TMA, which
+// leaves every dot product unchanged.
+int tile_dim(int d) { return d <= 32 ? 32 : (d <= 64 ? 64 : 128); }
+
 // [BH][N][d] bf16 viewed as a 3-D tensor; boxes of 64 elements x 128 rows x 1
-// with the 128-byte swizzle, or for d = 32 one box of 32 elements x 128 rows
-// x 1 with the 64-byte swizzle (the layouts the kernels' operand tiles
-// expect).  Rows past N read as zeros.
+// with the 128-byte swizzle, or for tile width 32 one box of 32 elements x
+// 128 rows x 1 with the 64-byte swizzle (the layouts the kernels' operand
+// tiles expect).  Rows past N and columns past d read as zeros.
 bool make_map(CUtensorMap* m, const void* ptr, long long BH, long long N, int d) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[3] = {cuuint64_t(d), cuuint64_t(N), cuuint64_t(BH)};
   cuuint64_t strides[2] = {cuuint64_t(d) * 2, cuuint64_t(N) * d * 2};
-  const bool narrow = d < 64;
+  const bool narrow = tile_dim(d) == 32;
   cuuint32_t box[3] = {narrow ? 32u : 64u, cuuint32_t(skl::kTile), 1};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
@@ -73,7 +78,7 @@ bool scale_ok(float s) { return std::isfinite(s) && s > 0.f && s <= 1.0e4f; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-bool head_dim_ok(int d) { return d == 32 || d == 64 || d == 128; }
+bool head_dim_ok(int d) { return d >= 16 && d <= 128 && d % 16 == 0; }
 
 // Shared validation of the problem description.  Returns STREAMKL_OK, or the
 // status to report.  Sets *empty when there is no row to compute.
@@ -138,7 +143,7 @@ int streamkl_fwd_scaled(const void* q1, const void* k1, const void* q2, const vo
   int* st = status_ptr();
   if (!st) return STREAMKL_CUDA_ERROR;
   skl::FwdArgs a{B * H, NQ, NK, causal, 1, scale1, scale2, kl, lse1, lse2, nullptr, st};
-  return as_status(skl::launch_fwd(m, d1, d2, a, reinterpret_cast<cudaStream_t>(stream)));
+  return as_status(skl::launch_fwd(m, tile_dim(d1), tile_dim(d2), a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int streamkl_fwd(const void* q1, const void* k1, const void* q2, const void* k2, int B, int H,
@@ -175,7 +180,7 @@ int streamkl_fwd_splitk_scaled(const void* q1, const void* k1, const void* q2, c
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   float* part = static_cast<float*>(workspace);
   skl::FwdArgs a{B * H, NQ, NK, causal, num_splits, scale1, scale2, kl, lse1, lse2, part, st};
-  int e = skl::launch_fwd(m, d1, d2, a, cs);
+  int e = skl::launch_fwd(m, tile_dim(d1), tile_dim(d2), a, cs);
   if (e != 0) return STREAMKL_CUDA_ERROR;
   return as_status(skl::launch_splitk_reduce(part, B * H * NQ, num_splits, kl, lse1, lse2, cs));
 }
@@ -228,17 +233,18 @@ int streamkl_bwd_scaled(const void* q1, const void* k1, const void* q2, const vo
   if ((s = make_maps(&m, q1, k1, q2, k2, B * H, NQ, NK, d1, d2)) != STREAMKL_OK) return s;
   int* st = status_ptr();
   if (!st) return STREAMKL_CUDA_ERROR;
-  skl::BwdArgs a{B * H, NQ, NK, causal, mode, scale1, scale2, kl, lse1, lse2, dkl, dq, dk, st, 1};
+  skl::BwdArgs a{B * H, NQ, NK, causal, mode, dg, scale1, scale2, kl, lse1, lse2, dkl, dq, dk, st, 1};
+  const int t1 = tile_dim(d1), t2 = tile_dim(d2);
   if (!deterministic) {
     const size_t dq_bytes = size_t(B) * H * NQ * dg * 4;
     if (!make_map_dq(&m.dq, dq, (long long)B * H, NQ, dg)) return STREAMKL_CUDA_ERROR;
     if (cudaMemsetAsync(dq, 0, dq_bytes, cs) != cudaSuccess) return STREAMKL_CUDA_ERROR;
-    return as_status(skl::launch_bwd_fused(m, d1, d2, a, cs));
+    return as_status(skl::launch_bwd_fused(m, t1, t2, a, cs));
   }
   a.write_dq = 0;
-  int e = skl::launch_bwd_fused(m, d1, d2, a, cs);
+  int e = skl::launch_bwd_fused(m, t1, t2, a, cs);
   if (e != 0) return STREAMKL_CUDA_ERROR;
-  return as_status(skl::launch_bwd_dq(m, d1, d2, a, cs));
+  return as_status(skl::launch_bwd_dq(m, t1, t2, a, cs));
 }
 
 int streamkl_bwd(const void* q1, const void* k1, const void* q2, const void* k2, int B, int H,
@@ -258,7 +264,7 @@ int streamkl_bwd_both(const void* q1, const void* k1, const void* q2, const void
   if (s == STREAMKL_OK && !scale_ok(scale2)) s = STREAMKL_INVALID_ARG;
   if (s != STREAMKL_OK) return s;
   if (deterministic != 0 && deterministic != 1) return STREAMKL_INVALID_ARG;
-  if (d1 != d2 || (d1 != 64 && d1 != 32) || deterministic || empty) {
+  if (d1 != d2 || tile_dim(d1) > 64 || deterministic || empty) {
     // one recompute per side (the single-side kernels; they also handle empty problems)
     s = streamkl_bwd_scaled(q1, k1, q2, k2, B, H, NQ, NK, d1, d2, scale1, scale2, causal, kl, lse1, lse2,
                             dkl, STREAMKL_GRAD_P2, deterministic, dq2, dk2, stream);
@@ -281,9 +287,9 @@ int streamkl_bwd_both(const void* q1, const void* k1, const void* q2, const void
   const size_t dq_bytes = size_t(B) * H * NQ * d1 * 4;
   if (cudaMemsetAsync(dq1, 0, dq_bytes, cs) != cudaSuccess || cudaMemsetAsync(dq2, 0, dq_bytes, cs) != cudaSuccess)
     return STREAMKL_CUDA_ERROR;
-  skl::BwdArgs a{B * H, NQ, NK, causal, STREAMKL_GRAD_P2, scale1, scale2, kl, lse1, lse2, dkl, dq1, dk1, st, 1,
+  skl::BwdArgs a{B * H, NQ, NK, causal, STREAMKL_GRAD_P2, d1, scale1, scale2, kl, lse1, lse2, dkl, dq1, dk1, st, 1,
                  dq2, dk2};
-  return as_status(skl::launch_bwd_both(m, d1, a, cs));
+  return as_status(skl::launch_bwd_both(m, tile_dim(d1), a, cs));
 }
 
 const char* streamkl_status_string(int status) {

@@ -339,6 +339,7 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
           }
 #pragma unroll
           for (int h = 0; h < 2 * kHalves; ++h) {
+            if (cp * kRead + h * 16 >= a.dg) break;  // columns past the head dim (zero-filled operand)
             const uint32_t box = stage + (nred % kDqBoxes) * 2048;
             // the box used kDqBoxes reduces ago has been read
             if (lane == 0) bulk_wait_read_le<kDqBoxes - 1>();
@@ -364,7 +365,7 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
     if (n > 0 && mbar_wait_warp(bar(L::B_DKFULL), 0, ctl)) {
       tc_fence_after();
       const int kj = k0 + row;
-      float* dst = a.dk + (size_t(bh) * a.NK + kj) * DG;
+      float* dst = a.dk + (size_t(bh) * a.NK + kj) * a.dg;
 #pragma unroll
       for (int ch = 0; ch < DG / 32; ++ch) {
         uint32_t v[32];
@@ -372,17 +373,18 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
         if (kj < a.NK) {
 #pragma unroll
           for (int e = 0; e < 32; e += 4)
-            *reinterpret_cast<float4*>(dst + ch * 32 + e) =
-                make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]), __uint_as_float(v[e + 2]),
-                            __uint_as_float(v[e + 3]));
+            if (ch * 32 + e < a.dg)
+              *reinterpret_cast<float4*>(dst + ch * 32 + e) =
+                  make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]), __uint_as_float(v[e + 2]),
+                              __uint_as_float(v[e + 3]));
         }
       }
     } else if (n == 0) {
       // no query row sees this key tile: its dK is zero
       const int kj = k0 + row;
       if (kj < a.NK)
-        for (int e = 0; e < DG; e += 4)
-          *reinterpret_cast<float4*>(a.dk + (size_t(bh) * a.NK + kj) * DG + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int e = 0; e < a.dg; e += 4)
+          *reinterpret_cast<float4*>(a.dk + (size_t(bh) * a.NK + kj) * a.dg + e) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
 
@@ -587,7 +589,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     }
     if (nkt > 0 && mbar_wait_warp(bar(L::B_DQFULL), 0, ctl)) {
       tc_fence_after();
-      float* dst = a.dq + (size_t(bh) * a.NQ + qi) * DG;
+      float* dst = a.dq + (size_t(bh) * a.NQ + qi) * a.dg;
 #pragma unroll
       for (int ch = 0; ch < DG / 32; ++ch) {
         uint32_t v[32];
@@ -595,9 +597,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         if (qi < a.NQ) {
 #pragma unroll
           for (int e = 0; e < 32; e += 4)
-            *reinterpret_cast<float4*>(dst + ch * 32 + e) =
-                make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]), __uint_as_float(v[e + 2]),
-                            __uint_as_float(v[e + 3]));
+            if (ch * 32 + e < a.dg)
+              *reinterpret_cast<float4*>(dst + ch * 32 + e) =
+                  make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]), __uint_as_float(v[e + 2]),
+                              __uint_as_float(v[e + 3]));
         }
       }
     }

@@ -4,7 +4,8 @@
 // pass is a widening of the method, not a mode the pages name):
 //   dS2 = dKL (P2 - P1)                 -> dQ2 = s2 dS2 K2, dK2 = s2 dS2^T Q2
 //   dS1 = dKL P1 (r - KL), r from logits -> dQ1 = s1 dS1 K1, dK1 = s1 dS1^T Q1
-// Built for d1 = d2 = D with D = 64 or 32, where the four accumulators fit
+// Built for tile widths D = 64 or 32 (d1 = d2 = a.dg <= D; columns past a.dg
+// are zero-filled by the TMA and not written), where the four accumulators fit
 // next to S1 and S2 in the 512 TMEM columns (each takes D columns of a
 // 64-column slot):
 //   S1 [0,128)  S2 [128,256)  dK1 256  dK2 320  dQ1 384  dQ2 448
@@ -303,6 +304,7 @@ __global__ void __launch_bounds__(kBothThreads, 1)
         }
 #pragma unroll
         for (int h = 0; h < 2 * kHalves; ++h) {
+          if (h * 16 >= a.dg) break;  // columns past the head dim (zero-filled operand)
           const uint32_t box = stage + (nred % kBothBoxes) * 2048;
           if (lane == 0) bulk_wait_read_le<kBothBoxes - 1>();  // the box used kBothBoxes reduces ago was read
           __syncwarp();
@@ -328,7 +330,7 @@ __global__ void __launch_bounds__(kBothThreads, 1)
       tc_fence_after();
 #pragma unroll
       for (int side = 0; side < 2; ++side) {
-        float* dst = (side == 0 ? a.dk : a.dk2) + (size_t(bh) * a.NK + kj) * D;
+        float* dst = (side == 0 ? a.dk : a.dk2) + (size_t(bh) * a.NK + kj) * a.dg;
 #pragma unroll
         for (int ch = 0; ch < D / 32; ++ch) {
           uint32_t v[32];
@@ -336,17 +338,18 @@ __global__ void __launch_bounds__(kBothThreads, 1)
           if (kj < a.NK) {
 #pragma unroll
             for (int e = 0; e < 32; e += 4)
-              *reinterpret_cast<float4*>(dst + ch * 32 + e) =
-                  make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]), __uint_as_float(v[e + 2]),
-                              __uint_as_float(v[e + 3]));
+              if (ch * 32 + e < a.dg)
+                *reinterpret_cast<float4*>(dst + ch * 32 + e) =
+                    make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]), __uint_as_float(v[e + 2]),
+                                __uint_as_float(v[e + 3]));
           }
         }
       }
     } else if (n == 0 && kj < a.NK) {
       // no query row sees this key tile: its dK is zero on both sides
-      for (int e = 0; e < D; e += 4) {
-        *reinterpret_cast<float4*>(a.dk + (size_t(bh) * a.NK + kj) * D + e) = make_float4(0.f, 0.f, 0.f, 0.f);
-        *reinterpret_cast<float4*>(a.dk2 + (size_t(bh) * a.NK + kj) * D + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int e = 0; e < a.dg; e += 4) {
+        *reinterpret_cast<float4*>(a.dk + (size_t(bh) * a.NK + kj) * a.dg + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+        *reinterpret_cast<float4*>(a.dk2 + (size_t(bh) * a.NK + kj) * a.dg + e) = make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
   }

@@ -11,7 +11,7 @@ namespace skl {
 constexpr int kTile = 128;  // query and key tile: 128 rows = 128 TMEM lanes
 
 struct TMaps {
-  CUtensorMap q1, k1, q2, k2;  // [BH][N][d] bf16, boxes of 64 x 128, 128-byte swizzle
+  CUtensorMap q1, k1, q2, k2;  // [BH][N][d] bf16, boxes of 64 (or 32) x 128, 128- (or 64-) byte swizzle
   CUtensorMap dq;              // [BH][NQ][dg] fp32, boxes of 16 x 32, 64-byte swizzle (fused backward)
   CUtensorMap dq2;             // the second side's dQ (both-sides backward)
 };
@@ -28,6 +28,7 @@ struct FwdArgs {
 
 struct BwdArgs {
   int BH, NQ, NK, causal, mode;
+  int dg;  // the gradient side's head dim: row length of dq, dk (at most the kernel's tile width)
   float scale1, scale2;
   const float* kl;
   const float* lse1;
@@ -41,7 +42,9 @@ struct BwdArgs {
   float* dk2;
 };
 
-// Each returns a cudaError_t value (cudaSuccess = 0).
+// Each returns a cudaError_t value (cudaSuccess = 0).  d1, d2 and d are the
+// kernels' tile widths (32, 64 or 128): a head dim below its tile width is
+// read with the columns past it zero-filled by the TMA.
 int launch_fwd(const TMaps& m, int d1, int d2, const FwdArgs& a, cudaStream_t st);
 int launch_splitk_reduce(const float* partial, int rows, int num_splits, float* kl, float* lse1,
                          float* lse2, cudaStream_t st);

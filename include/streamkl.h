@@ -32,7 +32,11 @@
  *   *_scaled calls take one scale per side, each under the same rule).
  * Causal: key j is visible to query i iff j <= i + (NK - NQ) (bottom-right
  *   aligned; j <= i when NQ == NK).  causal with NQ > NK is INVALID_ARG.
- * Head dims: d1, d2 in {32, 64, 128}, independently (UNSUPPORTED otherwise).
+ * Head dims: d1, d2 any multiple of 16 from 16 to 128, independently
+ *   (UNSUPPORTED otherwise).  The kernels compute in tiles 32, 64 or 128
+ *   wide; a head dim below its tile width is read with the columns past it
+ *   zero-filled, which changes no dot product (the padded work is not
+ *   credited in any throughput figure).
  * Empty problems: B*H*NQ == 0 is a no-op that returns OK (the backward then
  *   zeroes dk); NK == 0 with NQ > 0 is INVALID_ARG (rows without keys).
  * Return: a streamkl_status value; C++ exceptions never cross this ABI.
@@ -174,14 +178,14 @@ int streamkl_bwd_scaled(const void* q1, const void* k1, const void* q2, const vo
  * Both-sides backward: the gradients of sum_i dkl_i * KL_i with respect to
  * both distributions (dq1, dk1 with head dim d1; dq2, dk2 with d2; fp32,
  * fully overwritten), from one recompute of S1 and S2 per tile pair when
- * d1 = d2 = 64 or d1 = d2 = 32 and deterministic = 0.  (A widening of the
- * method: the article's two modes share P1 and P2.)  Other head-dimension
- * pairs (at 128 the four accumulators do not fit beside S1 and S2 in tensor
- * memory; unequal pairs have no one-pass kernel) and the deterministic mode
- * run the single-side backward twice (mode P2, then mode P1) and return what
- * those return.  Arguments, ownership and errors are
- * otherwise those of streamkl_bwd_scaled; kl, lse1, lse2 must come from a
- * forward with the same two scales.
+ * d1 = d2 <= 64 and deterministic = 0.  (A widening of the method: the
+ * article's two modes share P1 and P2.)  Other head-dimension pairs (above
+ * 64 the four accumulators do not fit beside S1 and S2 in tensor memory;
+ * unequal pairs have no one-pass kernel) and the deterministic mode run the
+ * single-side backward twice (mode P2, then mode P1) and return what those
+ * return.  Arguments, ownership and errors are otherwise those of
+ * streamkl_bwd_scaled; kl, lse1, lse2 must come from a forward with the
+ * same two scales.
  */
 int streamkl_bwd_both(const void* q1, const void* k1, const void* q2, const void* k2,
                       int B, int H, int NQ, int NK, int d1, int d2, float scale1, float scale2,

@@ -73,10 +73,11 @@ def fwd(L, q=(A, A, A, A), B=1, H=1, NQ=128, NK=128, d1=64, d2=64, scale=0.125, 
     (dict(scale=float("nan")), skl.STREAMKL_INVALID_ARG),
     (dict(scale=float("inf")), skl.STREAMKL_INVALID_ARG),
     (dict(causal=2), skl.STREAMKL_INVALID_ARG),
-    (dict(d1=96), skl.STREAMKL_UNSUPPORTED),
-    (dict(d2=48), skl.STREAMKL_UNSUPPORTED),
-    (dict(d1=16), skl.STREAMKL_UNSUPPORTED),
-    (dict(d2=256), skl.STREAMKL_UNSUPPORTED),
+    (dict(d1=8), skl.STREAMKL_UNSUPPORTED),
+    (dict(d2=40), skl.STREAMKL_UNSUPPORTED),
+    (dict(d1=0), skl.STREAMKL_UNSUPPORTED),
+    (dict(d2=144), skl.STREAMKL_UNSUPPORTED),
+    (dict(d1=256), skl.STREAMKL_UNSUPPORTED),
     (dict(NQ=256, NK=128, causal=1), skl.STREAMKL_INVALID_ARG),
     (dict(NK=0), skl.STREAMKL_INVALID_ARG),
     (dict(B=-1), skl.STREAMKL_INVALID_ARG),
@@ -161,4 +162,4 @@ def test_bwd_both_validation(L):
     assert f(*base, 0.125, 0.125, 0, *tail, 2, A, A, A, A, None) == skl.STREAMKL_INVALID_ARG   # deterministic flag
     assert f(*base, 0.125, 0.125, 0, *tail, 0, A, A, 0, A, None) == skl.STREAMKL_INVALID_ARG   # null dq2
     assert f(*base, 0.125, 0.125, 0, *tail, 0, A, A, A, A + 4, None) == skl.STREAMKL_INVALID_ARG  # misaligned dk2
-    assert f(A, A, A, A, 1, 1, 128, 128, 96, 64, 0.1, 0.1, 0, *tail, 0, A, A, A, A, None) == skl.STREAMKL_UNSUPPORTED
+    assert f(A, A, A, A, 1, 1, 128, 128, 72, 64, 0.1, 0.1, 0, *tail, 0, A, A, A, A, None) == skl.STREAMKL_UNSUPPORTED
