@@ -27,7 +27,11 @@ Readings taken where the pages are silent:
     j <= i + (NK - NQ); causal with NQ > NK is rejected (every row keeps at
     least one key);
   * LSE is the natural-log log-sum-exp over the visible keys;
-  * only KL is differentiated; the upstream gradient is dKL (one per row).
+  * only KL is differentiated; the upstream gradient is dKL (one per row);
+  * grouped key heads (GQA; MQA with one key head) are not on the pages and
+    are taken in their usual sense: with H query heads and HK key heads (HK
+    dividing H), query head h reads key head h // (H / HK) of its side, and a
+    shared key head's gradient is the sum over the query heads that read it.
 
 Arrays: q1 [NQ, d1], k1 [NK, d1], q2 [NQ, d2], k2 [NK, d2] per head; the
 batched wrappers take [B, H, N, d].  Callers pass float64 copies of the exact
@@ -124,13 +128,24 @@ def forward_head(q1, k1, q2, k2, scale, causal, row_block=256, scale2=None):
     return kl, lse1, lse2
 
 
+def _group(h_, k):
+    """Query heads per key head for a [B, HK, N, d] key tensor."""
+    hk = k.shape[1]
+    if hk < 1 or h_ % hk:
+        raise ValueError("the key head count must divide the query head count")
+    return h_ // hk
+
+
 def forward(q1, k1, q2, k2, scale, causal, row_block=256, scale2=None):
-    """Batched forward over [B, H, N, d] inputs -> (kl, lse1, lse2) [B, H, NQ]."""
+    """Batched forward over [B, H, N, d] inputs -> (kl, lse1, lse2) [B, H, NQ].
+    k1, k2 may have fewer heads (grouped key heads, see the module notes)."""
     b_, h_, nq = q1.shape[:3]
+    g1, g2 = _group(h_, k1), _group(h_, k2)
     out = [np.empty((b_, h_, nq)) for _ in range(3)]
     for b in range(b_):
         for h in range(h_):
-            res = forward_head(q1[b, h], k1[b, h], q2[b, h], k2[b, h], scale, causal, row_block, scale2)
+            res = forward_head(q1[b, h], k1[b, h // g1], q2[b, h], k2[b, h // g2], scale, causal, row_block,
+                               scale2)
             for o, v in zip(out, res):
                 o[b, h] = v
     return tuple(out)
@@ -281,16 +296,22 @@ def backward_head(q1, k1, q2, k2, scale, causal, dkl, mode, row_block=256, scale
 
 
 def backward(q1, k1, q2, k2, scale, causal, dkl, mode, row_block=256, scale2=None):
-    """Batched backward over [B, H, N, d] inputs; dkl is [B, H, NQ]."""
+    """Batched backward over [B, H, N, d] inputs; dkl is [B, H, NQ].  With
+    grouped key heads dK has the gradient side's key head count: each query
+    head's contribution is added into the key head it reads."""
     b_, h_, nq = q1.shape[:3]
     nk = k1.shape[2]
-    dg = q2.shape[3] if mode == MODE_P2 else q1.shape[3]
+    g1, g2 = _group(h_, k1), _group(h_, k2)
+    kg = k2 if mode == MODE_P2 else k1
+    gg = g2 if mode == MODE_P2 else g1
+    dg = kg.shape[3]
     dq = np.empty((b_, h_, nq, dg))
-    dk = np.empty((b_, h_, nk, dg))
+    dk = np.zeros((b_, kg.shape[1], nk, dg))
     for b in range(b_):
         for h in range(h_):
-            dq[b, h], dk[b, h] = backward_head(q1[b, h], k1[b, h], q2[b, h], k2[b, h],
-                                               scale, causal, dkl[b, h], mode, row_block, scale2)
+            dq[b, h], dk_h = backward_head(q1[b, h], k1[b, h // g1], q2[b, h], k2[b, h // g2],
+                                           scale, causal, dkl[b, h], mode, row_block, scale2)
+            dk[b, h // gg] += dk_h
     return dq, dk
 
 

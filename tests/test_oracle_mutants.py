@@ -39,6 +39,10 @@ MUTANTS = {
     "dq scale dropped": ("dq[rows] = sg * (ds @ kg)", "dq[rows] = (ds @ kg)"),
     "dk uses other side": ("dk += sg * (ds.T @ qg[rows])", "dk += sg * (ds.T @ (q1 if mode == MODE_P2 else q2)[rows][:, :qg.shape[1]])"),
     "sampled dq wrong side": ("kg, sg = (k2, s2) if mode == MODE_P2 else (k1, s1)", "kg, sg = (k1, s2) if mode == MODE_P2 else (k2, s1)"),
+    "grouped key head by modulo": ("k1[b, h // g1], q2[b, h], k2[b, h // g2], scale, causal, row_block,\n",
+                                   "k1[b, h % k1.shape[1]], q2[b, h], k2[b, h % k2.shape[1]], scale, causal, row_block,\n"),
+    "grouped dK overwritten, not summed": ("dk[b, h // gg] += dk_h", "dk[b, h // gg] = dk_h"),
+    "grouped dK into the other side's head": ("dk[b, h // gg] += dk_h", "dk[b, h // (g1 if gg == g2 else g2)] += dk_h"),
     "sampled dk missing scale": ("dk += sg * (ds.T @ qg[rows])\n    return dk\n\n\ndef loss", "dk += (ds.T @ qg[rows])\n    return dk\n\n\ndef loss"),
 }
 

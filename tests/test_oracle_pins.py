@@ -17,7 +17,10 @@ copies of the oracle with planted mistakes.  What each pin rests on:
 * a second softmax scale for the S2 side: s2 = 0 gives the uniform-student
   closed form, a power-of-two rescale of Q2 against s2 changes nothing, and
   per-side results equal single-scale results with Q2 pre-multiplied by
-  s2/s1 (gradients by the chain rule), plus finite differences.
+  s2/s1 (gradients by the chain rule), plus finite differences;
+* grouped key heads: equal to every key head repeated over its group and run
+  as independent heads (dK summed over the copies), plus finite differences
+  w.r.t. a shared key head.
 """
 
 import math
@@ -367,6 +370,62 @@ def pin_per_side_scale_online(o):
             np.testing.assert_allclose(kl2, kl, rtol=1e-12, atol=1e-13)
             np.testing.assert_allclose(a2, a, rtol=1e-13, atol=1e-13)
             np.testing.assert_allclose(b2, b, rtol=1e-13, atol=1e-13)
+
+
+def _gqa_inputs(rng, b_, h_, hk1, hk2, nq, nk, d1, d2, sd=1.2):
+    return (_rand(rng, b_, h_, nq, d1, sd=sd), _rand(rng, b_, hk1, nk, d1, sd=sd),
+            _rand(rng, b_, h_, nq, d2, sd=sd), _rand(rng, b_, hk2, nk, d2, sd=sd))
+
+
+def pin_grouped_key_heads_are_repeated_heads(o):
+    # grouped key heads = every key head repeated over its consecutive group
+    # of query heads (np.repeat), run as independent heads; dK of a shared
+    # head = the sum of the repeated copies' dK (chain rule of the repeat)
+    rng = np.random.default_rng(21)
+    for hk1, hk2, causal in ((3, 2, True), (1, 6, False), (2, 1, True)):
+        q1, k1, q2, k2 = _gqa_inputs(rng, 2, 6, hk1, hk2, 9, 11, 4, 3)
+        r1, r2 = np.repeat(k1, 6 // hk1, axis=1), np.repeat(k2, 6 // hk2, axis=1)
+        dkl = rng.uniform(0.5, 1.5, (2, 6, 9))
+        got = o.forward(q1, k1, q2, k2, 0.8, causal, scale2=0.6)
+        for b in range(2):
+            for h in range(6):
+                want = o.forward_head(q1[b, h], r1[b, h], q2[b, h], r2[b, h], 0.8, causal, scale2=0.6)
+                for g, w in zip(got, want):
+                    np.testing.assert_allclose(g[b, h], w, rtol=1e-14, atol=1e-14)
+        for mode, hk, rep in ((O.MODE_P2, hk2, r2), (O.MODE_P1, hk1, r1)):
+            dq, dk = o.backward(q1, k1, q2, k2, 0.8, causal, dkl, mode, scale2=0.6)
+            assert dk.shape == (2, hk) + rep.shape[2:]
+            for b in range(2):
+                dks = [o.backward_head(q1[b, h], r1[b, h], q2[b, h], r2[b, h], 0.8, causal, dkl[b, h], mode,
+                                       scale2=0.6) for h in range(6)]
+                for h in range(6):
+                    np.testing.assert_allclose(dq[b, h], dks[h][0], rtol=1e-13, atol=1e-14)
+                want_dk = np.stack([x[1] for x in dks]).reshape(hk, 6 // hk, *rep.shape[2:]).sum(axis=1)
+                np.testing.assert_allclose(dk[b], want_dk, rtol=1e-12, atol=1e-13)
+
+
+def pin_grouped_key_heads_finite_differences(o):
+    # central differences of sum(dKL * KL) w.r.t. a key head shared by three
+    # query heads (MQA on the gradient side) and w.r.t. each query head
+    rng = np.random.default_rng(22)
+    for mode, causal in ((O.MODE_P2, False), (O.MODE_P1, True)):
+        hk1, hk2 = (3, 1) if mode == O.MODE_P2 else (1, 3)
+        args = list(_gqa_inputs(rng, 1, 3, hk1, hk2, 4, 5, 3, 2))
+        dkl = rng.uniform(0.5, 1.5, (1, 3, 4))
+        dq, dk = o.backward(*args, 0.9, causal, dkl, mode, scale2=0.7)
+        iq, ik = (2, 3) if mode == O.MODE_P2 else (0, 1)
+        for idx, got in ((iq, dq), (ik, dk)):
+            fd = np.zeros_like(args[idx])
+            for e in np.ndindex(*fd.shape):
+                old = args[idx][e]
+                args[idx][e] = old + 1e-6
+                lp = o.loss(*args, 0.9, causal, dkl, scale2=0.7)
+                args[idx][e] = old - 1e-6
+                lm = o.loss(*args, 0.9, causal, dkl, scale2=0.7)
+                args[idx][e] = old
+                fd[e] = (lp - lm) / 2e-6
+            err = np.abs(got - fd).max() / max(1e-12, np.abs(fd).max())
+            assert err < 1e-7, (mode, idx, err)
 
 
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
