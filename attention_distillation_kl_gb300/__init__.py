@@ -54,6 +54,11 @@ _SIGS = {
                                         _P, _P, _P, _P]),
     "streamkl_bwd_scaled": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _F, _I, _P, _P, _P, _P, _I,
                                  _I, _P, _P, _P]),
+    "streamkl_fwd_gqa": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _F, _I, _P, _P, _P, _P]),
+    "streamkl_fwd_splitk_gqa": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _F, _I, _I, _P, _SZ,
+                                     _P, _P, _P, _P]),
+    "streamkl_bwd_gqa": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _F, _I, _P, _P, _P, _P, _I,
+                              _I, _P, _P, _P]),
     "streamkl_bwd_both": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _F, _I, _P, _P, _P, _P, _I,
                                _P, _P, _P, _P, _P]),
     "streamkl_status_string": (ctypes.c_char_p, [_I]),
@@ -117,6 +122,24 @@ def _dims(q1, k1, q2, k2):
         raise ValueError("inconsistent shapes: want q1 [B,H,NQ,d1], k1 [B,H,NK,d1], "
                          "q2 [B,H,NQ,d2], k2 [B,H,NK,d2]")
     return B, H, NQ, NK, d1, d2
+
+
+def _dims_gqa(q1, k1, q2, k2):
+    """Like _dims, with k1 and k2 allowed their own head counts (grouped key
+    heads; the library checks that each divides the query head count)."""
+    for name, t in (("q1", q1), ("k1", k1), ("q2", q2), ("k2", k2)):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or not t.is_cuda:
+            raise TypeError(f"{name} must be a CUDA bf16 tensor")
+        if t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous [B, H, N, d] tensor")
+    B, H, NQ, d1 = q1.shape
+    HK1, NK = k1.shape[1], k1.shape[2]
+    HK2, d2 = k2.shape[1], q2.shape[3]
+    if tuple(k1.shape) != (B, HK1, NK, d1) or tuple(q2.shape) != (B, H, NQ, d2) or \
+            tuple(k2.shape) != (B, HK2, NK, d2):
+        raise ValueError("inconsistent shapes: want q1 [B,H,NQ,d1], k1 [B,HK1,NK,d1], "
+                         "q2 [B,H,NQ,d2], k2 [B,HK2,NK,d2]")
+    return B, H, HK1, HK2, NQ, NK, d1, d2
 
 
 def _out(t, shape, device, name):
@@ -260,6 +283,59 @@ def streamkl_bwd_scaled(q1, k1, q2, k2, scale1, scale2, causal, kl, lse1, lse2, 
                                      int(mode), int(bool(deterministic)), dq.data_ptr(), dk.data_ptr(),
                                      _stream(stream)),
            "streamkl_bwd_scaled")
+    return dq, dk
+
+
+def streamkl_fwd_gqa(q1, k1, q2, k2, scale1, scale2, causal, kl=None, lse1=None, lse2=None, stream=None):
+    """streamkl_fwd_scaled with grouped key heads: k1 [B, HK1, NK, d1] and
+    k2 [B, HK2, NK, d2], query head h reading key head h // (H // HK)."""
+    B, H, HK1, HK2, NQ, NK, d1, d2 = _dims_gqa(q1, k1, q2, k2)
+    kl = _out(kl, (B, H, NQ), q1.device, "kl")
+    lse1 = _out(lse1, (B, H, NQ), q1.device, "lse1")
+    lse2 = _out(lse2, (B, H, NQ), q1.device, "lse2")
+    _check(lib().streamkl_fwd_gqa(q1.data_ptr(), k1.data_ptr(), q2.data_ptr(), k2.data_ptr(),
+                                  B, H, HK1, HK2, NQ, NK, d1, d2, float(scale1), float(scale2), int(bool(causal)),
+                                  kl.data_ptr(), lse1.data_ptr(), lse2.data_ptr(), _stream(stream)),
+           "streamkl_fwd_gqa")
+    return kl, lse1, lse2
+
+
+def streamkl_fwd_splitk_gqa(q1, k1, q2, k2, scale1, scale2, causal, num_splits, workspace=None,
+                            kl=None, lse1=None, lse2=None, stream=None):
+    """streamkl_fwd_splitk_scaled with grouped key heads."""
+    B, H, HK1, HK2, NQ, NK, d1, d2 = _dims_gqa(q1, k1, q2, k2)
+    need = streamkl_fwd_splitk_workspace_bytes(B, H, NQ, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q1.device)
+    kl = _out(kl, (B, H, NQ), q1.device, "kl")
+    lse1 = _out(lse1, (B, H, NQ), q1.device, "lse1")
+    lse2 = _out(lse2, (B, H, NQ), q1.device, "lse2")
+    _check(lib().streamkl_fwd_splitk_gqa(q1.data_ptr(), k1.data_ptr(), q2.data_ptr(), k2.data_ptr(),
+                                         B, H, HK1, HK2, NQ, NK, d1, d2, float(scale1), float(scale2),
+                                         int(bool(causal)), int(num_splits), workspace.data_ptr(),
+                                         workspace.numel() * workspace.element_size(),
+                                         kl.data_ptr(), lse1.data_ptr(), lse2.data_ptr(), _stream(stream)),
+           "streamkl_fwd_splitk_gqa")
+    return kl, lse1, lse2
+
+
+def streamkl_bwd_gqa(q1, k1, q2, k2, scale1, scale2, causal, kl, lse1, lse2, dkl, mode=STREAMKL_GRAD_P2,
+                     deterministic=False, dq=None, dk=None, stream=None):
+    """streamkl_bwd_scaled with grouped key heads: dq [B, H, NQ, dg] per query
+    head, dk [B, HK_g, NK, dg] per key head of the gradient side (summed over
+    the query heads that read it)."""
+    B, H, HK1, HK2, NQ, NK, d1, d2 = _dims_gqa(q1, k1, q2, k2)
+    dg, hkg = (d2, HK2) if mode == STREAMKL_GRAD_P2 else (d1, HK1)
+    for name, t in (("kl", kl), ("lse1", lse1), ("lse2", lse2), ("dkl", dkl)):
+        _out(t, (B, H, NQ), q1.device, name)
+    dq = _out(dq, (B, H, NQ, dg), q1.device, "dq")
+    dk = _out(dk, (B, hkg, NK, dg), q1.device, "dk")
+    _check(lib().streamkl_bwd_gqa(q1.data_ptr(), k1.data_ptr(), q2.data_ptr(), k2.data_ptr(),
+                                  B, H, HK1, HK2, NQ, NK, d1, d2, float(scale1), float(scale2), int(bool(causal)),
+                                  kl.data_ptr(), lse1.data_ptr(), lse2.data_ptr(), dkl.data_ptr(),
+                                  int(mode), int(bool(deterministic)), dq.data_ptr(), dk.data_ptr(),
+                                  _stream(stream)),
+           "streamkl_bwd_gqa")
     return dq, dk
 
 

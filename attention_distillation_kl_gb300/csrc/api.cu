@@ -82,10 +82,13 @@ bool head_dim_ok(int d) { return d >= 16 && d <= 128 && d % 16 == 0; }
 
 // Shared validation of the problem description.  Returns STREAMKL_OK, or the
 // status to report.  Sets *empty when there is no row to compute.
-int check_problem(const void* q1, const void* k1, const void* q2, const void* k2, int B, int H,
-                  int NQ, int NK, int d1, int d2, float scale, int causal, bool* empty) {
+int check_problem(const void* q1, const void* k1, const void* q2, const void* k2, int B, int H, int HK1,
+                  int HK2, int NQ, int NK, int d1, int d2, float scale, int causal, bool* empty) {
   *empty = false;
   if (B < 0 || H < 0 || NQ < 0 || NK < 0) return STREAMKL_INVALID_ARG;
+  // key heads: each side's count divides the query head count
+  if (HK1 < 0 || HK2 < 0 || HK1 > H || HK2 > H) return STREAMKL_INVALID_ARG;
+  if (H > 0 && (HK1 == 0 || HK2 == 0 || H % HK1 != 0 || H % HK2 != 0)) return STREAMKL_INVALID_ARG;
   if (!scale_ok(scale)) return STREAMKL_INVALID_ARG;
   if (causal != 0 && causal != 1) return STREAMKL_INVALID_ARG;
   if (!head_dim_ok(d1) || !head_dim_ok(d2)) return STREAMKL_UNSUPPORTED;
@@ -114,10 +117,10 @@ int device_ok() {
   return STREAMKL_OK;
 }
 
-int make_maps(skl::TMaps* m, const void* q1, const void* k1, const void* q2, const void* k2, int BH,
-              int NQ, int NK, int d1, int d2) {
-  if (!make_map(&m->q1, q1, BH, NQ, d1) || !make_map(&m->k1, k1, BH, NK, d1) ||
-      !make_map(&m->q2, q2, BH, NQ, d2) || !make_map(&m->k2, k2, BH, NK, d2))
+int make_maps(skl::TMaps* m, const void* q1, const void* k1, const void* q2, const void* k2, int B, int H,
+              int HK1, int HK2, int NQ, int NK, int d1, int d2) {
+  if (!make_map(&m->q1, q1, (long long)B * H, NQ, d1) || !make_map(&m->k1, k1, (long long)B * HK1, NK, d1) ||
+      !make_map(&m->q2, q2, (long long)B * H, NQ, d2) || !make_map(&m->k2, k2, (long long)B * HK2, NK, d2))
     return STREAMKL_CUDA_ERROR;
   return STREAMKL_OK;
 }
@@ -128,22 +131,29 @@ int as_status(int cuda_err) { return cuda_err == 0 ? STREAMKL_OK : STREAMKL_CUDA
 
 extern "C" {
 
-int streamkl_fwd_scaled(const void* q1, const void* k1, const void* q2, const void* k2, int B, int H,
-                        int NQ, int NK, int d1, int d2, float scale1, float scale2, int causal, float* kl,
-                        float* lse1, float* lse2, streamkl_stream_t stream) {
+int streamkl_fwd_gqa(const void* q1, const void* k1, const void* q2, const void* k2, int B, int H, int HK1,
+                     int HK2, int NQ, int NK, int d1, int d2, float scale1, float scale2, int causal, float* kl,
+                     float* lse1, float* lse2, streamkl_stream_t stream) {
   bool empty = false;
-  int s = check_problem(q1, k1, q2, k2, B, H, NQ, NK, d1, d2, scale1, causal, &empty);
+  int s = check_problem(q1, k1, q2, k2, B, H, HK1, HK2, NQ, NK, d1, d2, scale1, causal, &empty);
   if (s == STREAMKL_OK && !scale_ok(scale2)) s = STREAMKL_INVALID_ARG;
   if (s != STREAMKL_OK || empty) return s;
   if (!kl || !lse1 || !lse2 || !aligned16(kl) || !aligned16(lse1) || !aligned16(lse2))
     return STREAMKL_INVALID_ARG;
   if ((s = device_ok()) != STREAMKL_OK) return s;
   skl::TMaps m{};
-  if ((s = make_maps(&m, q1, k1, q2, k2, B * H, NQ, NK, d1, d2)) != STREAMKL_OK) return s;
+  if ((s = make_maps(&m, q1, k1, q2, k2, B, H, HK1, HK2, NQ, NK, d1, d2)) != STREAMKL_OK) return s;
   int* st = status_ptr();
   if (!st) return STREAMKL_CUDA_ERROR;
-  skl::FwdArgs a{B * H, NQ, NK, causal, 1, scale1, scale2, kl, lse1, lse2, nullptr, st};
+  skl::FwdArgs a{B * H, NQ, NK, causal, 1, H / HK1, H / HK2, scale1, scale2, kl, lse1, lse2, nullptr, st};
   return as_status(skl::launch_fwd(m, tile_dim(d1), tile_dim(d2), a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int streamkl_fwd_scaled(const void* q1, const void* k1, const void* q2, const void* k2, int B, int H,
+                        int NQ, int NK, int d1, int d2, float scale1, float scale2, int causal, float* kl,
+                        float* lse1, float* lse2, streamkl_stream_t stream) {
+  return streamkl_fwd_gqa(q1, k1, q2, k2, B, H, H, H, NQ, NK, d1, d2, scale1, scale2, causal, kl, lse1, lse2,
+                          stream);
 }
 
 int streamkl_fwd(const void* q1, const void* k1, const void* q2, const void* k2, int B, int H,
@@ -158,12 +168,12 @@ size_t streamkl_fwd_splitk_workspace_bytes(int B, int H, int NQ, int num_splits)
   return size_t(5) * 4 * size_t(num_splits) * size_t(B) * size_t(H) * size_t(NQ);
 }
 
-int streamkl_fwd_splitk_scaled(const void* q1, const void* k1, const void* q2, const void* k2, int B,
-                               int H, int NQ, int NK, int d1, int d2, float scale1, float scale2, int causal,
-                               int num_splits, void* workspace, size_t workspace_bytes, float* kl,
-                               float* lse1, float* lse2, streamkl_stream_t stream) {
+int streamkl_fwd_splitk_gqa(const void* q1, const void* k1, const void* q2, const void* k2, int B, int H,
+                            int HK1, int HK2, int NQ, int NK, int d1, int d2, float scale1, float scale2,
+                            int causal, int num_splits, void* workspace, size_t workspace_bytes, float* kl,
+                            float* lse1, float* lse2, streamkl_stream_t stream) {
   bool empty = false;
-  int s = check_problem(q1, k1, q2, k2, B, H, NQ, NK, d1, d2, scale1, causal, &empty);
+  int s = check_problem(q1, k1, q2, k2, B, H, HK1, HK2, NQ, NK, d1, d2, scale1, causal, &empty);
   if (s == STREAMKL_OK && !scale_ok(scale2)) s = STREAMKL_INVALID_ARG;
   if (s != STREAMKL_OK) return s;
   if (num_splits < 1 || num_splits > 1024) return STREAMKL_INVALID_ARG;
@@ -174,15 +184,23 @@ int streamkl_fwd_splitk_scaled(const void* q1, const void* k1, const void* q2, c
   if (!workspace || !aligned16(workspace) || workspace_bytes < need) return STREAMKL_INVALID_ARG;
   if ((s = device_ok()) != STREAMKL_OK) return s;
   skl::TMaps m{};
-  if ((s = make_maps(&m, q1, k1, q2, k2, B * H, NQ, NK, d1, d2)) != STREAMKL_OK) return s;
+  if ((s = make_maps(&m, q1, k1, q2, k2, B, H, HK1, HK2, NQ, NK, d1, d2)) != STREAMKL_OK) return s;
   int* st = status_ptr();
   if (!st) return STREAMKL_CUDA_ERROR;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   float* part = static_cast<float*>(workspace);
-  skl::FwdArgs a{B * H, NQ, NK, causal, num_splits, scale1, scale2, kl, lse1, lse2, part, st};
+  skl::FwdArgs a{B * H, NQ, NK, causal, num_splits, H / HK1, H / HK2, scale1, scale2, kl, lse1, lse2, part, st};
   int e = skl::launch_fwd(m, tile_dim(d1), tile_dim(d2), a, cs);
   if (e != 0) return STREAMKL_CUDA_ERROR;
   return as_status(skl::launch_splitk_reduce(part, B * H * NQ, num_splits, kl, lse1, lse2, cs));
+}
+
+int streamkl_fwd_splitk_scaled(const void* q1, const void* k1, const void* q2, const void* k2, int B,
+                               int H, int NQ, int NK, int d1, int d2, float scale1, float scale2, int causal,
+                               int num_splits, void* workspace, size_t workspace_bytes, float* kl,
+                               float* lse1, float* lse2, streamkl_stream_t stream) {
+  return streamkl_fwd_splitk_gqa(q1, k1, q2, k2, B, H, H, H, NQ, NK, d1, d2, scale1, scale2, causal, num_splits,
+                                 workspace, workspace_bytes, kl, lse1, lse2, stream);
 }
 
 int streamkl_fwd_splitk(const void* q1, const void* k1, const void* q2, const void* k2, int B, int H,
@@ -205,24 +223,25 @@ int streamkl_suggest_splits(int B, int H, int NQ, int NK, int causal) {
   return s;
 }
 
-int streamkl_bwd_scaled(const void* q1, const void* k1, const void* q2, const void* k2, int B, int H,
-                        int NQ, int NK, int d1, int d2, float scale1, float scale2, int causal,
-                        const float* kl, const float* lse1, const float* lse2, const float* dkl, int mode,
-                        int deterministic, float* dq, float* dk, streamkl_stream_t stream) {
+int streamkl_bwd_gqa(const void* q1, const void* k1, const void* q2, const void* k2, int B, int H, int HK1,
+                     int HK2, int NQ, int NK, int d1, int d2, float scale1, float scale2, int causal,
+                     const float* kl, const float* lse1, const float* lse2, const float* dkl, int mode,
+                     int deterministic, float* dq, float* dk, streamkl_stream_t stream) {
   bool empty = false;
-  int s = check_problem(q1, k1, q2, k2, B, H, NQ, NK, d1, d2, scale1, causal, &empty);
+  int s = check_problem(q1, k1, q2, k2, B, H, HK1, HK2, NQ, NK, d1, d2, scale1, causal, &empty);
   if (s == STREAMKL_OK && !scale_ok(scale2)) s = STREAMKL_INVALID_ARG;
   if (s != STREAMKL_OK) return s;
   if (mode != STREAMKL_GRAD_P2 && mode != STREAMKL_GRAD_P1) return STREAMKL_INVALID_ARG;
   if (deterministic != 0 && deterministic != 1) return STREAMKL_INVALID_ARG;
   const int dg = mode == STREAMKL_GRAD_P2 ? d2 : d1;
+  const int hkg = mode == STREAMKL_GRAD_P2 ? HK2 : HK1;  // key heads of dk
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const size_t dk_bytes = size_t(B) * hkg * NK * dg * 4;
   if (empty) {
     // no query rows: dK is zero (dq is empty)
-    const size_t bytes = size_t(B) * H * NK * dg * 4;
-    if (bytes == 0) return STREAMKL_OK;
+    if (dk_bytes == 0) return STREAMKL_OK;
     if (!dk || !aligned16(dk)) return STREAMKL_INVALID_ARG;
-    return as_status(cudaMemsetAsync(dk, 0, bytes, cs));
+    return as_status(cudaMemsetAsync(dk, 0, dk_bytes, cs));
   }
   if (!kl || !lse1 || !lse2 || !dkl || !dq || !dk) return STREAMKL_INVALID_ARG;
   if (!aligned16(kl) || !aligned16(lse1) || !aligned16(lse2) || !aligned16(dkl) || !aligned16(dq) ||
@@ -230,21 +249,38 @@ int streamkl_bwd_scaled(const void* q1, const void* k1, const void* q2, const vo
     return STREAMKL_INVALID_ARG;
   if ((s = device_ok()) != STREAMKL_OK) return s;
   skl::TMaps m{};
-  if ((s = make_maps(&m, q1, k1, q2, k2, B * H, NQ, NK, d1, d2)) != STREAMKL_OK) return s;
+  if ((s = make_maps(&m, q1, k1, q2, k2, B, H, HK1, HK2, NQ, NK, d1, d2)) != STREAMKL_OK) return s;
   int* st = status_ptr();
   if (!st) return STREAMKL_CUDA_ERROR;
-  skl::BwdArgs a{B * H, NQ, NK, causal, mode, dg, scale1, scale2, kl, lse1, lse2, dkl, dq, dk, st, 1};
+  const int gg = H / hkg;  // query heads per key head of dk
+  skl::BwdArgs a{B * H, NQ, NK, causal, mode, dg, H / HK1, H / HK2, -1, scale1, scale2, kl, lse1, lse2, dkl, dq,
+                 dk, st, 1};
   const int t1 = tile_dim(d1), t2 = tile_dim(d2);
   if (!deterministic) {
     const size_t dq_bytes = size_t(B) * H * NQ * dg * 4;
     if (!make_map_dq(&m.dq, dq, (long long)B * H, NQ, dg)) return STREAMKL_CUDA_ERROR;
     if (cudaMemsetAsync(dq, 0, dq_bytes, cs) != cudaSuccess) return STREAMKL_CUDA_ERROR;
+    // a shared key head's dK is accumulated by the CTAs of its query heads
+    if (gg > 1 && cudaMemsetAsync(dk, 0, dk_bytes, cs) != cudaSuccess) return STREAMKL_CUDA_ERROR;
     return as_status(skl::launch_bwd_fused(m, t1, t2, a, cs));
   }
+  // deterministic: dK from one launch per query head of each group, in order
+  // (the first stores, the others add), then dQ from its own kernel
   a.write_dq = 0;
-  int e = skl::launch_bwd_fused(m, t1, t2, a, cs);
-  if (e != 0) return STREAMKL_CUDA_ERROR;
+  for (int j = 0; j < gg; ++j) {
+    a.hsel = gg > 1 ? j : -1;
+    if (skl::launch_bwd_fused(m, t1, t2, a, cs) != 0) return STREAMKL_CUDA_ERROR;
+  }
+  a.hsel = -1;
   return as_status(skl::launch_bwd_dq(m, t1, t2, a, cs));
+}
+
+int streamkl_bwd_scaled(const void* q1, const void* k1, const void* q2, const void* k2, int B, int H,
+                        int NQ, int NK, int d1, int d2, float scale1, float scale2, int causal,
+                        const float* kl, const float* lse1, const float* lse2, const float* dkl, int mode,
+                        int deterministic, float* dq, float* dk, streamkl_stream_t stream) {
+  return streamkl_bwd_gqa(q1, k1, q2, k2, B, H, H, H, NQ, NK, d1, d2, scale1, scale2, causal, kl, lse1, lse2,
+                          dkl, mode, deterministic, dq, dk, stream);
 }
 
 int streamkl_bwd(const void* q1, const void* k1, const void* q2, const void* k2, int B, int H,
@@ -260,7 +296,7 @@ int streamkl_bwd_both(const void* q1, const void* k1, const void* q2, const void
                       const float* lse1, const float* lse2, const float* dkl, int deterministic, float* dq1,
                       float* dk1, float* dq2, float* dk2, streamkl_stream_t stream) {
   bool empty = false;
-  int s = check_problem(q1, k1, q2, k2, B, H, NQ, NK, d1, d2, scale1, causal, &empty);
+  int s = check_problem(q1, k1, q2, k2, B, H, H, H, NQ, NK, d1, d2, scale1, causal, &empty);
   if (s == STREAMKL_OK && !scale_ok(scale2)) s = STREAMKL_INVALID_ARG;
   if (s != STREAMKL_OK) return s;
   if (deterministic != 0 && deterministic != 1) return STREAMKL_INVALID_ARG;
@@ -278,7 +314,7 @@ int streamkl_bwd_both(const void* q1, const void* k1, const void* q2, const void
     return STREAMKL_INVALID_ARG;
   if ((s = device_ok()) != STREAMKL_OK) return s;
   skl::TMaps m{};
-  if ((s = make_maps(&m, q1, k1, q2, k2, B * H, NQ, NK, d1, d2)) != STREAMKL_OK) return s;
+  if ((s = make_maps(&m, q1, k1, q2, k2, B, H, H, H, NQ, NK, d1, d2)) != STREAMKL_OK) return s;
   if (!make_map_dq(&m.dq, dq1, (long long)B * H, NQ, d1) || !make_map_dq(&m.dq2, dq2, (long long)B * H, NQ, d1))
     return STREAMKL_CUDA_ERROR;
   int* st = status_ptr();
@@ -287,8 +323,8 @@ int streamkl_bwd_both(const void* q1, const void* k1, const void* q2, const void
   const size_t dq_bytes = size_t(B) * H * NQ * d1 * 4;
   if (cudaMemsetAsync(dq1, 0, dq_bytes, cs) != cudaSuccess || cudaMemsetAsync(dq2, 0, dq_bytes, cs) != cudaSuccess)
     return STREAMKL_CUDA_ERROR;
-  skl::BwdArgs a{B * H, NQ, NK, causal, STREAMKL_GRAD_P2, d1, scale1, scale2, kl, lse1, lse2, dkl, dq1, dk1, st, 1,
-                 dq2, dk2};
+  skl::BwdArgs a{B * H, NQ, NK, causal, STREAMKL_GRAD_P2, d1, 1, 1, -1, scale1, scale2, kl, lse1, lse2,
+                 dkl, dq1, dk1, st, 1, dq2, dk2};
   return as_status(skl::launch_bwd_both(m, tile_dim(d1), a, cs));
 }
 

@@ -91,7 +91,8 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
   const uint32_t sb = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  const int kt = blockIdx.x, bh = blockIdx.y;
+  const int gg = kP2 ? a.g2 : a.g1;  // query heads per gradient-side key head
+  const int kt = blockIdx.x, bh = a.hsel < 0 ? int(blockIdx.y) : int(blockIdx.y) * gg + a.hsel;
   const int k0 = kt * kTile;
   const int off = a.NK - a.NQ;
   const int nqt = (a.NQ + kTile - 1) / kTile;
@@ -137,8 +138,8 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
       tma_prefetch_desc(&tq2);
       tma_prefetch_desc(&tk2);
       mbar_arrive_expect_tx(bar(L::B_KFULL), L::kK1 + L::kK2);
-      T1::load(sb + L::oK1, &tk1, bar(L::B_KFULL), k0, bh);
-      T2::load(sb + L::oK2, &tk2, bar(L::B_KFULL), k0, bh);
+      T1::load(sb + L::oK1, &tk1, bar(L::B_KFULL), k0, bh / a.g1);
+      T2::load(sb + L::oK2, &tk2, bar(L::B_KFULL), k0, bh / a.g2);
       int issued = 0;
       for (int i = 0; i < n; ++i) {
         const int q0 = (qt_lo + i) * kTile;
@@ -362,10 +363,13 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
       }
       if (lane == 0) bulk_wait_all();  // every reduce has landed before the CTA exits
     }
+    // dK of key head bh / gg: stored, or (grouped key heads) added to what
+    // the other query heads of the group contribute
+    const int dk_how = (gg == 1 || a.hsel == 0) ? kDkStore : (a.hsel < 0 ? kDkAtomic : kDkAdd);
+    const int kj = k0 + row;
+    float* dst = a.dk + (size_t(bh / gg) * a.NK + kj) * a.dg;
     if (n > 0 && mbar_wait_warp(bar(L::B_DKFULL), 0, ctl)) {
       tc_fence_after();
-      const int kj = k0 + row;
-      float* dst = a.dk + (size_t(bh) * a.NK + kj) * a.dg;
 #pragma unroll
       for (int ch = 0; ch < DG / 32; ++ch) {
         uint32_t v[32];
@@ -374,17 +378,15 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 32; e += 4)
             if (ch * 32 + e < a.dg)
-              *reinterpret_cast<float4*>(dst + ch * 32 + e) =
-                  make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]), __uint_as_float(v[e + 2]),
-                              __uint_as_float(v[e + 3]));
+              put_dk4(dst + ch * 32 + e,
+                      make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]), __uint_as_float(v[e + 2]),
+                                  __uint_as_float(v[e + 3])),
+                      dk_how);
         }
       }
-    } else if (n == 0) {
+    } else if (n == 0 && dk_how == kDkStore && kj < a.NK) {
       // no query row sees this key tile: its dK is zero
-      const int kj = k0 + row;
-      if (kj < a.NK)
-        for (int e = 0; e < a.dg; e += 4)
-          *reinterpret_cast<float4*>(a.dk + (size_t(bh) * a.NK + kj) * a.dg + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int e = 0; e < a.dg; e += 4) *reinterpret_cast<float4*>(dst + e) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
 
@@ -486,8 +488,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         if (!mbar_wait_polled(bar(L::B_KEMPTY0 + s), ((j >> 1) & 1) ^ 1, ctl)) break;
         mbar_arrive_expect_tx(bar(L::B_KFULL0 + s), L::kStage);
         const uint32_t st = sb + L::oK + s * L::kStage;
-        T1::load(st, &tk1, bar(L::B_KFULL0 + s), j * kTile, bh);
-        T2::load(st + L::kK1, &tk2, bar(L::B_KFULL0 + s), j * kTile, bh);
+        T1::load(st, &tk1, bar(L::B_KFULL0 + s), j * kTile, bh / a.g1);
+        T2::load(st + L::kK1, &tk2, bar(L::B_KFULL0 + s), j * kTile, bh / a.g2);
         issued = j + 1;
       }
       if (*abort_flag) {
@@ -620,7 +622,8 @@ static int launch_fused_t(const TMaps& m, const BwdArgs& a, cudaStream_t st) {
   auto kern = bwd_fused_kernel<D1, D2, MODE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
-  dim3 grid((a.NK + kTile - 1) / kTile, a.BH);
+  const int gg = MODE == STREAMKL_GRAD_P2 ? a.g2 : a.g1;
+  dim3 grid((a.NK + kTile - 1) / kTile, a.hsel < 0 ? a.BH : a.BH / gg);
   kern<<<grid, L::kThreads, L::kAlloc, st>>>(m.q1, m.k1, m.q2, m.k2, m.dq, a);
   return cudaGetLastError();
 }

@@ -14,6 +14,23 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// How a dK row chunk reaches global memory: plain store (the CTA owns the
+// key head), atomic add (several CTAs of a key-head group at once) or
+// read-add-write (the launches of a group run one after the other).
+enum { kDkStore = 0, kDkAtomic = 1, kDkAdd = 2 };
+
+__device__ __forceinline__ void put_dk4(float* p, float4 v, int how) {
+  float4* q = reinterpret_cast<float4*>(p);
+  if (how == kDkStore) {
+    *q = v;
+  } else if (how == kDkAtomic) {
+    atomicAdd(q, v);
+  } else {
+    const float4 o = *q;
+    *q = make_float4(o.x + v.x, o.y + v.y, o.z + v.z, o.w + v.w);
+  }
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)

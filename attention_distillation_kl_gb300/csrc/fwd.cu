@@ -193,8 +193,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         mbar_arrive_expect_tx(bar_kfull(s), L::kStage);
         const int k0 = (kt_lo + j) * kTile;
         const uint32_t st = sb + L::oK + s * L::kStage;
-        T1::load(st, &tk1, bar_kfull(s), k0, bh);
-        T2::load(st + L::kK1, &tk2, bar_kfull(s), k0, bh);
+        T1::load(st, &tk1, bar_kfull(s), k0, bh / a.g1);
+        T2::load(st + L::kK1, &tk2, bar_kfull(s), k0, bh / a.g2);
         issued = j + 1;
       }
       if (*abort_flag) {  // let the copies already started land before the CTA exits

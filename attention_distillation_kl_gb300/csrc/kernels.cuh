@@ -18,6 +18,7 @@ struct TMaps {
 
 struct FwdArgs {
   int BH, NQ, NK, causal, num_splits;
+  int g1, g2;  // query heads per key head of each side (grouped key heads; 1 = one key head per query head)
   float scale1, scale2;  // S1 = scale1 Q1 K1^T, S2 = scale2 Q2 K2^T
   float* kl;
   float* lse1;
@@ -29,6 +30,12 @@ struct FwdArgs {
 struct BwdArgs {
   int BH, NQ, NK, causal, mode;
   int dg;  // the gradient side's head dim: row length of dq, dk (at most the kernel's tile width)
+  int g1, g2;  // query heads per key head of each side; dk has BH / g_grad heads
+  // Query heads of the fused kernel: -1 = every head (grid.y = BH), dK of a
+  // shared key head added with atomics into a zeroed dk; j >= 0 = head
+  // j of every group only (grid.y = BH / g_grad), dK stored (j = 0) or added
+  // in place (j > 0), so launches j = 0, 1, ... sum in a fixed order.
+  int hsel;
   float scale1, scale2;
   const float* kl;
   const float* lse1;

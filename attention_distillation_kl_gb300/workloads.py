@@ -117,6 +117,15 @@ def generate(w: Workload, heads=None):
     return q1, k1, q2, k2
 
 
+def generate_gqa(w: Workload, hk1: int, hk2: int, sd: float = 1.2):
+    """Inputs with grouped key heads: q1 [B, H, NQ, d1], k1 [B, hk1, NK, d1],
+    q2 [B, H, NQ, d2], k2 [B, hk2, NK, d2], every element N(0, sd^2) drawn
+    independently from a generator seeded with w.seed (bf16 CPU tensors)."""
+    g = torch.Generator().manual_seed(w.seed)
+    shapes = ((w.H, w.NQ, w.d1), (hk1, w.NK, w.d1), (w.H, w.NQ, w.d2), (hk2, w.NK, w.d2))
+    return [(sd * torch.randn((w.B,) + s, generator=g)).to(torch.bfloat16) for s in shapes]
+
+
 def generate_dkl(w: Workload, kind: str = "ones", seed: int = 0) -> torch.Tensor:
     """Upstream gradient dL/dKL, fp32 [B, H, NQ]: all ones (the gradient of
     sum(KL)), U(0.5, 1.5) to exercise per-row indexing ("uniform"), or

@@ -175,6 +175,35 @@ int streamkl_bwd_scaled(const void* q1, const void* k1, const void* q2, const vo
                         streamkl_stream_t stream);
 
 /*
+ * Grouped key heads (GQA; MQA with one key head per side).  Not on the
+ * pages; taken in the usual sense: q1, q2 have H heads, k1 has HK1 and k2
+ * has HK2 heads ([B, HK, NK, d], each count dividing H, else INVALID_ARG),
+ * and query head h reads key head h / (H / HK) of its side.  KL, LSE1, LSE2
+ * stay per query head [B, H, NQ]; dq is [B, H, NQ, dg]; dk is the gradient
+ * of the shared key heads, [B, HK_g, NK, dg] with HK_g the gradient side's
+ * count (HK2 in mode P2, HK1 in mode P1): the sum over the query heads
+ * that read each key head.  With deterministic = 0 a shared head's dK is
+ * added up with fp32 atomics (order not fixed); with deterministic = 1 the
+ * query heads of a group are taken one launch after another in head order,
+ * so the result is bitwise repeatable.  Otherwise as the *_scaled calls,
+ * which are these with HK1 = HK2 = H.
+ */
+int streamkl_fwd_gqa(const void* q1, const void* k1, const void* q2, const void* k2,
+                     int B, int H, int HK1, int HK2, int NQ, int NK, int d1, int d2,
+                     float scale1, float scale2, int causal, float* kl, float* lse1, float* lse2,
+                     streamkl_stream_t stream);
+int streamkl_fwd_splitk_gqa(const void* q1, const void* k1, const void* q2, const void* k2,
+                            int B, int H, int HK1, int HK2, int NQ, int NK, int d1, int d2,
+                            float scale1, float scale2, int causal, int num_splits, void* workspace,
+                            size_t workspace_bytes, float* kl, float* lse1, float* lse2,
+                            streamkl_stream_t stream);
+int streamkl_bwd_gqa(const void* q1, const void* k1, const void* q2, const void* k2,
+                     int B, int H, int HK1, int HK2, int NQ, int NK, int d1, int d2,
+                     float scale1, float scale2, int causal, const float* kl, const float* lse1,
+                     const float* lse2, const float* dkl, int mode, int deterministic, float* dq,
+                     float* dk, streamkl_stream_t stream);
+
+/*
  * Both-sides backward: the gradients of sum_i dkl_i * KL_i with respect to
  * both distributions (dq1, dk1 with head dim d1; dq2, dk2 with d2; fp32,
  * fully overwritten), from one recompute of S1 and S2 per tile pair when

@@ -163,3 +163,30 @@ def test_bwd_both_validation(L):
     assert f(*base, 0.125, 0.125, 0, *tail, 0, A, A, 0, A, None) == skl.STREAMKL_INVALID_ARG   # null dq2
     assert f(*base, 0.125, 0.125, 0, *tail, 0, A, A, A, A + 4, None) == skl.STREAMKL_INVALID_ARG  # misaligned dk2
     assert f(A, A, A, A, 1, 1, 128, 128, 72, 64, 0.1, 0.1, 0, *tail, 0, A, A, A, A, None) == skl.STREAMKL_UNSUPPORTED
+
+
+@pytest.mark.parametrize("H,HK1,HK2,ok", [
+    (8, 8, 8, True), (8, 2, 8, True), (8, 1, 4, True),
+    (8, 3, 8, False),    # 3 does not divide 8
+    (8, 8, 16, False),   # more key heads than query heads
+    (8, 0, 8, False),
+    (8, 8, -1, False),
+])
+def test_gqa_head_counts(L, H, HK1, HK2, ok):
+    # a bad head layout is INVALID_ARG before anything else is looked at; a
+    # good one is accepted (shown on an empty problem, which needs no GPU)
+    fwd_args = (A, A, A, A, 1, H, HK1, HK2, 128, 128, 64, 64, 0.125, 0.125, 0)
+    if ok:
+        # empty problem (NQ = 0) with the same head layout is a no-op
+        assert L.streamkl_fwd_gqa(0, 0, 0, 0, 1, H, HK1, HK2, 0, 128, 64, 64, 0.125, 0.125, 0, 0, 0, 0,
+                                  None) == skl.STREAMKL_OK
+    else:
+        assert L.streamkl_fwd_gqa(*fwd_args, A, A, A, None) == skl.STREAMKL_INVALID_ARG
+        assert L.streamkl_fwd_splitk_gqa(*fwd_args, 2, A, 1 << 20, A, A, A, None) == skl.STREAMKL_INVALID_ARG
+        assert L.streamkl_bwd_gqa(*fwd_args, A, A, A, A, 0, 0, A, A, None) == skl.STREAMKL_INVALID_ARG
+
+
+def test_gqa_empty_backward_zeroes_key_heads_only(L):
+    # NQ = 0: nothing to compute, and with no dk buffer (size 0) nothing to zero
+    assert L.streamkl_bwd_gqa(0, 0, 0, 0, 0, 8, 2, 2, 0, 128, 64, 64, 0.125, 0.125, 0, 0, 0, 0, 0, 0, 0, 0, 0,
+                              None) == skl.STREAMKL_OK
