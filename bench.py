@@ -246,6 +246,45 @@ def key_split_timing(skl, stream):
     return out
 
 
+def gqa_timing(skl, stream):
+    """Grouped key heads: 32 query heads sharing 8 key heads on each side
+    (16K tokens, d = 128, causal): forward, fused and deterministic P2
+    backward (dK of each shared head summed over its 4 query heads)."""
+    from attention_distillation_kl_gb300.workloads import Workload, generate_gqa
+    w = Workload("gqa", 1, 32, 16384, 16384, 128, 128, True, 1 / np.sqrt(128), "independent", 0.0, 1.0, 1007)
+    hk = 8
+    dev = [t.cuda() for t in generate_gqa(w, hk, hk, sd=1.0)]
+    kl, l1, l2 = skl.streamkl_fwd_gqa(*dev, w.scale, w.scale, w.causal)
+    dkl = torch.ones_like(kl)
+    dq = torch.empty(w.B, w.H, w.NQ, w.d2, device="cuda")
+    dk = torch.empty(w.B, hk, w.NK, w.d2, device="cuda")
+
+    def timed(fn, reps=4):
+        fn()
+        ts = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return float(np.median(ts))
+
+    f_fwd, f_bwd = flops(w)
+    out = {"workload": f"B={w.B} H={w.H} HK1=HK2={hk} NQ=NK={w.NQ} d1=d2=128 causal"}
+    out["fwd_ms"] = timed(lambda: skl.streamkl_fwd_gqa(*dev, w.scale, w.scale, w.causal, kl, l1, l2))
+    out["bwd_p2_ms"] = timed(lambda: skl.streamkl_bwd_gqa(*dev, w.scale, w.scale, w.causal, kl, l1, l2, dkl,
+                                                          skl.STREAMKL_GRAD_P2, False, dq, dk))
+    out["bwd_p2_det_ms"] = timed(lambda: skl.streamkl_bwd_gqa(*dev, w.scale, w.scale, w.causal, kl, l1, l2, dkl,
+                                                              skl.STREAMKL_GRAD_P2, True, dq, dk))
+    out["fwd_tflops"] = f_fwd / (out["fwd_ms"] * 1e-3) / 1e12
+    out["bwd_p2_tflops"] = f_bwd / (out["bwd_p2_ms"] * 1e-3) / 1e12
+    del dev, dq, dk
+    torch.cuda.empty_cache()
+    return out
+
+
 def both_sides_timing(skl, stream, d=64):
     """Both-sides backward in one pass against the two single-side passes,
     on a d1 = d2 = d problem (16K tokens x 32 heads, causal)."""
@@ -411,6 +450,7 @@ def run_mine(args, rank, world, local):
     c5 = key_split_timing(skl, stream) if rank == 0 and world == 1 and not args.no_cpu_baseline else None
     both = both_sides_timing(skl, stream) if rank == 0 and world == 1 and not args.no_cpu_baseline else None
     both32 = both_sides_timing(skl, stream, 32) if both is not None else None
+    gqa = gqa_timing(skl, stream) if both is not None else None
 
     rate = ex2_rate(skl)
     burst, sustained, _hbm, src = peaks()
@@ -448,6 +488,7 @@ def run_mine(args, rank, world, local):
             "key_split_131k": c5,
             "both_sides_d64": both,
             "both_sides_d32": both32,
+            "gqa_16k": gqa,
             "ex2_per_s": rate,
             "roofline": {"bound": "tensor", "achieved": bwd_tf if dom == "bwd" else fwd_tf,
                          "peak": sustained, "unit": "TFLOP/s",
