@@ -17,6 +17,9 @@ __all__ = [
     "StreamKLError", "lib", "library_path",
     "streamkl_fwd", "streamkl_fwd_splitk", "streamkl_fwd_splitk_workspace_bytes",
     "streamkl_suggest_splits", "streamkl_fwd_splitk_noalloc", "streamkl_bwd", "streamkl_status_string",
+    "streamkl_fwd_scaled", "streamkl_fwd_splitk_scaled", "streamkl_bwd_scaled",
+    "streamkl_fwd_gqa", "streamkl_fwd_splitk_gqa", "streamkl_bwd_gqa", "streamkl_bwd_both",
+    "status_string", "STREAMKL_STATIC_WORKSPACE_BYTES",
     "streamkl_get_device_status", "streamkl_probe_ex2", "streamkl_selftest_wait_timeout",
     "STREAMKL_OK", "STREAMKL_INVALID_ARG", "STREAMKL_UNSUPPORTED", "STREAMKL_CUDA_ERROR",
     "STREAMKL_DEVICE_TIMEOUT", "STREAMKL_GRAD_P2", "STREAMKL_GRAD_P1",

@@ -41,6 +41,13 @@ def test_library_exports_every_declared_symbol(L):
         assert name in skl._SIGS, f"binding lacks {name}"
 
 
+def test_binding_wraps_every_entry_point():
+    # each C entry point has a Python function of the same name, exported
+    for name in declared_symbols():
+        assert callable(getattr(skl, name, None)), f"no Python wrapper for {name}"
+        assert name in skl.__all__, f"{name} missing from __all__"
+
+
 def test_status_strings(L):
     for s in range(5):
         assert skl.status_string(s) and skl.status_string(s) != "unknown status"
