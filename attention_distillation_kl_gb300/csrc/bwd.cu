@@ -31,8 +31,8 @@
 //   warps 8-11 dQ tile: TMEM -> registers (scaled) -> 32 x 16 fp32 boxes in
 //              swizzled shared memory (four per warp, round robin) -> TMA
 //              bulk tensor reduce-add into global dQ (rows past NQ are
-//              clipped by the tensor map); finally dK (each CTA owns its
-//              keys: plain stores)
+//              clipped by the tensor map); finally dK (stored, or added when
+//              a key head is shared by several query heads: put_dk4)
 // TMEM: S1 [0,128), S2 [128,256), dK [256, 256+dg), dQ [384, 384+dg).
 //
 // dQ-only kernel (deterministic two-pass mode): one CTA per query tile walks

@@ -11,7 +11,7 @@
 // S1 - S2).
 //
 // GB300 mapping (10 warps, 1 CTA per SM):
-//   warp 8      TMA producer: Q1/Q2 once, then K1_j/K2_j into a ring of stages
+//   warp 8      TMA producer: Q1/Q2 once, then K1_j/K2_j (key head h / G) into a ring
 //   warp 9      TMEM owner and MMA issuer: S1 = Q1 K1_j^T and S2 = Q2 K2_j^T
 //               (tcgen05, M = N = 128, bf16 -> fp32) into one of two TMEM
 //               buffers of 256 columns, so tile j+1 is multiplied while the
