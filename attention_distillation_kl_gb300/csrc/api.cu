@@ -1,5 +1,6 @@
 // C-ABI entry points of libstreamkl: argument validation, TMA tensor maps,
 // launches.  Every check that can fail does so before anything is enqueued.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -212,15 +213,43 @@ int streamkl_fwd_splitk(const void* q1, const void* k1, const void* q2, const vo
 }
 
 int streamkl_suggest_splits(int B, int H, int NQ, int NK, int causal) {
-  if (B <= 0 || H <= 0 || NQ <= 0 || NK <= 0 || (causal && NQ > NK)) return 0;
-  int dev = 0, sms = 152;
-  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const long long ctas = (long long)B * H * ((NQ + skl::kTile - 1) / skl::kTile);
+  if (B <= 0 || H <= 0 || NQ <= 0 || NK <= 0 || (causal != 0 && causal != 1) || (causal && NQ > NK)) return 0;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+    return 1;  // no device to size for: no split
+  const long long nqt = (NQ + skl::kTile - 1) / skl::kTile;
+  const long long ctas = (long long)B * H * nqt;
+  if (ctas >= 4ll * sms) return 1;  // several waves of whole rows already
   const int max_kt = (NK + skl::kTile - 1) / skl::kTile;
-  int s = 1;
-  // at least two full waves of one CTA per SM, and at least 8 key tiles per split
-  while (ctas * s < 2ll * sms && s * 2 <= max_kt / 8 && s < 1024) s *= 2;
-  return s;
+  const int off = NK - NQ;
+  // Cost model in units of one key tile of one CTA: a CTA with t key tiles
+  // takes t + kFixed (Q load, pipeline fill, epilogue); the CTAs (one per SM,
+  // longest first) finish after max(total / SMs, longest CTA); a split count
+  // s > 1 adds the merge kernel (a launch plus 20 bytes per row and split).
+  constexpr double kFixed = 3.0, kMergeLaunch = 10.0, kMergeBytesPerTile = 3.6e6;
+  const double rows = double(B) * H * NQ;
+  int best = 1;
+  double best_t = 0.0;
+  for (int s = 1; s <= 1024 && s <= max_kt; ++s) {
+    double total = 0.0, longest = 0.0;
+    for (long long qt = 0; qt < nqt; ++qt) {
+      const long long kend = causal ? (long long)std::min<long long>((qt + 1) * skl::kTile, NQ) + off : NK;
+      const long long tiles = (kend + skl::kTile - 1) / skl::kTile;
+      // splits take contiguous shares of the key tiles; the largest share bounds the CTA
+      const double t = double((tiles + s - 1) / s) + kFixed;
+      total += t * s;
+      longest = std::max(longest, t);
+    }
+    total *= double(B) * H;
+    double t = std::max(total / sms, longest);
+    if (s > 1) t += kMergeLaunch + rows * s * 20.0 / kMergeBytesPerTile;
+    if (s == 1 || t < best_t * 0.98) {  // a split has to earn its merge
+      best = s;
+      best_t = t;
+    }
+  }
+  return best;
 }
 
 int streamkl_bwd_gqa(const void* q1, const void* k1, const void* q2, const void* k2, int B, int H, int HK1,

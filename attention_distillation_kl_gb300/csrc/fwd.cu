@@ -412,9 +412,10 @@ int launch_fwd(const TMaps& m, int d1, int d2, const FwdArgs& a, cudaStream_t st
 
 int launch_splitk_reduce(const float* partial, int rows, int num_splits, float* kl, float* lse1,
                          float* lse2, cudaStream_t st) {
-  int dev = 0, sms = 152;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+    sms = 1;  // the grid-stride loop covers every row with any block count
   int blocks = (rows + 255) / 256;
   if (blocks > sms * 8) blocks = sms * 8;
   if (blocks < 1) blocks = 1;

@@ -32,7 +32,9 @@ std::mutex g_mu;
 void* g_ws_addr[kMaxDevices] = {};
 
 // Device address of g_splitk_static_ws on the current device, looked up on
-// the first call for that device.  Returns STREAMKL_OK and sets *out.
+// the first call for that device.  Returns STREAMKL_OK and sets *out.  The
+// cache outlives a cudaDeviceReset (which unloads the module and may move
+// the array), so the entry point is documented as unusable after one.
 int static_ws_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return STREAMKL_CUDA_ERROR;

@@ -191,7 +191,7 @@ def run_reference(args, rank):
 
 def ex2_rate(skl):
     out = torch.empty(1, device="cuda")
-    blocks, iters = 152 * 8, 4096
+    blocks, iters = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count * 8, 4096
     skl.streamkl_probe_ex2(out, blocks, iters)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     best = None

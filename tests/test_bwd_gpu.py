@@ -151,3 +151,25 @@ def test_signed_upstream_gradient(shape, mode, det):
     B, H, NQ, NK, d1, d2, causal = shape
     w = Workload("signed", B, H, NQ, NK, d1, d2, causal, 1.0 / np.sqrt(d1), "independent", 0.0, 1.2, 81)
     check_full(w, mode, det, "signed")
+
+
+@pytest.mark.parametrize("name,hb", [("c4", (0, 17)), ("c5", (0, 2))], ids=["c4-P2", "c5-P2"])
+def test_large_workload_early_key_tiles(name, hb):
+    """dK at the headline sizes for keys of the first key tile (summed over
+    every query tile of the head: 512 at 64K, 1024 at 128K) and of a middle
+    tile, against the oracle over all the rows that see them (row blocks in
+    a spawn pool: tests/oracle_pool.py), in the benchmark's launch
+    configuration (fused P2 backward over all heads)."""
+    from oracle_pool import dk_keys_pooled
+    w = WORKLOADS[name]
+    host, dev = inputs(w)
+    dkl = generate_dkl(w)
+    gdq, gdk = gpu_grads(w, dev, dkl.cuda(), skl.STREAMKL_GRAD_P2, False)
+    del dev, gdq
+    b, h = hb
+    mid = (w.NK // 128 // 2) * 128
+    keys = np.array([0, 1, 37, 64, 90, 126, 127, mid, mid + 5, mid + 63, mid + 64, mid + 100, mid + 127])
+    f = head64(host, b, h)
+    rdk = dk_keys_pooled(*f, w.scale, w.causal, to_f64(dkl)[b, h], oracle.MODE_P2, keys)
+    assert frob_rel(gdk[b, h, keys[:7]], rdk[:7]) <= GRAD_RTOL, (name, "key tile 0")
+    assert frob_rel(gdk[b, h, keys[7:]], rdk[7:]) <= GRAD_RTOL, (name, "middle key tile")

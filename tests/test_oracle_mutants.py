@@ -43,6 +43,10 @@ MUTANTS = {
                                    "k1[b, h % k1.shape[1]], q2[b, h], k2[b, h % k2.shape[1]], scale, causal, row_block,\n"),
     "grouped dK overwritten, not summed": ("dk[b, h // gg] += dk_h", "dk[b, h // gg] = dk_h"),
     "grouped dK into the other side's head": ("dk[b, h // gg] += dk_h", "dk[b, h // (g1 if gg == g2 else g2)] += dk_h"),
+    "sampled forward rows taken as positions": ("causal, np.asarray(rows))\n    return r[\"kl\"]",
+                                                "causal, np.arange(len(rows)))\n    return r[\"kl\"]"),
+    "sampled forward ignores the second scale": ("r = _head_rows(q1, k1, q2, k2, *_scales(scale, scale2), causal, np.asarray(rows))",
+                                                 "r = _head_rows(q1, k1, q2, k2, scale, scale, causal, np.asarray(rows))"),
     "sampled dk missing scale": ("dk += sg * (ds.T @ qg[rows])\n    return dk\n\n\ndef loss", "dk += (ds.T @ qg[rows])\n    return dk\n\n\ndef loss"),
 }
 

@@ -289,6 +289,21 @@ def pin_sampled_backward(o):
                                            dk[[13, 25]], rtol=1e-12, atol=1e-15)
 
 
+def pin_sampled_forward(o):
+    """forward_rows on scattered, unsorted rows equals those rows of the
+    full forward (which the closed forms, brute force and library pins fix),
+    for causal NQ < NK (bottom-right mask), non-causal and per-side scales."""
+    rng = np.random.default_rng(17)
+    q1, k1, q2, k2 = _head(rng, 23, 37, 5, 3)
+    rows = [22, 0, 9, 3, 17, 9]  # unsorted, one repeated, first and last row
+    for causal in (False, True):
+        for s2 in (None, 0.45):
+            kl, a, b = o.forward_head(q1, k1, q2, k2, 0.8, causal, row_block=4, scale2=s2)
+            skl, sa, sb = o.forward_rows(q1, k1, q2, k2, 0.8, causal, rows, scale2=s2)
+            for got, want in ((skl, kl), (sa, a), (sb, b)):
+                np.testing.assert_allclose(got, want[rows], rtol=1e-13, atol=1e-15)
+
+
 def pin_underflow_is_finite(o):
     """Unit scale and peaky teacher rows: many probabilities fall below the
     fp32 normal range, yet every oracle output stays finite."""

@@ -38,6 +38,18 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls():
         assert_fwd_close(*(np_(t) for t in got), *(np_(t) for t in want), f"{w.name} noalloc")
 
 
+def test_noalloc_larger_call_then_smaller_call():
+    """The bigger layout first: partials it leaves past the smaller call's
+    extent, or at the smaller call's offsets, must not leak into the latter."""
+    for w, splits in reversed(CASES):
+        host, dev = inputs(w)
+        got = skl.streamkl_fwd_splitk_noalloc(*dev, w.scale, w.causal, splits)
+        want = skl.streamkl_fwd_splitk(*dev, w.scale, w.causal, splits)
+        torch.cuda.synchronize()
+        assert skl.streamkl_get_device_status() == 0
+        assert_fwd_close(*(np_(t) for t in got), *(np_(t) for t in want), f"{w.name} noalloc after larger")
+
+
 def test_noalloc_repeated_call_is_stable():
     w, splits = CASES[0]
     host, dev = inputs(w)
