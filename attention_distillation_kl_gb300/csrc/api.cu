@@ -75,6 +75,27 @@ bool make_map_dq(CUtensorMap* m, void* ptr, long long BH, long long NQ, int dg) 
   return r == CUDA_SUCCESS;
 }
 
+// The fused backward's dQ target: boxes of 32 fp32 x 32 rows with the
+// 128-byte swizzle (one full 128-byte line per row and box: fewer, larger
+// reduce operations than 64-byte pieces), or the 16-wide map for dg = 16.
+bool make_map_dq_wide(CUtensorMap* m, void* ptr, long long BH, long long NQ, int dg, int* box_cols) {
+  if (dg < 32) {
+    *box_cols = 16;
+    return make_map_dq(m, ptr, BH, NQ, dg);
+  }
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[3] = {cuuint64_t(dg), cuuint64_t(NQ), cuuint64_t(BH)};
+  cuuint64_t strides[2] = {cuuint64_t(dg) * 4, cuuint64_t(NQ) * dg * 4};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  *box_cols = 32;
+  return r == CUDA_SUCCESS;
+}
+
 bool scale_ok(float s) { return std::isfinite(s) && s > 0.f && s <= 1.0e4f; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -287,7 +308,7 @@ int streamkl_bwd_gqa(const void* q1, const void* k1, const void* q2, const void*
   const int t1 = tile_dim(d1), t2 = tile_dim(d2);
   if (!deterministic) {
     const size_t dq_bytes = size_t(B) * H * NQ * dg * 4;
-    if (!make_map_dq(&m.dq, dq, (long long)B * H, NQ, dg)) return STREAMKL_CUDA_ERROR;
+    if (!make_map_dq_wide(&m.dqw, dq, (long long)B * H, NQ, dg, &a.dq_box)) return STREAMKL_CUDA_ERROR;
     if (cudaMemsetAsync(dq, 0, dq_bytes, cs) != cudaSuccess) return STREAMKL_CUDA_ERROR;
     // a shared key head's dK is accumulated by the CTAs of its query heads
     if (gg > 1 && cudaMemsetAsync(dk, 0, dk_bytes, cs) != cudaSuccess) return STREAMKL_CUDA_ERROR;

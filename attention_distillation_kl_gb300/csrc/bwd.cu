@@ -28,11 +28,14 @@
 //              half the work).  dS goes to shared memory as bf16 rows in the
 //              128-byte-swizzled layout both products read: K-major A for
 //              dQ, M-major A (dS^T) for dK
-//   warps 8-11 dQ tile: TMEM -> registers (scaled) -> 32 x 16 fp32 boxes in
-//              swizzled shared memory (four per warp, round robin) -> TMA
-//              bulk tensor reduce-add into global dQ (rows past NQ are
-//              clipped by the tensor map); finally dK (stored, or added when
-//              a key head is shared by several query heads: put_dk4)
+//   warps 8-11 dQ tile: TMEM -> registers (96 columns, one box staged, the
+//              last 32 columns, then the accumulator is free; the register
+//              budget of 512 threads holds no whole 128-column row)
+//              -> 32 x 32 fp32 boxes in 128-byte-swizzled
+//              shared memory (two per warp, round robin) -> TMA bulk tensor
+//              reduce-add into global dQ (rows past NQ are clipped by the
+//              tensor map); finally dK (stored, or added when a key head is
+//              shared by several query heads: put_dk4)
 // TMEM: S1 [0,128), S2 [128,256), dK [256, 256+dg), dQ [384, 384+dg).
 //
 // dQ-only kernel (deterministic two-pass mode): one CTA per query tile walks
@@ -46,7 +49,8 @@
 namespace skl {
 
 
-constexpr int kDqBoxes = 4;  // dQ staging boxes per epilogue warp
+constexpr int kDqBoxes = 2;          // dQ staging boxes per epilogue warp
+constexpr uint32_t kDqBoxBytes = 4096;  // [32 rows][32 fp32], 128-byte swizzle
 
 template <int D1, int D2, int MODE>
 struct BwdLayout {
@@ -61,8 +65,8 @@ struct BwdLayout {
   static constexpr uint32_t kK1 = kTile * D1 * 2, kK2 = kTile * D2 * 2;
   static constexpr uint32_t kQo = kTile * DO * 2, kQg = kTile * DG * 2;
   static constexpr uint32_t oDS = 0, oK1 = kDS, oK2 = oK1 + kK1, oQo = oK2 + kK2, oQg = oQo + kQo;
-  static constexpr uint32_t oStage = oQg + 2 * kQg;  // dQ staging: 4 warps x kDqBoxes x [32 rows][64 B]
-  static constexpr uint32_t oBar = oStage + 4 * kDqBoxes * 2048;
+  static constexpr uint32_t oStage = oQg + 2 * kQg;  // dQ staging: 4 warps x kDqBoxes x kDqBoxBytes
+  static constexpr uint32_t oBar = oStage + 4 * kDqBoxes * kDqBoxBytes;
   enum {
     B_KFULL, B_QOFULL, B_QOEMPTY, B_QGFULL0, B_QGFULL1, B_QGEMPTY0, B_QGEMPTY1, B_SFULL, B_SFREE,
     B_DSFULL, B_DSEMPTY, B_DQFULL, B_DQEMPTY, B_DKFULL, B_DONE, kNumBars
@@ -229,26 +233,28 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
       if (n > 0 && t == n && !*abort_flag) mma_commit(1u, bar(L::B_DKFULL));
       mma_commit(1u, bar(L::B_DONE));  // the TMEM owner drains it before releasing TMEM
     }
-  } else if (L::kSplitIssue && warp == 15) {
-    // ---------------------------------------------------------------- dQ issuer (mode P1)
-    if (lane == 0) {
-      constexpr uint32_t id_dq = idesc_bf16(128, DG, 0, 1);  // A = dS K-major, B = K_g N-major
-      const uint64_t dsk = sdesc_sw128(sb + L::oDS, 16, 1024);  // dS, K-major
-      const uint64_t kgn = TG::desc_n(sb + (kP2 ? L::oK2 : L::oK1));
-      if (a.write_dq && n > 0 && mbar_wait_polled(bar(L::B_KFULL), 0, ctl)) {
-        for (int t = 0; t < n; ++t) {
-          if (!mbar_wait_polled(bar(L::B_DSFULL), t & 1, ctl)) break;
-          if (!mbar_wait_polled(bar(L::B_DQEMPTY), (t & 1) ^ 1, ctl)) break;
-          tc_fence_after();
+  } else if (warp == 15) {  // exists in mode P1 only
+    if constexpr (L::kSplitIssue) {
+      // ---------------------------------------------------------------- dQ issuer (mode P1)
+      if (lane == 0) {
+        constexpr uint32_t id_dq = idesc_bf16(128, DG, 0, 1);  // A = dS K-major, B = K_g N-major
+        const uint64_t dsk = sdesc_sw128(sb + L::oDS, 16, 1024);  // dS, K-major
+        const uint64_t kgn = TG::desc_n(sb + (kP2 ? L::oK2 : L::oK1));
+        if (a.write_dq && n > 0 && mbar_wait_polled(bar(L::B_KFULL), 0, ctl)) {
+          for (int t = 0; t < n; ++t) {
+            if (!mbar_wait_polled(bar(L::B_DSFULL), t & 1, ctl)) break;
+            if (!mbar_wait_polled(bar(L::B_DQEMPTY), (t & 1) ^ 1, ctl)) break;
+            tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_bf16_ss(1u, t_dq, sdesc_add(dsk, (kk >> 2) * (kTile * 128) + (kk & 3) * 32),
-                        sdesc_add(kgn, TG::off_n(kk)), id_dq, kk > 0 ? 1u : 0u);
-          mma_commit(1u, bar(L::B_DSEMPTY));
-          mma_commit(1u, bar(L::B_DQFULL));
+            for (int kk = 0; kk < kTile / 16; ++kk)
+              mma_bf16_ss(1u, t_dq, sdesc_add(dsk, (kk >> 2) * (kTile * 128) + (kk & 3) * 32),
+                          sdesc_add(kgn, TG::off_n(kk)), id_dq, kk > 0 ? 1u : 0u);
+            mma_commit(1u, bar(L::B_DSEMPTY));
+            mma_commit(1u, bar(L::B_DQFULL));
+          }
         }
+        mma_commit(1u, bar(L::B_DONE));  // the TMEM owner drains it before releasing TMEM
       }
-      mma_commit(1u, bar(L::B_DONE));  // the TMEM owner drains it before releasing TMEM
     }
   } else if (warp < 8) {
     // ---------------------------------------------------------------- dS (thread = query row)
@@ -313,53 +319,72 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
     const int row = w4 * 32 + lane;
     const uint32_t lane_off = uint32_t(w4 * 32) << 16;
     if (a.write_dq) {
-      // kDqBoxes 2 KB staging boxes per warp ([32 rows][16 fp32], 64-byte
-      // swizzle: 16-byte chunk c of row r at chunk c ^ ((r / 2) % 4)), used
-      // round robin so up to kDqBoxes bulk reduce-adds are in flight.  The
-      // tile is read from TMEM kRead columns at a time; the last read
-      // releases the dQ accumulator before its boxes are staged, so the
-      // next dQ product does not wait for the reduce-adds.
-      constexpr int kHalves = DG >= 64 ? 2 : 1, kRead = 32 * kHalves;
-      const uint32_t stage = sb + L::oStage + w4 * (kDqBoxes * 2048);
-      const uint32_t swz = (lane >> 1) & 3;
+      // This thread's dQ row (DG fp32) is read from TMEM and the accumulator
+      // released before most of it is staged, so the next dQ product rarely
+      // waits for the reduce-adds.  The row leaves in boxes of [32 rows][32 fp32]
+      // (128-byte swizzle: 16-byte chunk c of row r at chunk c ^ (r % 8); one
+      // full 128-byte line per row) through kDqBoxes staging boxes per warp,
+      // each a bulk tensor reduce-add into the fp32 dQ.  For dg = 16 the map
+      // has boxes of [32 rows][16 fp32] with the 64-byte swizzle instead
+      // (chunk c of row r at c ^ ((r / 2) % 4)).
+      constexpr int kChunks = DG / 32;
+      const bool wide = a.dq_box == 32;
+      const uint32_t stage = sb + L::oStage + w4 * (kDqBoxes * kDqBoxBytes);
       int nred = 0;
       if (lane == 0) tma_prefetch_desc(&tdq);
       for (int i = 0; i < n; ++i) {
         if (!mbar_wait_warp(bar(L::B_DQFULL), i & 1, ctl)) break;
         tc_fence_after();
         const int r0 = (qt_lo + i) * kTile + w4 * 32;  // first query row of this warp
+        uint32_t v[kChunks][32];
+        // one box of the dQ tile: row `lane` of this warp's 32 rows, columns [32 h, 32 h + 32)
+        auto put_box = [&](int h) {
+          // columns past the head dim (zero-filled operand), or rows all past
+          // NQ: nothing to add, and no box is touched (the box count must
+          // match the committed reduce groups, or a box still being read by
+          // an earlier reduce could be overwritten)
+          if (h * 32 >= a.dg || r0 >= a.NQ) return;
+          const uint32_t box = stage + (nred % kDqBoxes) * kDqBoxBytes;
+          // the box used kDqBoxes reduces ago has been read
+          if (lane == 0) bulk_wait_read_le<kDqBoxes - 1>();
+          __syncwarp();
+          if (wide) {
 #pragma unroll
-        for (int cp = 0; cp < DG / kRead; ++cp) {
-          uint32_t v[kHalves][32];
+            for (int c = 0; c < 8; ++c)
+              st_shared_v4(box + lane * 128 + ((c ^ (lane & 7)) << 4), v[h][4 * c], v[h][4 * c + 1],
+                           v[h][4 * c + 2], v[h][4 * c + 3]);
+          } else {
+            const uint32_t swz = (lane >> 1) & 3;
 #pragma unroll
-          for (int x = 0; x < kHalves; ++x) tmem_ld32(t_dq + lane_off + cp * kRead + 32 * x, v[x]);
-          if (cp == DG / kRead - 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(L::B_DQEMPTY));
+            for (int c = 0; c < 4; ++c)
+              st_shared_v4(box + lane * 64 + ((c ^ swz) << 4), v[h][4 * c], v[h][4 * c + 1], v[h][4 * c + 2],
+                           v[h][4 * c + 3]);
           }
-#pragma unroll
-          for (int h = 0; h < 2 * kHalves; ++h) {
-            if (cp * kRead + h * 16 >= a.dg) break;  // columns past the head dim (zero-filled operand)
-            const uint32_t box = stage + (nred % kDqBoxes) * 2048;
-            // the box used kDqBoxes reduces ago has been read
-            if (lane == 0) bulk_wait_read_le<kDqBoxes - 1>();
-            __syncwarp();
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              const int e = (h & 1) * 16 + 4 * c;
-              st_shared_v4(box + lane * 64 + ((c ^ swz) << 4), v[h >> 1][e], v[h >> 1][e + 1], v[h >> 1][e + 2],
-                           v[h >> 1][e + 3]);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0 && r0 < a.NQ) {  // a box starting past NQ has nothing to add
-              tma_reduce_add_3d(&tdq, box, cp * kRead + h * 16, r0, bh);
-              bulk_commit();
-            }
-            ++nred;
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_reduce_add_3d(&tdq, box, h * 32, r0, bh);
+            bulk_commit();
           }
+          ++nred;
+        };
+        // read the tile; at DG = 128 the first box is staged before the last
+        // 32 columns are read, so at most 96 columns are live at once
+        if constexpr (kChunks == 4) {
+          tmem_ld2x32(t_dq + lane_off, t_dq + lane_off + 32, v[0], v[1]);
+          tmem_ld32(t_dq + lane_off + 64, v[2]);
+          put_box(0);
+          tmem_ld32(t_dq + lane_off + 96, v[3]);
+        } else if constexpr (kChunks == 2) {
+          tmem_ld2x32(t_dq + lane_off, t_dq + lane_off + 32, v[0], v[1]);
+        } else {
+          tmem_ld32(t_dq + lane_off, v[0]);
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(L::B_DQEMPTY));
+#pragma unroll
+        for (int h = kChunks == 4 ? 1 : 0; h < kChunks; ++h) put_box(h);
       }
       if (lane == 0) bulk_wait_all();  // every reduce has landed before the CTA exits
     }
@@ -624,7 +649,7 @@ static int launch_fused_t(const TMaps& m, const BwdArgs& a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   const int gg = MODE == STREAMKL_GRAD_P2 ? a.g2 : a.g1;
   dim3 grid((a.NK + kTile - 1) / kTile, a.hsel < 0 ? a.BH : a.BH / gg);
-  kern<<<grid, L::kThreads, L::kAlloc, st>>>(m.q1, m.k1, m.q2, m.k2, m.dq, a);
+  kern<<<grid, L::kThreads, L::kAlloc, st>>>(m.q1, m.k1, m.q2, m.k2, m.dqw, a);
   return cudaGetLastError();
 }
 

@@ -304,7 +304,10 @@ __global__ void __launch_bounds__(kBothThreads, 1)
         }
 #pragma unroll
         for (int h = 0; h < 2 * kHalves; ++h) {
-          if (h * 16 >= a.dg) break;  // columns past the head dim (zero-filled operand)
+          // columns past the head dim (zero-filled operand), or rows all past
+          // NQ: no box is touched, so the box count matches the committed
+          // reduce groups and no box still being read is overwritten
+          if (h * 16 >= a.dg || r0 >= a.NQ) break;
           const uint32_t box = stage + (nred % kBothBoxes) * 2048;
           if (lane == 0) bulk_wait_read_le<kBothBoxes - 1>();  // the box used kBothBoxes reduces ago was read
           __syncwarp();
@@ -316,7 +319,7 @@ __global__ void __launch_bounds__(kBothThreads, 1)
           }
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0 && r0 < a.NQ) {  // a box starting past NQ has nothing to add
+          if (lane == 0) {
             tma_reduce_add_3d(side == 0 ? &tdq1 : &tdq2, box, h * 16, r0, bh);
             bulk_commit();
           }

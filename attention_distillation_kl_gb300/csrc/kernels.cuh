@@ -12,8 +12,10 @@ constexpr int kTile = 128;  // query and key tile: 128 rows = 128 TMEM lanes
 
 struct TMaps {
   CUtensorMap q1, k1, q2, k2;  // [BH][N][d] bf16, boxes of 64 (or 32) x 128, 128- (or 64-) byte swizzle
-  CUtensorMap dq;              // [BH][NQ][dg] fp32, boxes of 16 x 32, 64-byte swizzle (fused backward)
+  CUtensorMap dq;              // [BH][NQ][dg] fp32, boxes of 16 x 32, 64-byte swizzle (both-sides backward)
   CUtensorMap dq2;             // the second side's dQ (both-sides backward)
+  CUtensorMap dqw;             // [BH][NQ][dg] fp32 for the fused backward: boxes of 32 x 32 with the
+                               // 128-byte swizzle when dg >= 32, else as dq (BwdArgs::dq_box says which)
 };
 
 struct FwdArgs {
@@ -47,6 +49,7 @@ struct BwdArgs {
   int write_dq;  // 0: skip the dQ product (deterministic two-pass uses its own dQ kernel)
   float* dq2;    // both-sides backward: dQ2, dK2 (dq, dk then hold dQ1, dK1)
   float* dk2;
+  int dq_box;    // fused backward: width of the dQ reduce-add boxes, 32 (dqw, 128-byte swizzle) or 16
 };
 
 // Each returns a cudaError_t value (cudaSuccess = 0).  d1, d2 and d are the

@@ -367,6 +367,20 @@ __device__ __forceinline__ void tmem_ld32(uint32_t ta, uint32_t (&a)[32]) {
       : "memory");
 }
 
+// Moves a whole warpgroup's per-thread register budget down or up (the
+// registers one warpgroup gives back are what another can take; an increase
+// waits until enough are free, so every decrease must run first or
+// concurrently, and the sum over warpgroups must stay within the block's
+// launch budget).
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
