@@ -15,7 +15,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libstreamkl.so")
-SOURCES = ["api.cu", "fwd.cu", "bwd.cu", "bwd_both.cu", "static_ws.cu"]
+SOURCES = ["api.cu", "fwd.cu", "fwd_wide.cu", "bwd.cu", "bwd_wide_p0.cu", "bwd_wide_p1.cu", "bwd_both.cu",
+           "static_ws.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -36,10 +36,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// The kernels' tile width for head dim d (a multiple of 16 up to 128): 32,
-// 64 or 128.  Columns past d in a tile are zero-filled by the TMA, which
+// The kernels' tile width for head dim d (a multiple of 16 up to 256): 32,
+// 64, 128, 192 or 256.  Columns past d in a tile are zero-filled by the TMA, which
 // leaves every dot product unchanged.
-int tile_dim(int d) { return d <= 32 ? 32 : (d <= 64 ? 64 : 128); }
+int tile_dim(int d) { return d <= 32 ? 32 : (d <= 64 ? 64 : (d <= 128 ? 128 : (d <= 192 ? 192 : 256))); }
 
 // [BH][N][d] bf16 viewed as a 3-D tensor; boxes of 64 elements x 128 rows x 1
 // with the 128-byte swizzle, or for tile width 32 one box of 32 elements x
@@ -100,7 +100,7 @@ bool scale_ok(float s) { return std::isfinite(s) && s > 0.f && s <= 1.0e4f; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-bool head_dim_ok(int d) { return d >= 16 && d <= 128 && d % 16 == 0; }
+bool head_dim_ok(int d) { return d >= 16 && d <= 256 && d % 16 == 0; }
 
 // Shared validation of the problem description.  Returns STREAMKL_OK, or the
 // status to report.  Sets *empty when there is no row to compute.
@@ -306,6 +306,18 @@ int streamkl_bwd_gqa(const void* q1, const void* k1, const void* q2, const void*
   skl::BwdArgs a{B * H, NQ, NK, causal, mode, dg, H / HK1, H / HK2, -1, scale1, scale2, kl, lse1, lse2, dkl, dq,
                  dk, st, 1};
   const int t1 = tile_dim(d1), t2 = tile_dim(d2);
+  if (t1 > 128 || t2 > 128) {
+    // a head above 128: dK by key tiles (the launches of a key-head group in
+    // order, the first storing), then dQ by query tiles; no atomics, so both
+    // values of `deterministic` take this path
+    a.write_dq = 0;
+    for (int j = 0; j < gg; ++j) {
+      a.hsel = gg > 1 ? j : -1;
+      if (skl::launch_bwd_wide_pass0(m, t1, t2, a, cs) != 0) return STREAMKL_CUDA_ERROR;
+    }
+    a.hsel = -1;
+    return as_status(skl::launch_bwd_wide_pass1(m, t1, t2, a, cs));
+  }
   if (!deterministic) {
     const size_t dq_bytes = size_t(B) * H * NQ * dg * 4;
     if (!make_map_dq_wide(&m.dqw, dq, (long long)B * H, NQ, dg, &a.dq_box)) return STREAMKL_CUDA_ERROR;

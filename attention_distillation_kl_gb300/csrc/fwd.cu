@@ -1,329 +1,9 @@
-// Forward kernel: one CTA streams all visible key tiles past one 128-row query
-// tile and keeps the coupled online statistics of the StreamKL article
-// ("Online formula", "Forward") in registers:
-//   m1, m2   running maxima of the raw logits q.k
-//   l1, l2   running sums of 2^(c (x - m))        (c = s log2 e of that side)
-//   acc      running sum of 2^(c1 (x1 - m1)) (x1 - rho x2),  rho = s2 / s1
-// When m1 moves, l1 and acc are multiplied by 2^(c1 (m1_old - m1_new)) -- a
-// vector rescale per row, never a B_Q x d matrix.  At the end
-//   LSE = s m + ln l,  KL = s1 acc / l1 + LSE2 - LSE1
-// (s1 (x1 - rho x2) = S1 - S2, so s1 acc / l1 is the P1-weighted mean of
-// S1 - S2).
-//
-// GB300 mapping (10 warps, 1 CTA per SM):
-//   warp 8      TMA producer: Q1/Q2 once, then K1_j/K2_j (key head h / G) into a ring
-//   warp 9      TMEM owner and MMA issuer: S1 = Q1 K1_j^T and S2 = Q2 K2_j^T
-//               (tcgen05, M = N = 128, bf16 -> fp32) into one of two TMEM
-//               buffers of 256 columns, so tile j+1 is multiplied while the
-//               statistics of tile j are reduced.  The whole warp runs the
-//               loop and one elected lane issues (see elect_one).
-//   warps 0-7   statistics: thread = query row (TMEM lane); warps 0-3 take
-//               key columns 0-63 of every tile, warps 4-7 columns 64-127, and
-//               the two partial states are merged at the end with the same
-//               algebra as the key-split reduce.  (Four warpgroups of 32
-//               columns each were timed slower: the statistics loop is close
-//               to the one-instruction-per-cycle issue limit, and more warps
-//               only add per-tile overhead.)
-// With num_splits > 1 (article section "GPU kernel engineering", split-K) a
-// CTA covers only its share of the key tiles and writes (m1, l1, acc, m2, l2)
-// instead of the final values; splitk_reduce_kernel merges them.
-#include "kernels.cuh"
-#include "ptx.cuh"
-#include "tiles.cuh"
+// Forward launchers for tile widths up to 128, the key-split merge, the ex2
+// throughput probe and the bounded-wait self-test.  The forward kernel
+// itself is in fwd_kernel.cuh.
+#include "fwd_kernel.cuh"
 
 namespace skl {
-
-// Statistics warpgroups: each takes kTile / kStatWGs key columns of every
-// tile (32-column chunks), so every SM sub-partition runs kStatWGs warps
-// of row statistics; then one producer warp and one MMA warp.
-constexpr int kStatWGs = 2;
-constexpr int kStatWarps = 4 * kStatWGs;
-constexpr int kColsPerWG = kTile / kStatWGs;
-constexpr int kProdWarp = kStatWarps, kMmaWarp = kStatWarps + 1;
-constexpr int kFwdThreads = 32 * (kStatWarps + 2);
-static_assert(kColsPerWG % 32 == 0, "whole 32-column chunks per warpgroup");
-
-template <int D1, int D2>
-struct FwdLayout {
-  static constexpr uint32_t kQ1 = kTile * D1 * 2, kQ2 = kTile * D2 * 2;
-  static constexpr uint32_t kK1 = kTile * D1 * 2, kK2 = kTile * D2 * 2;
-  static constexpr uint32_t kStage = kK1 + kK2;
-  static constexpr int kStagesFit = int((210u * 1024u - kQ1 - kQ2) / kStage);
-  static constexpr int kStages = kStagesFit > 4 ? 4 : kStagesFit;
-  static constexpr uint32_t oQ1 = 0, oQ2 = kQ1, oK = kQ1 + kQ2;
-  static constexpr uint32_t oBar = oK + kStages * kStage;
-  // q_full, k_full[S], k_empty[S], s_full[2], s_empty[2], mma_done
-  static constexpr int kNumBars = 1 + 2 * kStages + 4 + 1;
-  static constexpr uint32_t oMisc = oBar + kNumBars * 8;  // tmem base, abort flag
-  static constexpr uint32_t oMerge = (oMisc + 8 + 15) / 16 * 16;
-  static constexpr uint32_t kBytes = oMerge + (kStatWGs - 1) * kTile * 5 * 4;
-  static constexpr uint32_t kAlloc = kBytes + 1024;
-  static_assert(kStages >= 2, "shared memory ring needs two stages");
-  static_assert(kAlloc <= 232448, "over the 227 KB shared memory limit");
-};
-
-// Per-row running state of one thread.
-struct RowStats {
-  float m1, m2, l1, l2, acc;
-};
-
-// Folds 32 consecutive key columns into the running state.  Columns k with
-// k > lim_rel are masked (causal or past NK): they neither move the maxima
-// nor add to the sums.  Pairs of columns go through the packed FP32 pipe.
-// c1, c2: s log2 e of each side; nrho = -s2 / s1 (x1 - rho x2 is one fma,
-// exactly x1 - x2 when the scales are equal).
-template <bool kMask>
-__device__ __forceinline__ void fold_chunk(RowStats& st, const uint32_t (&x1u)[32],
-                                           const uint32_t (&x2u)[32], float c1, float c2, float nrho,
-                                           int lim_rel) {
-  float t1 = st.m1, t2 = st.m2;
-#pragma unroll
-  for (int k = 0; k < 32; k += 2) {
-    const bool oa = !kMask || k <= lim_rel, ob = !kMask || k + 1 <= lim_rel;
-    t1 = max3(t1, oa ? __uint_as_float(x1u[k]) : kNegBig, ob ? __uint_as_float(x1u[k + 1]) : kNegBig);
-    t2 = max3(t2, oa ? __uint_as_float(x2u[k]) : kNegBig, ob ? __uint_as_float(x2u[k + 1]) : kNegBig);
-  }
-  const float a1 = ex2((st.m1 - t1) * c1);
-  const float a2 = ex2((st.m2 - t2) * c2);
-  st.m1 = t1;
-  st.m2 = t2;
-  const uint64_t C1 = f2(c1, c1), C2 = f2(c2, c2), NR = f2(nrho, nrho);
-  const uint64_t NB1 = f2(-t1 * c1, -t1 * c1), NB2 = f2(-t2 * c2, -t2 * c2);
-  uint64_t L1 = f2(0.f, 0.f), L2 = L1, ACC = L1;
-#pragma unroll
-  for (int k = 0; k < 32; k += 2) {
-    const uint64_t X1 = f2(__uint_as_float(x1u[k]), __uint_as_float(x1u[k + 1]));
-    const uint64_t X2 = f2(__uint_as_float(x2u[k]), __uint_as_float(x2u[k + 1]));
-    float e1a, e1b, e2a, e2b;
-    f2_split(f2_fma(X1, C1, NB1), e1a, e1b);
-    f2_split(f2_fma(X2, C2, NB2), e2a, e2b);
-    float p1a = ex2(e1a), p1b = ex2(e1b), p2a = ex2(e2a), p2b = ex2(e2b);
-    if (kMask) {
-      if (k > lim_rel) { p1a = 0.f; p2a = 0.f; }
-      if (k + 1 > lim_rel) { p1b = 0.f; p2b = 0.f; }
-    }
-    const uint64_t P1 = f2(p1a, p1b);
-    L1 = f2_add(L1, P1);
-    L2 = f2_add(L2, f2(p2a, p2b));
-    ACC = f2_fma(P1, f2_fma(X2, NR, X1), ACC);
-  }
-  float l1a, l1b, l2a, l2b, aca, acb;
-  f2_split(L1, l1a, l1b);
-  f2_split(L2, l2a, l2b);
-  f2_split(ACC, aca, acb);
-  st.l1 = fmaf(st.l1, a1, l1a + l1b);
-  st.acc = fmaf(st.acc, a1, aca + acb);
-  st.l2 = fmaf(st.l2, a2, l2a + l2b);
-}
-
-template <int D1, int D2>
-__global__ void __launch_bounds__(kFwdThreads, 1)
-    fwd_kernel(const __grid_constant__ CUtensorMap tq1, const __grid_constant__ CUtensorMap tk1,
-               const __grid_constant__ CUtensorMap tq2, const __grid_constant__ CUtensorMap tk2,
-               const FwdArgs a) {
-  using L = FwdLayout<D1, D2>;
-  using T1 = OpTile<D1>;
-  using T2 = OpTile<D2>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
-  const uint32_t sb = smem_u32(smem);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  const int nqt = (a.NQ + kTile - 1) / kTile;
-  const int qt = a.causal ? (nqt - 1 - int(blockIdx.x)) : int(blockIdx.x);  // longest rows first
-  const int bh = blockIdx.y, split = blockIdx.z;
-  const int q0 = qt * kTile;
-  const int off = a.NK - a.NQ;
-  const int kend = a.causal ? min(q0 + kTile, a.NQ) + off : a.NK;
-  const int nkt_all = (kend + kTile - 1) / kTile;
-  const int kt_lo = int((long long)split * nkt_all / a.num_splits);
-  const int kt_hi = int((long long)(split + 1) * nkt_all / a.num_splits);
-  const int nkt = kt_hi - kt_lo;
-
-  const uint32_t bar0 = sb + L::oBar;
-  const uint32_t bar_q = bar0;
-  auto bar_kfull = [&](int s) { return bar0 + 8u * (1 + s); };
-  auto bar_kempty = [&](int s) { return bar0 + 8u * (1 + L::kStages + s); };
-  auto bar_sfull = [&](int b) { return bar0 + 8u * (1 + 2 * L::kStages + b); };
-  auto bar_sempty = [&](int b) { return bar0 + 8u * (3 + 2 * L::kStages + b); };
-  const uint32_t bar_done = bar0 + 8u * (5 + 2 * L::kStages);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::oMisc);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::oMisc + 4);
-  const Ctl ctl{abort_flag, a.status};
-
-  if (threadIdx.x == 0) {
-    mbar_init(bar_q, 1);
-    for (int s = 0; s < L::kStages; ++s) {
-      mbar_init(bar_kfull(s), 1);
-      mbar_init(bar_kempty(s), 1);
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(bar_sfull(b), 1);
-      mbar_init(bar_sempty(b), kStatWarps);
-    }
-    mbar_init(bar_done, 1);
-    *abort_flag = 0;
-    fence_barrier_init();
-  }
-  if (warp == kMmaWarp) {
-    tmem_alloc(smem_u32(tmem_slot), 512);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-
-  if (warp == kProdWarp) {
-    // ---------------------------------------------------------------- TMA producer
-    if (lane == 0 && nkt > 0) {
-      tma_prefetch_desc(&tq1);
-      tma_prefetch_desc(&tk1);
-      tma_prefetch_desc(&tq2);
-      tma_prefetch_desc(&tk2);
-      mbar_arrive_expect_tx(bar_q, L::kQ1 + L::kQ2);
-      T1::load(sb + L::oQ1, &tq1, bar_q, q0, bh);
-      T2::load(sb + L::oQ2, &tq2, bar_q, q0, bh);
-      int issued = 0;
-      for (int j = 0; j < nkt; ++j) {
-        const int s = j % L::kStages;
-        const uint32_t ph = (j / L::kStages) & 1;
-        if (!mbar_wait(bar_kempty(s), ph ^ 1, ctl)) break;
-        mbar_arrive_expect_tx(bar_kfull(s), L::kStage);
-        const int k0 = (kt_lo + j) * kTile;
-        const uint32_t st = sb + L::oK + s * L::kStage;
-        T1::load(st, &tk1, bar_kfull(s), k0, bh / a.g1);
-        T2::load(st + L::kK1, &tk2, bar_kfull(s), k0, bh / a.g2);
-        issued = j + 1;
-      }
-      if (*abort_flag) {  // let the copies already started land before the CTA exits
-        mbar_drain(bar_q, 0, 200000000ull);
-        for (int j = issued > L::kStages ? issued - L::kStages : 0; j < issued; ++j)
-          mbar_drain(bar_kfull(j % L::kStages), (j / L::kStages) & 1, 200000000ull);
-      }
-    }
-  } else if (warp == kMmaWarp) {
-    // ---------------------------------------------------------------- MMA issuer
-    // (the whole warp runs the loop; the elected lane issues)
-    const uint32_t leader = elect_one();
-    constexpr uint32_t idesc = idesc_bf16(128, 128, 0, 0);
-    if (nkt > 0 && mbar_wait_warp(bar_q, 0, ctl)) {
-      for (int j = 0; j < nkt; ++j) {
-        const int s = j % L::kStages;
-        const uint32_t ph = (j / L::kStages) & 1;
-        const int b = j & 1;
-        const uint32_t bph = (j >> 1) & 1;
-        if (!mbar_wait_warp(bar_kfull(s), ph, ctl)) break;
-        if (!mbar_wait_warp(bar_sempty(b), bph ^ 1, ctl)) break;
-        tc_fence_after();
-        const uint32_t d1 = tmem + b * 256, d2 = d1 + 128;
-        const uint32_t k1s = sb + L::oK + s * L::kStage, k2s = k1s + L::kK1;
-#pragma unroll
-        for (int kk = 0; kk < D1 / 16; ++kk) {
-          const uint32_t o = T1::off_k(kk);
-          mma_bf16_ss(leader, d1, T1::desc_k(sb + L::oQ1 + o), T1::desc_k(k1s + o), idesc, kk > 0);
-        }
-#pragma unroll
-        for (int kk = 0; kk < D2 / 16; ++kk) {
-          const uint32_t o = T2::off_k(kk);
-          mma_bf16_ss(leader, d2, T2::desc_k(sb + L::oQ2 + o), T2::desc_k(k2s + o), idesc, kk > 0);
-        }
-        mma_commit(leader, bar_kempty(s));
-        mma_commit(leader, bar_sfull(b));
-      }
-    }
-    // every MMA this warp issued has finished before TMEM is released
-    mma_commit(leader, bar_done);
-    mbar_drain(bar_done, 0, 1000000000ull);
-  } else {
-    // ---------------------------------------------------------------- statistics
-    const int wg = warp >> 2;
-    const int row = (warp & 3) * 32 + lane;
-    const int grow = q0 + row;
-    const float c1 = a.scale1 * kLog2e, c2 = a.scale2 * kLog2e, nrho = -a.scale2 / a.scale1;
-    const int lim = a.causal ? min(grow + off, a.NK - 1) : a.NK - 1;  // last visible key
-    const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
-    RowStats st{kNegBig, kNegBig, 0.f, 0.f, 0.f};
-    for (int j = 0; j < nkt; ++j) {
-      const int b = j & 1;
-      const uint32_t bph = (j >> 1) & 1;
-      if (!mbar_wait_warp(bar_sfull(b), bph, ctl)) break;
-      tc_fence_after();
-      const int k0 = (kt_lo + j) * kTile;
-      const bool need_mask = (k0 + kTile > a.NK) || (a.causal && k0 + kTile - 1 > q0 + off);
-#pragma unroll
-      for (int ch = 0; ch < kColsPerWG / 32; ++ch) {
-        const int col = wg * kColsPerWG + ch * 32;
-        uint32_t x1[32], x2[32];
-        const uint32_t t = tmem + lane_off + uint32_t(b * 256 + col);
-        tmem_ld2x32(t, t + 128, x1, x2);
-        if (ch == kColsPerWG / 32 - 1) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar_sempty(b));
-        }
-        if (need_mask)
-          fold_chunk<true>(st, x1, x2, c1, c2, nrho, lim - (k0 + col));
-        else
-          fold_chunk<false>(st, x1, x2, c1, c2, nrho, 0);
-      }
-    }
-    // merge the column shares of every row (warpgroups 1.. -> warpgroup 0)
-    // with the same algebra as the key-split reduce
-    float* mg = reinterpret_cast<float*>(smem + L::oMerge);
-    if (wg > 0) {
-      float* o = mg + (wg - 1) * kTile * 5 + row * 5;
-      o[0] = st.m1;
-      o[1] = st.l1;
-      o[2] = st.acc;
-      o[3] = st.m2;
-      o[4] = st.l2;
-    }
-    named_bar_sync(1, 32 * kStatWarps);
-    if (wg == 0 && !*abort_flag && grow < a.NQ) {
-      float M1 = st.m1, M2 = st.m2;
-#pragma unroll
-      for (int w = 0; w < kStatWGs - 1; ++w) {
-        M1 = fmaxf(M1, mg[w * kTile * 5 + row * 5 + 0]);
-        M2 = fmaxf(M2, mg[w * kTile * 5 + row * 5 + 3]);
-      }
-      const float e1 = ex2((st.m1 - M1) * c1), e2 = ex2((st.m2 - M2) * c2);
-      float L1 = st.l1 * e1, A = st.acc * e1, L2 = st.l2 * e2;
-#pragma unroll
-      for (int w = 0; w < kStatWGs - 1; ++w) {
-        const float* o = mg + w * kTile * 5 + row * 5;
-        const float g1 = ex2((o[0] - M1) * c1), g2 = ex2((o[3] - M2) * c2);
-        L1 = fmaf(o[1], g1, L1);
-        A = fmaf(o[2], g1, A);
-        L2 = fmaf(o[4], g2, L2);
-      }
-      const size_t rows = size_t(a.BH) * a.NQ;
-      const size_t idx = size_t(bh) * a.NQ + grow;
-      if (a.partial != nullptr) {
-        float* p = a.partial + size_t(split) * 5 * rows + idx;
-        p[0 * rows] = a.scale1 * M1;
-        p[1 * rows] = L1;
-        p[2 * rows] = a.scale1 * A;
-        p[3 * rows] = a.scale2 * M2;
-        p[4 * rows] = L2;
-      } else {
-        const float lse1 = a.scale1 * M1 + logf(L1);
-        const float lse2 = a.scale2 * M2 + logf(L2);
-        a.lse1[idx] = lse1;
-        a.lse2[idx] = lse2;
-        a.kl[idx] = a.scale1 * A / L1 + lse2 - lse1;
-      }
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == kMmaWarp) {
-    tc_fence_after();
-    tmem_dealloc(tmem, 512);
-  }
-}
 
 // Merges the key-split partials of every row: with M = max over splits of
 // m_s (natural-log units), l = sum_s e^(m_s - M) l_s and the same weights for
@@ -388,18 +68,6 @@ __global__ void wait_timeout_selftest_kernel(int* status, uint64_t limit_ns) {
   }
 }
 
-template <int D1, int D2>
-static int launch_fwd_t(const TMaps& m, const FwdArgs& a, cudaStream_t st) {
-  using L = FwdLayout<D1, D2>;
-  auto kern = fwd_kernel<D1, D2>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
-  if (e != cudaSuccess) return e;
-  const int nqt = (a.NQ + kTile - 1) / kTile;
-  dim3 grid(nqt, a.BH, a.num_splits);
-  kern<<<grid, kFwdThreads, L::kAlloc, st>>>(m.q1, m.k1, m.q2, m.k2, a);
-  return cudaGetLastError();
-}
-
 int launch_fwd(const TMaps& m, int d1, int d2, const FwdArgs& a, cudaStream_t st) {
 #define SKL_FWD_CASE(A, B) \
   if (d1 == A && d2 == B) return launch_fwd_t<A, B>(m, a, st);
@@ -407,7 +75,7 @@ int launch_fwd(const TMaps& m, int d1, int d2, const FwdArgs& a, cudaStream_t st
   SKL_FWD_CASE(64, 128) SKL_FWD_CASE(64, 64) SKL_FWD_CASE(64, 32)
   SKL_FWD_CASE(32, 128) SKL_FWD_CASE(32, 64) SKL_FWD_CASE(32, 32)
 #undef SKL_FWD_CASE
-  return cudaErrorInvalidValue;
+  return launch_fwd_wide(m, d1, d2, a, st);
 }
 
 int launch_splitk_reduce(const float* partial, int rows, int num_splits, float* kl, float* lse1,

@@ -53,14 +53,19 @@ struct BwdArgs {
 };
 
 // Each returns a cudaError_t value (cudaSuccess = 0).  d1, d2 and d are the
-// kernels' tile widths (32, 64 or 128): a head dim below its tile width is
+// kernels' tile widths (32, 64, 128, 192 or 256): a head dim below its tile width is
 // read with the columns past it zero-filled by the TMA.
 int launch_fwd(const TMaps& m, int d1, int d2, const FwdArgs& a, cudaStream_t st);
+int launch_fwd_wide(const TMaps& m, int d1, int d2, const FwdArgs& a, cudaStream_t st);  // a side above 128
 int launch_splitk_reduce(const float* partial, int rows, int num_splits, float* kl, float* lse1,
                          float* lse2, cudaStream_t st);
 int launch_bwd_fused(const TMaps& m, int d1, int d2, const BwdArgs& a, cudaStream_t st);
 int launch_bwd_dq(const TMaps& m, int d1, int d2, const BwdArgs& a, cudaStream_t st);
 int launch_bwd_both(const TMaps& m, int d, const BwdArgs& a, cudaStream_t st);  // d1 = d2 = d, 32 or 64
+// Backward with a side above 128: pass 0 writes dK (ordered launches over a
+// key-head group via hsel), pass 1 writes dQ; neither uses atomics.
+int launch_bwd_wide_pass0(const TMaps& m, int d1, int d2, const BwdArgs& a, cudaStream_t st);
+int launch_bwd_wide_pass1(const TMaps& m, int d1, int d2, const BwdArgs& a, cudaStream_t st);
 int launch_ex2_probe(float* out, int blocks, int iters, cudaStream_t st);
 int launch_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t st);
 

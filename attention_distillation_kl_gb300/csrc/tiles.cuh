@@ -1,6 +1,6 @@
 // Shared-memory layout of one 128-row bf16 operand tile ([128 rows][D]) as
 // the TMA writes it, and its tcgen05 descriptors.
-//   D a multiple of 64: D / 64 blocks of [128 rows][64 elements], 128-byte
+//   D a multiple of 64 (up to 256): D / 64 blocks of [128 rows][64 elements], 128-byte
 //                       rows, 128-byte swizzle
 //   D = 32:             one block of [128 rows][32 elements], 64-byte rows,
 //                       64-byte swizzle
@@ -17,7 +17,7 @@ namespace skl {
 
 template <int D>
 struct OpTile {
-  static_assert(D == 32 || (D % 64 == 0 && D <= 128), "head dim 32, 64 or 128");
+  static_assert(D == 32 || (D % 64 == 0 && D <= 256), "tile width 32, 64, 128, 192 or 256");
   static constexpr int kD = D;
   static constexpr bool kWide = D >= 64;                 // 128-byte swizzle
   static constexpr int kBox = kWide ? 64 : 32;           // TMA box width, elements

@@ -32,11 +32,13 @@
  *   *_scaled calls take one scale per side, each under the same rule).
  * Causal: key j is visible to query i iff j <= i + (NK - NQ) (bottom-right
  *   aligned; j <= i when NQ == NK).  causal with NQ > NK is INVALID_ARG.
- * Head dims: d1, d2 any multiple of 16 from 16 to 128, independently
- *   (UNSUPPORTED otherwise).  The kernels compute in tiles 32, 64 or 128
- *   wide; a head dim below its tile width is read with the columns past it
- *   zero-filled, which changes no dot product (the padded work is not
- *   credited in any throughput figure).
+ * Head dims: d1, d2 any multiple of 16 from 16 to 256, independently
+ *   (UNSUPPORTED otherwise).  The kernels compute in tiles 32, 64, 128, 192
+ *   or 256 wide; a head dim below its tile width is read with the columns
+ *   past it zero-filled, which changes no dot product (the padded work is
+ *   not credited in any throughput figure).  Above 128 on either side the
+ *   forward streams K in 64-column blocks and the backward always runs as
+ *   two passes without atomics (dK, then dQ), whatever `deterministic` says.
  * Empty problems: B*H*NQ == 0 is a no-op that returns OK (the backward then
  *   zeroes dk); NK == 0 with NQ > 0 is INVALID_ARG (rows without keys).
  * Return: a streamkl_status value; C++ exceptions never cross this ABI.

@@ -83,8 +83,9 @@ def fwd(L, q=(A, A, A, A), B=1, H=1, NQ=128, NK=128, d1=64, d2=64, scale=0.125, 
     (dict(d1=8), skl.STREAMKL_UNSUPPORTED),
     (dict(d2=40), skl.STREAMKL_UNSUPPORTED),
     (dict(d1=0), skl.STREAMKL_UNSUPPORTED),
-    (dict(d2=144), skl.STREAMKL_UNSUPPORTED),
-    (dict(d1=256), skl.STREAMKL_UNSUPPORTED),
+    (dict(d2=136), skl.STREAMKL_UNSUPPORTED),
+    (dict(d1=272), skl.STREAMKL_UNSUPPORTED),
+    (dict(d2=512), skl.STREAMKL_UNSUPPORTED),
     (dict(NQ=256, NK=128, causal=1), skl.STREAMKL_INVALID_ARG),
     (dict(NK=0), skl.STREAMKL_INVALID_ARG),
     (dict(B=-1), skl.STREAMKL_INVALID_ARG),
