@@ -205,45 +205,153 @@ def ex2_rate(skl):
     return blocks * 256 * iters * 8 / best
 
 
-def key_split_timing(skl, stream):
-    w = WORKLOADS["c5"]
+def timed(fn, stream, reps=4):
+    """Median CUDA-event time (ms) of fn on `stream` over `reps` calls, after
+    one warm-up call."""
+    fn()
+    ts = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    return float(np.median(ts))
+
+
+def oracle_seconds(w, rows, modes):
+    """The float64 oracle, as it stands, on head (0, 0) of workload w: the
+    whole head when rows is None, else its last `rows` query rows (for a
+    causal problem the rows x all-keys sub-problem, bottom-right aligned, is
+    exactly those rows); forward plus one backward per mode in `modes`.
+    Returns (seconds for all B*H heads, extrapolated by unmasked pairs when
+    sampled; the sample's own seconds; its pairs)."""
+    import oracle
+    from attention_distillation_kl_gb300.workloads import generate_head, to_f64
+    q1, k1, q2, k2 = [to_f64(t) for t in generate_head(w, 0, 0)]
+    n = w.NQ if rows is None else min(rows, w.NQ)
+    q1, q2 = q1[-n:], q2[-n:]
+    t0 = time.perf_counter()
+    oracle.forward_head(q1, k1, q2, k2, w.scale, w.causal)
+    for m in modes:
+        oracle.backward_head(q1, k1, q2, k2, w.scale, w.causal, np.ones(n), m)
+    dt = time.perf_counter() - t0
+    off = w.NK - w.NQ
+    if w.causal:  # rows NQ - n .. NQ - 1 see i + off + 1 keys each
+        pairs = sum(i + off + 1 for i in range(w.NQ - n, w.NQ))
+    else:
+        pairs = n * w.NK
+    return dt * w.pairs / pairs, dt, pairs
+
+
+def config_report(skl, stream, sustained, rate, with_oracle):
+    """Every named workload besides the headline one: forward and backward
+    times, algorithmic TFLOP/s (2(d1+d2) flops per unmasked pair forward,
+    + 4 d_g backward) and the fraction of the roofline (the slower of the
+    sustained tensor peak and the measured ex2 rate; 2 ex2 per pair forward
+    and in mode P2, 1 in mode P1), with the oracle's time on the host."""
+    import oracle
+    out = {}
+    plan = [("pr1", ("p2", "p1"), None), ("c2", ("p2",), 256), ("c3", ("p2", "p1"), 128), ("c5", ("p2",), 32)]
+    for name, modes, rows in plan:
+        w = WORKLOADS[name]
+        dev = [t.cuda() for t in generate(w)]
+        kl, l1, l2 = skl.streamkl_fwd(*dev, w.scale, w.causal)
+        dkl = torch.ones_like(kl)
+        p = w.pairs
+        f_fwd = 2 * (w.d1 + w.d2) * p
+        r = {"workload": f"{name}: B={w.B} H={w.H} NQ={w.NQ} NK={w.NK} d1={w.d1} d2={w.d2} "
+                         f"{'causal' if w.causal else 'non-causal'}", "pairs": p}
+        r["fwd_ms"] = timed(lambda: skl.streamkl_fwd(*dev, w.scale, w.causal, kl, l1, l2), stream)
+        r["fwd_tflops"] = f_fwd / (r["fwd_ms"] * 1e-3) / 1e12
+        r["fwd_roofline_frac"] = max(f_fwd / (sustained * 1e12), 2 * p / rate) / (r["fwd_ms"] * 1e-3)
+        for m in modes:
+            mode = skl.STREAMKL_GRAD_P2 if m == "p2" else skl.STREAMKL_GRAD_P1
+            dg = w.d2 if m == "p2" else w.d1
+            dq = torch.empty(w.B, w.H, w.NQ, dg, device="cuda")
+            dk = torch.empty(w.B, w.H, w.NK, dg, device="cuda")
+            ms = timed(lambda: skl.streamkl_bwd(*dev, w.scale, w.causal, kl, l1, l2, dkl, mode, False, dq, dk), stream)
+            f = (2 * (w.d1 + w.d2) + 4 * dg) * p
+            r[f"bwd_{m}_ms"] = ms
+            r[f"bwd_{m}_tflops"] = f / (ms * 1e-3) / 1e12
+            r[f"bwd_{m}_roofline_frac"] = max(f / (sustained * 1e12), (2 if m == "p2" else 1) * p / rate) / (ms * 1e-3)
+            del dq, dk
+        if name == "c5":  # the key-split workload: forced and suggested split counts
+            heur = skl.streamkl_suggest_splits(w.B, w.H, w.NQ, w.NK, w.causal)
+            ws = torch.empty(skl.streamkl_fwd_splitk_workspace_bytes(w.B, w.H, w.NQ, max(8, heur)),
+                             dtype=torch.uint8, device="cuda")
+            r["suggested_splits"] = heur
+            r["fwd_splitk8_ms"] = timed(lambda: skl.streamkl_fwd_splitk(*dev, w.scale, w.causal, 8, ws, kl, l1, l2),
+                                        stream)
+            r["fwd_splitk_suggested_ms"] = timed(
+                lambda: skl.streamkl_fwd_splitk(*dev, w.scale, w.causal, heur, ws, kl, l1, l2), stream)
+            del ws
+        if with_oracle:
+            omodes = [oracle.MODE_P2 if m == "p2" else oracle.MODE_P1 for m in modes]
+            secs, dt, sp = oracle_seconds(w, rows, omodes)
+            r["oracle_s"] = secs
+            r["oracle_sample"] = ("all rows of head (0,0)" if rows is None else f"last {rows} rows of head (0,0)") + \
+                (f", {dt:.2f} s for {sp} pairs" + ("" if rows is None and w.B * w.H == 1 else
+                                                    f", scaled to {w.B * w.H} heads by pairs"))
+        out[name] = r
+        del dev, kl, l1, l2, dkl
+        torch.cuda.empty_cache()
+    return out
+
+
+def key_split_shapes(skl, stream):
+    """Short query blocks against long keys, where a CTA per query tile
+    leaves most SMs idle: the plain forward against the key-split forward
+    with the heuristic's split count and with fixed counts (B=1, H=4,
+    NQ=256, NK=131072, d=128, causal and not)."""
+    from attention_distillation_kl_gb300.workloads import Workload
+    out = {}
+    for causal in (True, False):
+        w = Workload("short-q", 1, 4, 256, 131072, 128, 128, causal, 1 / np.sqrt(128), "independent", 0.0, 1.0, 1008)
+        dev = [t.cuda() for t in generate(w)]
+        kl, l1, l2 = skl.streamkl_fwd(*dev, w.scale, w.causal)
+        heur = skl.streamkl_suggest_splits(w.B, w.H, w.NQ, w.NK, w.causal)
+        ws = torch.empty(skl.streamkl_fwd_splitk_workspace_bytes(w.B, w.H, w.NQ, max(64, heur)), dtype=torch.uint8,
+                         device="cuda")
+        f = 2 * (w.d1 + w.d2) * w.pairs
+        r = {"workload": f"B=1 H=4 NQ=256 NK=131072 d1=d2=128 {'causal' if causal else 'non-causal'}",
+             "suggested_splits": heur}
+        r["fwd_ms"] = timed(lambda: skl.streamkl_fwd(*dev, w.scale, w.causal, kl, l1, l2), stream)
+        for sp in sorted({8, 32, heur}):
+            r[f"fwd_splitk{sp}_ms"] = timed(
+                lambda: skl.streamkl_fwd_splitk(*dev, w.scale, w.causal, sp, ws, kl, l1, l2), stream)
+        r["fwd_tflops"] = f / (r["fwd_ms"] * 1e-3) / 1e12
+        r["fwd_splitk_suggested_tflops"] = f / (r[f"fwd_splitk{heur}_ms"] * 1e-3) / 1e12
+        r["speedup_suggested_over_plain"] = r["fwd_ms"] / r[f"fwd_splitk{heur}_ms"]
+        out["causal" if causal else "non_causal"] = r
+        del dev, ws
+        torch.cuda.empty_cache()
+    return out
+
+
+def wide_head_timing(skl, stream, sustained, rate):
+    """Head dim 256 on both sides (16K tokens x 8 heads, causal): forward
+    (K streamed in 64-column blocks) and the two-pass P2 backward."""
+    from attention_distillation_kl_gb300.workloads import Workload
+    w = Workload("wide256", 1, 8, 16384, 16384, 256, 256, True, 1 / 16.0, "perturbed", 0.3, 1.0, 1009)
     dev = [t.cuda() for t in generate(w)]
-    kl = torch.empty(w.B, w.H, w.NQ, device="cuda")
-    l1, l2 = torch.empty_like(kl), torch.empty_like(kl)
+    kl, l1, l2 = skl.streamkl_fwd(*dev, w.scale, w.causal)
+    dkl = torch.ones_like(kl)
     dq = torch.empty(w.B, w.H, w.NQ, w.d2, device="cuda")
     dk = torch.empty(w.B, w.H, w.NK, w.d2, device="cuda")
-    dkl = torch.ones(w.B, w.H, w.NQ, device="cuda")
-    heur = skl.streamkl_suggest_splits(w.B, w.H, w.NQ, w.NK, w.causal)
-    ws = torch.empty(skl.streamkl_fwd_splitk_workspace_bytes(w.B, w.H, w.NQ, max(8, heur)), dtype=torch.uint8,
-                     device="cuda")
-
-    def timed(fn, reps=4):
-        fn()
-        ts = []
-        for _ in range(reps):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            fn()
-            b.record(stream)
-            torch.cuda.synchronize()
-            ts.append(a.elapsed_time(b))
-        return float(np.median(ts))
-
     f_fwd, f_bwd = flops(w)
-    out = {"workload": f"c5: B={w.B} H={w.H} NQ=NK={w.NQ} d1={w.d1} d2={w.d2} causal"}
-    out["fwd_ms"] = timed(lambda: skl.streamkl_fwd(*dev, w.scale, w.causal, kl, l1, l2))
-    out["fwd_splitk8_ms"] = timed(lambda: skl.streamkl_fwd_splitk(*dev, w.scale, w.causal, 8, ws, kl, l1, l2))
-    out["suggested_splits"] = heur
-    out["fwd_splitk_suggested_ms"] = timed(lambda: skl.streamkl_fwd_splitk(*dev, w.scale, w.causal, heur, ws, kl,
-                                                                           l1, l2))
-    out["bwd_p2_ms"] = timed(lambda: skl.streamkl_bwd(*dev, w.scale, w.causal, kl, l1, l2, dkl,
-                                                      skl.STREAMKL_GRAD_P2, False, dq, dk))
-    out["fwd_tflops"] = f_fwd / (out["fwd_ms"] * 1e-3) / 1e12
-    out["fwd_splitk8_tflops"] = f_fwd / (out["fwd_splitk8_ms"] * 1e-3) / 1e12
-    out["bwd_p2_tflops"] = f_bwd / (out["bwd_p2_ms"] * 1e-3) / 1e12
-    del dev, dq, dk, ws
+    r = {"workload": "B=1 H=8 NQ=NK=16384 d1=d2=256 causal"}
+    r["fwd_ms"] = timed(lambda: skl.streamkl_fwd(*dev, w.scale, w.causal, kl, l1, l2), stream)
+    r["bwd_p2_ms"] = timed(lambda: skl.streamkl_bwd(*dev, w.scale, w.causal, kl, l1, l2, dkl,
+                                                    skl.STREAMKL_GRAD_P2, False, dq, dk), stream)
+    r["fwd_tflops"] = f_fwd / (r["fwd_ms"] * 1e-3) / 1e12
+    r["bwd_p2_tflops"] = f_bwd / (r["bwd_p2_ms"] * 1e-3) / 1e12
+    r["fwd_roofline_frac"] = max(f_fwd / (sustained * 1e12), 2 * w.pairs / rate) / (r["fwd_ms"] * 1e-3)
+    r["bwd_p2_roofline_frac"] = max(f_bwd / (sustained * 1e12), 2 * w.pairs / rate) / (r["bwd_p2_ms"] * 1e-3)
+    del dev, dq, dk
     torch.cuda.empty_cache()
-    return out
+    return r
 
 
 def gqa_timing(skl, stream):
@@ -258,26 +366,13 @@ def gqa_timing(skl, stream):
     dkl = torch.ones_like(kl)
     dq = torch.empty(w.B, w.H, w.NQ, w.d2, device="cuda")
     dk = torch.empty(w.B, hk, w.NK, w.d2, device="cuda")
-
-    def timed(fn, reps=4):
-        fn()
-        ts = []
-        for _ in range(reps):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            fn()
-            b.record(stream)
-            torch.cuda.synchronize()
-            ts.append(a.elapsed_time(b))
-        return float(np.median(ts))
-
     f_fwd, f_bwd = flops(w)
     out = {"workload": f"B={w.B} H={w.H} HK1=HK2={hk} NQ=NK={w.NQ} d1=d2=128 causal"}
-    out["fwd_ms"] = timed(lambda: skl.streamkl_fwd_gqa(*dev, w.scale, w.scale, w.causal, kl, l1, l2))
+    out["fwd_ms"] = timed(lambda: skl.streamkl_fwd_gqa(*dev, w.scale, w.scale, w.causal, kl, l1, l2), stream)
     out["bwd_p2_ms"] = timed(lambda: skl.streamkl_bwd_gqa(*dev, w.scale, w.scale, w.causal, kl, l1, l2, dkl,
-                                                          skl.STREAMKL_GRAD_P2, False, dq, dk))
+                                                          skl.STREAMKL_GRAD_P2, False, dq, dk), stream)
     out["bwd_p2_det_ms"] = timed(lambda: skl.streamkl_bwd_gqa(*dev, w.scale, w.scale, w.causal, kl, l1, l2, dkl,
-                                                              skl.STREAMKL_GRAD_P2, True, dq, dk))
+                                                              skl.STREAMKL_GRAD_P2, True, dq, dk), stream)
     out["fwd_tflops"] = f_fwd / (out["fwd_ms"] * 1e-3) / 1e12
     out["bwd_p2_tflops"] = f_bwd / (out["bwd_p2_ms"] * 1e-3) / 1e12
     del dev, dq, dk
@@ -294,26 +389,13 @@ def both_sides_timing(skl, stream, d=64):
     kl, l1, l2 = skl.streamkl_fwd(*dev, w.scale, w.causal)
     dkl = torch.ones_like(kl)
     bufs = [torch.empty(w.B, w.H, n, d, device="cuda") for n in (w.NQ, w.NK, w.NQ, w.NK)]
-
-    def timed(fn, reps=4):
-        fn()
-        ts = []
-        for _ in range(reps):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            fn()
-            b.record(stream)
-            torch.cuda.synchronize()
-            ts.append(a.elapsed_time(b))
-        return float(np.median(ts))
-
     out = {"workload": f"B={w.B} H={w.H} NQ=NK={w.NQ} d1=d2={d} causal"}
     out["bwd_p2_ms"] = timed(lambda: skl.streamkl_bwd(*dev, w.scale, w.causal, kl, l1, l2, dkl,
-                                                      skl.STREAMKL_GRAD_P2, False, bufs[2], bufs[3]))
+                                                      skl.STREAMKL_GRAD_P2, False, bufs[2], bufs[3]), stream)
     out["bwd_p1_ms"] = timed(lambda: skl.streamkl_bwd(*dev, w.scale, w.causal, kl, l1, l2, dkl,
-                                                      skl.STREAMKL_GRAD_P1, False, bufs[0], bufs[1]))
+                                                      skl.STREAMKL_GRAD_P1, False, bufs[0], bufs[1]), stream)
     out["bwd_both_ms"] = timed(lambda: skl.streamkl_bwd_both(*dev, w.scale, w.scale, w.causal, kl, l1, l2, dkl,
-                                                             False, *bufs))
+                                                             False, *bufs), stream)
     # two S products and four gradient products, 2 d flops each per pair
     out["bwd_both_tflops"] = 12 * d * w.pairs / (out["bwd_both_ms"] * 1e-3) / 1e12
     del dev, bufs
@@ -321,12 +403,69 @@ def both_sides_timing(skl, stream, d=64):
     return out
 
 
+def gpu_numa(dev_id):
+    """The GPU's PCI address, the host NUMA node sysfs gives for it and the
+    CPUs local to it (empty when the system does not say)."""
+    info = {"pci_bus_id": None, "numa_node": None, "local_cpus": None}
+    try:
+        bus = subprocess.run(["nvidia-smi", "-i", str(dev_id), "--query-gpu=pci.bus_id", "--format=csv,noheader"],
+                             capture_output=True, text=True, timeout=20).stdout.strip()
+        dom, rest = bus.split(":", 1)
+        sys_id = f"{int(dom, 16):04x}:{rest}".lower()
+        info["pci_bus_id"] = sys_id
+        base = f"/sys/bus/pci/devices/{sys_id}"
+        if os.path.exists(base + "/numa_node"):
+            info["numa_node"] = int(open(base + "/numa_node").read().strip())
+        if os.path.exists(base + "/local_cpulist"):
+            info["local_cpus"] = open(base + "/local_cpulist").read().strip()
+    except (OSError, ValueError, subprocess.SubprocessError):
+        pass
+    return info
+
+
+def parse_cpulist(txt):
+    cpus = set()
+    for part in txt.split(","):
+        if "-" in part:
+            lo, hi = part.split("-")
+            cpus.update(range(int(lo), int(hi) + 1))
+        elif part.strip():
+            cpus.add(int(part))
+    return cpus
+
+
+def pages_by_node(ptr):
+    """NUMA nodes of the pages of the mapping that holds host address ptr,
+    from /proc/self/numa_maps ({"N0": pages, ...}; empty if unknown)."""
+    try:
+        best, fields = -1, []
+        for line in open("/proc/self/numa_maps"):
+            parts = line.split()
+            start = int(parts[0], 16)
+            if best < start <= ptr:
+                best, fields = start, parts
+        return {f.split("=")[0]: int(f.split("=")[1]) for f in fields if f[:1] == "N" and "=" in f}
+    except (OSError, ValueError, IndexError):
+        return {}
+
+
 def run_mine(args, rank, world, local):
     import attention_distillation_kl_gb300 as skl  # raises if the CUDA library is missing
     torch.cuda.set_device(local)
     dev_id = torch.cuda.current_device()
     w = rank_workload(W, rank)  # each rank its own batch
+    # Pinned host inputs on the memory node local to this GPU: run on its
+    # local CPUs while the buffers are allocated and touched, so the pages
+    # land there (first touch); then record where they actually are.
+    numa = gpu_numa(dev_id)
+    affinity0 = os.sched_getaffinity(0)
+    if numa["local_cpus"]:
+        local = parse_cpulist(numa["local_cpus"]) & affinity0
+        if local:
+            os.sched_setaffinity(0, local)
     host = [t.pin_memory() for t in generate(w)]
+    numa["pinned_pages_by_node"] = pages_by_node(host[0].data_ptr())
+    os.sched_setaffinity(0, affinity0)
     dkl_h = generate_dkl(w).pin_memory()
     dev = [t.cuda() for t in host]
     dkl = dkl_h.cuda()
@@ -444,16 +583,18 @@ def run_mine(args, rank, world, local):
     extra_bytes = free0 - torch.cuda.mem_get_info()[0]
     f_p1 = (2 * (w.d1 + w.d2) + 4 * w.d1) * w.pairs
 
-    # key-split forward (and the d2 = 64 backward) on the 131K-token,
-    # 4-head workload, timed on their own after the step loop: forced 8
-    # splits, the heuristic's choice, and the plain forward for comparison
-    c5 = key_split_timing(skl, stream) if rank == 0 and world == 1 and not args.no_cpu_baseline else None
-    both = both_sides_timing(skl, stream) if rank == 0 and world == 1 and not args.no_cpu_baseline else None
-    both32 = both_sides_timing(skl, stream, 32) if both is not None else None
-    gqa = gqa_timing(skl, stream) if both is not None else None
-
     rate = ex2_rate(skl)
     burst, sustained, _hbm, src = peaks()
+    # every other named workload, the short-query key-split shapes, head dim
+    # 256, both-sides and grouped-key-head calls: each timed on its own after
+    # the step loop (single-GPU runs only; the oracle times need the host)
+    extras = rank == 0 and world == 1 and not args.no_cpu_baseline
+    configs = config_report(skl, stream, sustained, rate, with_oracle=True) if extras else None
+    short = key_split_shapes(skl, stream) if extras else None
+    wide = wide_head_timing(skl, stream, sustained, rate) if extras else None
+    both = both_sides_timing(skl, stream) if extras else None
+    both32 = both_sides_timing(skl, stream, 32) if extras else None
+    gqa = gqa_timing(skl, stream) if extras else None
     pairs = w.pairs
     # roofline time of each kernel: the slower of the tensor pipe and the ex2 unit
     t_fwd = max(f_fwd / (sustained * 1e12), 2 * pairs / rate)
@@ -485,7 +626,9 @@ def run_mine(args, rank, world, local):
             "bwd_p1_ms": p1_ms, "bwd_p1_tflops": f_p1 / (p1_ms * 1e-3) / 1e12,
             "bwd_p1_roofline_frac": max(f_p1 / (sustained * 1e12), pairs / rate) / (p1_ms * 1e-3),
             "extra_device_bytes": extra_bytes,
-            "key_split_131k": c5,
+            "configs": configs,
+            "key_split_short_queries": short,
+            "wide_head_d256": wide,
             "both_sides_d64": both,
             "both_sides_d32": both32,
             "gqa_16k": gqa,
@@ -500,7 +643,8 @@ def run_mine(args, rank, world, local):
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                     "copies": "pinned host -> device on a second stream, double-buffered, overlapping "
                               "the previous step; KL read back every step",
-                    "h2d_gbs_alone": sum(t.numel() * t.element_size() for t in host) / (h2d_ms * 1e-3) / 1e9},
+                    "h2d_gbs_alone": sum(t.numel() * t.element_size() for t in host) / (h2d_ms * 1e-3) / 1e9,
+                    "numa": numa},
             "gpu_launches": 2 * args.steps,
             "clocks": clk.summary(),
         }

@@ -85,3 +85,28 @@ def test_c5_split(splits):
         rows = np.unique(np.concatenate([[0, 1, 128, w.NQ - 1], g.integers(0, w.NQ, 16)]))
         rkl, rl1, rl2 = oracle.forward_rows(*head64(host, 0, h), w.scale, w.causal, rows)
         assert_fwd_close(gkl[0, h, rows], gl1[0, h, rows], gl2[0, h, rows], rkl, rl1, rl2, f"c5 h{h}")
+
+
+@pytest.mark.parametrize("causal", [True, False], ids=["causal", "non-causal"])
+def test_short_queries_long_keys(causal):
+    """256 queries against 131072 keys (4 heads, d = 128): the shape the key
+    split exists for.  The heuristic's split count (well above 1 here) and a
+    fixed 32 against the oracle on rows of every head, and against the plain
+    forward on all rows."""
+    w = Workload("short-q", 1, 4, 256, 131072, 128, 128, causal, 1.0 / np.sqrt(128), "independent", 0.0, 1.0, 1008)
+    host, dev = inputs(w)
+    s = skl.streamkl_suggest_splits(w.B, w.H, w.NQ, w.NK, w.causal)
+    assert s > 1
+    ukl, ul1, ul2 = skl.streamkl_fwd(*dev, w.scale, w.causal)
+    g = np.random.default_rng(6)
+    for splits in (s, 32):
+        kl, l1, l2 = skl.streamkl_fwd_splitk(*dev, w.scale, w.causal, splits)
+        torch.cuda.synchronize()
+        assert skl.streamkl_get_device_status() == 0
+        gkl, gl1, gl2 = np_(kl), np_(l1), np_(l2)
+        assert_fwd_close(gkl, gl1, gl2, np_(ukl), np_(ul1), np_(ul2), f"split {splits} vs unsplit")
+        for h in range(w.H):
+            rows = np.unique(np.concatenate([[0, 127, 128, w.NQ - 1], g.integers(0, w.NQ, 12)]))
+            rkl, rl1, rl2 = oracle.forward_rows(*head64(host, 0, h), w.scale, w.causal, rows)
+            assert_fwd_close(gkl[0, h, rows], gl1[0, h, rows], gl2[0, h, rows], rkl, rl1, rl2,
+                             f"short queries split {splits} h{h}")
