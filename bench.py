@@ -579,6 +579,9 @@ def run_mine(args, rank, world, local):
         if k > 0:  # the first is warm-up
             p1_ms.append(a.elapsed_time(b_))
     p1_ms = float(np.median(p1_ms))
+    # the deterministic (atomic-free, two-pass) P2 backward on the same inputs
+    det_ms = timed(lambda: skl.streamkl_bwd(*dev, w.scale, w.causal, kl, l1, l2, dkl, skl.STREAMKL_GRAD_P2, True,
+                                            dq, dk), stream, reps=3)
     # the library allocates nothing: device memory free before and after the calls must agree
     extra_bytes = free0 - torch.cuda.mem_get_info()[0]
     f_p1 = (2 * (w.d1 + w.d2) + 4 * w.d1) * w.pairs
@@ -625,6 +628,7 @@ def run_mine(args, rank, world, local):
             "fwd_roofline_frac": t_fwd / (fwd_ms * 1e-3), "bwd_roofline_frac": t_bwd / (bwd_ms * 1e-3),
             "bwd_p1_ms": p1_ms, "bwd_p1_tflops": f_p1 / (p1_ms * 1e-3) / 1e12,
             "bwd_p1_roofline_frac": max(f_p1 / (sustained * 1e12), pairs / rate) / (p1_ms * 1e-3),
+            "bwd_p2_deterministic_ms": det_ms, "bwd_p2_deterministic_over_fused": det_ms / bwd_ms,
             "extra_device_bytes": extra_bytes,
             "configs": configs,
             "key_split_short_queries": short,
