@@ -77,6 +77,18 @@ struct BwdLayout {
   static_assert(kAlloc <= 232448, "over the 227 KB shared memory limit");
 };
 
+// The gradient products of tile t are issued only once the S products of
+// tile t + 1 are queued: the tensor pipe takes them in issue order, and S is
+// what the dS warps wait for, so S should not queue behind dK and dQ.  A
+// scheduling hint only (the two groups touch different TMEM columns and
+// operands), so the wait gives up after 20 us rather than reporting anything.
+__device__ __forceinline__ void wait_s_queued(volatile int* s_queued, int want) {
+  if (want <= 0 || *s_queued >= want) return;
+  const uint64_t t0 = globaltimer();
+  while (*s_queued < want && globaltimer() - t0 < 20000ull) {
+  }
+}
+
 template <int D1, int D2, int MODE>
 __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
     bwd_fused_kernel(const __grid_constant__ CUtensorMap tq1, const __grid_constant__ CUtensorMap tk1,
@@ -110,9 +122,13 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
   const CUtensorMap* tqg = kP2 ? &tq2 : &tq1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::oMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::oMisc + 4);
+  // query tiles whose S products the S issuer has queued (a scheduling
+  // hint for the gradient issuers, see below)
+  volatile int* s_queued = reinterpret_cast<volatile int*>(smem + L::oMisc + 8);
   const Ctl ctl{abort_flag, a.status};
 
   if (threadIdx.x == 0) {
+    *s_queued = 0;
     for (int b = 0; b < L::kNumBars; ++b) {
       uint32_t count = 1;  // TMA transaction barriers and tcgen05.commit targets
       if (b == L::B_SFREE || b == L::B_DSFULL) count = 8;  // one per dS warp
@@ -192,6 +208,7 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
         if constexpr (kP2) s_product(T2{}, t_s2, sb + L::oQg + (i & 1) * L::kQg, sb + L::oK2);
         else s_product(T1{}, t_s1, sb + L::oQg + (i & 1) * L::kQg, sb + L::oK1);
         mma_commit(1u, bar(L::B_SFULL));
+        *s_queued = i + 1;
       }
       // every MMA of every issuer has finished before TMEM is released
       mma_commit(1u, bar(L::B_DONE));
@@ -210,6 +227,7 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
       if (n > 0 && mbar_wait_polled(bar(L::B_KFULL), 0, ctl)) {
         for (; t < n; ++t) {
           if (!mbar_wait_polled(bar(L::B_DSFULL), t & 1, ctl)) break;
+          wait_s_queued(s_queued, t + 1 < n ? t + 2 : 0);
           tc_fence_after();
           const uint64_t qgn = TG::desc_n(sb + L::oQg + (t & 1) * L::kQg);
 #pragma unroll
@@ -243,6 +261,7 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
         if (a.write_dq && n > 0 && mbar_wait_polled(bar(L::B_KFULL), 0, ctl)) {
           for (int t = 0; t < n; ++t) {
             if (!mbar_wait_polled(bar(L::B_DSFULL), t & 1, ctl)) break;
+            wait_s_queued(s_queued, t + 1 < n ? t + 2 : 0);
             if (!mbar_wait_polled(bar(L::B_DQEMPTY), (t & 1) ^ 1, ctl)) break;
             tc_fence_after();
 #pragma unroll
