@@ -22,7 +22,7 @@ __all__ = [
     "status_string", "STREAMKL_STATIC_WORKSPACE_BYTES",
     "streamkl_get_device_status", "streamkl_probe_ex2", "streamkl_selftest_wait_timeout",
     "STREAMKL_OK", "STREAMKL_INVALID_ARG", "STREAMKL_UNSUPPORTED", "STREAMKL_CUDA_ERROR",
-    "STREAMKL_DEVICE_TIMEOUT", "STREAMKL_GRAD_P2", "STREAMKL_GRAD_P1",
+    "STREAMKL_DEVICE_TIMEOUT", "STREAMKL_DEBUG_BOUNDS", "STREAMKL_GRAD_P2", "STREAMKL_GRAD_P1",
 ]
 
 STREAMKL_OK = 0
@@ -30,6 +30,7 @@ STREAMKL_INVALID_ARG = 1
 STREAMKL_UNSUPPORTED = 2
 STREAMKL_CUDA_ERROR = 3
 STREAMKL_DEVICE_TIMEOUT = 4
+STREAMKL_DEBUG_BOUNDS = 5
 STREAMKL_GRAD_P2 = 0
 STREAMKL_GRAD_P1 = 1
 

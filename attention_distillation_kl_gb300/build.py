@@ -15,6 +15,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libstreamkl.so")
+DEBUG_LIB = os.path.join(PKG, "libstreamkl_debug.so")
 SOURCES = ["api.cu", "fwd.cu", "fwd_wide.cu", "bwd.cu", "bwd_wide_p0.cu", "bwd_wide_p1.cu", "bwd_both.cu",
            "static_ws.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -33,13 +34,22 @@ def cflags(extra=()):
                    "-I", CSRC, "--expt-relaxed-constexpr", *extra]
 
 
-def build(verbose=False, extra_flags=()):
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose=False, extra_flags=(), debug=True):
+    """Compiles libstreamkl.so and, with debug=True, libstreamkl_debug.so (the
+    same sources with STREAMKL_DEBUG: in-kernel bounds checks that record a
+    failed check in the device status word), all translation units of both
+    in parallel."""
     nvcc = nvcc_path()
+    variants = [("", LIB, [])]
+    if debug:
+        variants.append(("debug", DEBUG_LIB, ["-DSTREAMKL_DEBUG"]))
+    for sub, _, _ in variants:
+        os.makedirs(os.path.join(BUILD, sub), exist_ok=True)
 
-    def one(src):
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
-        cmd = [nvcc, *cflags(extra_flags), "-c", os.path.join(CSRC, src), "-o", obj]
+    def one(job):
+        sub, flags, src = job
+        obj = os.path.join(BUILD, sub, src.replace(".cu", ".o"))
+        cmd = [nvcc, *cflags([*extra_flags, *flags]), "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
@@ -47,14 +57,17 @@ def build(verbose=False, extra_flags=()):
             print(r.stdout, r.stderr)
         return obj
 
-    with ThreadPoolExecutor(len(SOURCES)) as ex:
-        objs = list(ex.map(one, SOURCES))
-    tmp = LIB + ".tmp"
-    cmd = [nvcc, *ARCH, "-shared", "-Xcompiler", "-fPIC", "-o", tmp, *objs]
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    if r.returncode != 0:
-        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    jobs = [(sub, flags, src) for sub, _, flags in variants for src in SOURCES]
+    with ThreadPoolExecutor(min(len(jobs), max(4, os.cpu_count() or 4))) as ex:
+        objs = list(ex.map(one, jobs))
+    for k, (sub, lib, _) in enumerate(variants):
+        tmp = lib + ".tmp"
+        part = objs[k * len(SOURCES):(k + 1) * len(SOURCES)]
+        cmd = [nvcc, *ARCH, "-shared", "-Xcompiler", "-fPIC", "-o", tmp, *part]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+        os.replace(tmp, lib)
     return LIB
 
 

@@ -397,6 +397,7 @@ const char* streamkl_status_string(int status) {
     case STREAMKL_UNSUPPORTED: return "unsupported head dimension or device";
     case STREAMKL_CUDA_ERROR: return "CUDA error";
     case STREAMKL_DEVICE_TIMEOUT: return "a kernel abandoned a wait (device timeout)";
+    case STREAMKL_DEBUG_BOUNDS: return "debug build: an index failed its bounds check (access skipped)";
     default: return "unknown status";
   }
 }

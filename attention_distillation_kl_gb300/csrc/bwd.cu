@@ -290,7 +290,7 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
       na = -INFINITY;
       nb = kP2 ? -INFINITY : 0.f;
       ws = 0.f;
-      if (qi < a.NQ) {
+      if (qi < a.NQ && SKL_CHECK(a.status, bh < a.BH)) {
         const size_t idx = size_t(bh) * a.NQ + qi;
         const float l1 = a.lse1[idx];
         na = -l1 * kLog2e;
@@ -364,6 +364,7 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
           // an earlier reduce could be overwritten)
           if (h * 32 >= a.dg || r0 >= a.NQ) return;
           const uint32_t box = stage + (nred % kDqBoxes) * kDqBoxBytes;
+          if (!SKL_CHECK(a.status, box + kDqBoxBytes <= sb + L::oBar && h * 32 < a.dg && r0 < a.NQ)) return;
           // the box used kDqBoxes reduces ago has been read
           if (lane == 0) bulk_wait_read_le<kDqBoxes - 1>();
           __syncwarp();
@@ -418,7 +419,7 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
       for (int ch = 0; ch < DG / 32; ++ch) {
         uint32_t v[32];
         tmem_ld32(t_dk + lane_off + ch * 32, v);
-        if (kj < a.NK) {
+        if (kj < a.NK && SKL_CHECK(a.status, bh / gg < a.BH / gg && a.dg <= DG)) {
 #pragma unroll
           for (int e = 0; e < 32; e += 4)
             if (ch * 32 + e < a.dg)
@@ -640,7 +641,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       for (int ch = 0; ch < DG / 32; ++ch) {
         uint32_t v[32];
         tmem_ld32(t_dq + lane_off + ch * 32, v);
-        if (qi < a.NQ) {
+        if (qi < a.NQ && SKL_CHECK(a.status, bh < a.BH && a.dg <= DG)) {
 #pragma unroll
           for (int e = 0; e < 32; e += 4)
             if (ch * 32 + e < a.dg)

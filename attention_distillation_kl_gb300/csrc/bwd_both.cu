@@ -309,6 +309,7 @@ __global__ void __launch_bounds__(kBothThreads, 1)
           // reduce groups and no box still being read is overwritten
           if (h * 16 >= a.dg || r0 >= a.NQ) break;
           const uint32_t box = stage + (nred % kBothBoxes) * 2048;
+          if (!SKL_CHECK(a.status, box + 2048 <= sb + L::oBar && h * 16 < a.dg)) break;
           if (lane == 0) bulk_wait_read_le<kBothBoxes - 1>();  // the box used kBothBoxes reduces ago was read
           __syncwarp();
 #pragma unroll
@@ -338,7 +339,7 @@ __global__ void __launch_bounds__(kBothThreads, 1)
         for (int ch = 0; ch < D / 32; ++ch) {
           uint32_t v[32];
           tmem_ld32((side == 0 ? t_dk1 : t_dk2) + lane_off + ch * 32, v);
-          if (kj < a.NK) {
+          if (kj < a.NK && SKL_CHECK(a.status, bh < a.BH && a.dg <= D)) {
 #pragma unroll
             for (int e = 0; e < 32; e += 4)
               if (ch * 32 + e < a.dg)

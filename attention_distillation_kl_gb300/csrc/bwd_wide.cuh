@@ -148,6 +148,10 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             break;
           }
           const uint32_t dst = sb + L::oRing + s * L::kSlot;
+          if (!SKL_CHECK(a.status, dst + L::kSlot <= sb + L::oBar && r0 < (kDK ? a.NQ : a.NK) + kTile)) {
+            go = false;
+            break;
+          }
           if (blk < L::kNb1) {
             mbar_arrive_expect_tx(bar(L::B_VFULL + s), T1::kBlockBytes);
             tma_load_3d(dst, m1, bar(L::B_VFULL + s), blk * T1::kBox, r0, z1);
@@ -303,7 +307,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         for (int ch = wg; ch < DG / 32; ch += 2) {
           uint32_t x[32];
           tmem_ld32(t_g + lane_off + ch * 32, x);
-          if (kj < a.NK) {
+          if (kj < a.NK && SKL_CHECK(a.status, bh / gg < a.BH / gg && a.dg <= DG)) {
 #pragma unroll
             for (int e = 0; e < 32; e += 4)
               if (ch * 32 + e < a.dg)
@@ -326,7 +330,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         for (int ch = wg; ch < DG / 32; ch += 2) {
           uint32_t x[32];
           tmem_ld32(t_g + lane_off + ch * 32, x);
-          if (qi < a.NQ) {
+          if (qi < a.NQ && SKL_CHECK(a.status, bh < a.BH && a.dg <= DG)) {
 #pragma unroll
             for (int e = 0; e < 32; e += 4)
               if (ch * 32 + e < a.dg)

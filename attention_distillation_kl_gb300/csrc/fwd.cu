@@ -16,6 +16,7 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restr
                                                             float* __restrict__ lse2) {
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < rows; i += gridDim.x * blockDim.x) {
     const size_t R = size_t(rows);
+    if (num_splits < 1) continue;  // nothing to merge (the host never launches this)
     float M1 = -INFINITY, M2 = -INFINITY;
     for (int s = 0; s < num_splits; ++s) {
       M1 = fmaxf(M1, part[(size_t(s) * 5 + 0) * R + i]);

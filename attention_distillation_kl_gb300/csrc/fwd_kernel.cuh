@@ -276,6 +276,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
               break;
             }
             const uint32_t st = sb + L::oK + s * L::kStage;
+            if (!SKL_CHECK(a.status, s < L::kStages && k0 < a.NK + kTile)) {
+              go = false;
+              break;
+            }
             if (b < L::kNb1) {
               mbar_arrive_expect_tx(bar_kfull(s), T1::kBlockBytes);
               tma_load_3d(st, &tk1, bar_kfull(s), b * T1::kBox, k0, bh / a.g1);
@@ -437,7 +441,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       const size_t rows = size_t(a.BH) * a.NQ;
       const size_t idx = size_t(bh) * a.NQ + grow;
-      if (a.partial != nullptr) {
+      if (!SKL_CHECK(a.status, idx < rows && split < a.num_splits)) {
+        // (debug build) out-of-range row or split: nothing is written
+      } else if (a.partial != nullptr) {
         float* p = a.partial + size_t(split) * 5 * rows + idx;
         p[0 * rows] = a.scale1 * M1;
         p[1 * rows] = L1;

@@ -19,6 +19,19 @@ namespace skl {
 #define STREAMKL_WAIT_LIMIT_NS 4000000000ull
 #endif
 
+// Bounds checks of the debug build (compiled with STREAMKL_DEBUG): every
+// global-memory index a kernel computes, and the shared-memory staging and
+// TMA coordinates, are checked against the extents the kernel was given; a
+// failed check skips the access and records STREAMKL_DEBUG_BOUNDS in the
+// device status word (no trap, the context stays usable).  In the normal
+// build the checks compile to nothing.
+#ifdef STREAMKL_DEBUG
+#define SKL_CHECK(status, cond) \
+  ((cond) ? true : (atomicCAS((status), 0, (int)STREAMKL_DEBUG_BOUNDS), false))
+#else
+#define SKL_CHECK(status, cond) true
+#endif
+
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 // Finite stand-in for -inf in running maxima: scaled by any allowed softmax

@@ -60,7 +60,10 @@ enum streamkl_status {
   STREAMKL_INVALID_ARG = 1,    /* null/misaligned pointer, bad size, causal with NQ > NK, small workspace */
   STREAMKL_UNSUPPORTED = 2,    /* head dim or device not supported */
   STREAMKL_CUDA_ERROR = 3,     /* a CUDA runtime/driver call failed (launch, tensor map, attribute) */
-  STREAMKL_DEVICE_TIMEOUT = 4  /* reported by streamkl_get_device_status(): a kernel gave up a wait */
+  STREAMKL_DEVICE_TIMEOUT = 4, /* reported by streamkl_get_device_status(): a kernel gave up a wait */
+  STREAMKL_DEBUG_BOUNDS = 5    /* reported by streamkl_get_device_status() of a build with STREAMKL_DEBUG
+                                  defined: an index a kernel computed failed its bounds check, and the
+                                  access was skipped */
 };
 
 enum streamkl_grad_mode {

@@ -41,6 +41,20 @@ def test_library_exports_every_declared_symbol(L):
         assert name in skl._SIGS, f"binding lacks {name}"
 
 
+def test_debug_library_exports_every_declared_symbol():
+    # the STREAMKL_DEBUG build of the same sources (bounds checks in the kernels)
+    import ctypes
+    import os
+    path = os.path.join(os.path.dirname(skl.library_path), "libstreamkl_debug.so")
+    if not os.path.exists(path):
+        pytest.skip("debug library not built")
+    D = ctypes.CDLL(path)
+    for name in declared_symbols():
+        assert hasattr(D, name), name
+    D.streamkl_status_string.restype = ctypes.c_char_p
+    assert b"bounds" in D.streamkl_status_string(skl.STREAMKL_DEBUG_BOUNDS)
+
+
 def test_binding_wraps_every_entry_point():
     # each C entry point has a Python function of the same name, exported
     for name in declared_symbols():
