@@ -16,7 +16,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libstreamkl.so")
 DEBUG_LIB = os.path.join(PKG, "libstreamkl_debug.so")
-SOURCES = ["api.cu", "fwd.cu", "fwd_wide.cu", "bwd.cu", "bwd_wide_p0.cu", "bwd_wide_p1.cu", "bwd_both.cu",
+SOURCES = ["api.cu", "fwd.cu", "fwd_wide.cu", "bwd.cu", "dq_fixed.cu", "bwd_wide_p0.cu", "bwd_wide_p1.cu", "bwd_both.cu",
            "static_ws.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -60,16 +60,18 @@ bool make_map(CUtensorMap* m, const void* ptr, long long BH, long long N, int d)
   return r == CUDA_SUCCESS;
 }
 
-// dQ [BH][NQ][dg] fp32 as a 3-D tensor: boxes of 16 elements x 32 rows x 1,
-// 64-byte swizzle, the target of the backward's bulk reduce-adds.
-bool make_map_dq(CUtensorMap* m, void* ptr, long long BH, long long NQ, int dg) {
+// dQ [BH][NQ][dg] fp32 (or int32: the deterministic backward's fixed-point
+// sums) as a 3-D tensor: boxes of 16 elements x 32 rows x 1, 64-byte
+// swizzle, the target of the backward's bulk reduce-adds.
+bool make_map_dq(CUtensorMap* m, void* ptr, long long BH, long long NQ, int dg, bool int32 = false) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[3] = {cuuint64_t(dg), cuuint64_t(NQ), cuuint64_t(BH)};
   cuuint64_t strides[2] = {cuuint64_t(dg) * 4, cuuint64_t(NQ) * dg * 4};
   cuuint32_t box[3] = {16, 32, 1};
   cuuint32_t es[3] = {1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, es,
+  CUresult r = fn(m, int32 ? CU_TENSOR_MAP_DATA_TYPE_INT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims,
+                  strides, box, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -78,10 +80,11 @@ bool make_map_dq(CUtensorMap* m, void* ptr, long long BH, long long NQ, int dg) 
 // The fused backward's dQ target: boxes of 32 fp32 x 32 rows with the
 // 128-byte swizzle (one full 128-byte line per row and box: fewer, larger
 // reduce operations than 64-byte pieces), or the 16-wide map for dg = 16.
-bool make_map_dq_wide(CUtensorMap* m, void* ptr, long long BH, long long NQ, int dg, int* box_cols) {
+bool make_map_dq_wide(CUtensorMap* m, void* ptr, long long BH, long long NQ, int dg, int* box_cols,
+                      bool int32 = false) {
   if (dg < 32) {
     *box_cols = 16;
-    return make_map_dq(m, ptr, BH, NQ, dg);
+    return make_map_dq(m, ptr, BH, NQ, dg, int32);
   }
   auto fn = encode_fn();
   if (fn == nullptr) return false;
@@ -89,8 +92,8 @@ bool make_map_dq_wide(CUtensorMap* m, void* ptr, long long BH, long long NQ, int
   cuuint64_t strides[2] = {cuuint64_t(dg) * 4, cuuint64_t(NQ) * dg * 4};
   cuuint32_t box[3] = {32, 32, 1};
   cuuint32_t es[3] = {1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, es,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  CUresult r = fn(m, int32 ? CU_TENSOR_MAP_DATA_TYPE_INT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims,
+                  strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   *box_cols = 32;
   return r == CUDA_SUCCESS;
@@ -304,13 +307,12 @@ int streamkl_bwd_gqa(const void* q1, const void* k1, const void* q2, const void*
   if (!st) return STREAMKL_CUDA_ERROR;
   const int gg = H / hkg;  // query heads per key head of dk
   skl::BwdArgs a{B * H, NQ, NK, causal, mode, dg, H / HK1, H / HK2, -1, scale1, scale2, kl, lse1, lse2, dkl, dq,
-                 dk, st, 1};
+                 dk, st};
   const int t1 = tile_dim(d1), t2 = tile_dim(d2);
   if (t1 > 128 || t2 > 128) {
     // a head above 128: dK by key tiles (the launches of a key-head group in
     // order, the first storing), then dQ by query tiles; no atomics, so both
     // values of `deterministic` take this path
-    a.write_dq = 0;
     for (int j = 0; j < gg; ++j) {
       a.hsel = gg > 1 ? j : -1;
       if (skl::launch_bwd_wide_pass0(m, t1, t2, a, cs) != 0) return STREAMKL_CUDA_ERROR;
@@ -326,15 +328,32 @@ int streamkl_bwd_gqa(const void* q1, const void* k1, const void* q2, const void*
     if (gg > 1 && cudaMemsetAsync(dk, 0, dk_bytes, cs) != cudaSuccess) return STREAMKL_CUDA_ERROR;
     return as_status(skl::launch_bwd_fused(m, t1, t2, a, cs));
   }
-  // deterministic: dK from one launch per query head of each group, in order
-  // (the first stores, the others add), then dQ from its own kernel
-  a.write_dq = 0;
-  for (int j = 0; j < gg; ++j) {
+  // deterministic: the same fused kernel with dQ summed in int32 fixed
+  // point (exact in any order), one launch per query head of each key-head
+  // group in order (the first stores a shared key head's dK, the others
+  // add), then the int32 sums converted to fp32 in place.  The per-key-head
+  // bound on |K| lives in a stream-ordered scratch block of 4 bytes a head.
+  const size_t dq_bytes = size_t(B) * H * NQ * dg * 4;
+  const int kg_heads = B * hkg;
+  if (!make_map_dq_wide(&m.dqw, dq, (long long)B * H, NQ, dg, &a.dq_box, true)) return STREAMKL_CUDA_ERROR;
+  if (cudaMemsetAsync(dq, 0, dq_bytes, cs) != cudaSuccess) return STREAMKL_CUDA_ERROR;
+  unsigned* kmax = nullptr;
+  if (cudaMallocAsync(reinterpret_cast<void**>(&kmax), size_t(kg_heads) * sizeof(unsigned), cs) != cudaSuccess)
+    return STREAMKL_CUDA_ERROR;
+  int rc = STREAMKL_OK;
+  if (cudaMemsetAsync(kmax, 0, size_t(kg_heads) * sizeof(unsigned), cs) != cudaSuccess ||
+      skl::launch_kmax(mode == STREAMKL_GRAD_P2 ? k2 : k1, kg_heads, NK, dg, kmax, cs) != 0)
+    rc = STREAMKL_CUDA_ERROR;
+  a.dq_fixed = 1;
+  a.kmax = kmax;
+  a.ln_nk = std::log(float(NK));
+  for (int j = 0; j < gg && rc == STREAMKL_OK; ++j) {
     a.hsel = gg > 1 ? j : -1;
-    if (skl::launch_bwd_fused(m, t1, t2, a, cs) != 0) return STREAMKL_CUDA_ERROR;
+    if (skl::launch_bwd_fused(m, t1, t2, a, cs) != 0) rc = STREAMKL_CUDA_ERROR;
   }
-  a.hsel = -1;
-  return as_status(skl::launch_bwd_dq(m, t1, t2, a, cs));
+  if (rc == STREAMKL_OK && skl::launch_dq_fixed_finish(a, cs) != 0) rc = STREAMKL_CUDA_ERROR;
+  if (cudaFreeAsync(kmax, cs) != cudaSuccess) rc = STREAMKL_CUDA_ERROR;
+  return rc;
 }
 
 int streamkl_bwd_scaled(const void* q1, const void* k1, const void* q2, const void* k2, int B, int H,
@@ -386,7 +405,7 @@ int streamkl_bwd_both(const void* q1, const void* k1, const void* q2, const void
   if (cudaMemsetAsync(dq1, 0, dq_bytes, cs) != cudaSuccess || cudaMemsetAsync(dq2, 0, dq_bytes, cs) != cudaSuccess)
     return STREAMKL_CUDA_ERROR;
   skl::BwdArgs a{B * H, NQ, NK, causal, STREAMKL_GRAD_P2, d1, 1, 1, -1, scale1, scale2, kl, lse1, lse2,
-                 dkl, dq1, dk1, st, 1, dq2, dk2};
+                 dkl, dq1, dk1, st, dq2, dk2};
   return as_status(skl::launch_bwd_both(m, tile_dim(d1), a, cs));
 }
 

@@ -38,9 +38,10 @@
 //              shared by several query heads: put_dk4)
 // TMEM: S1 [0,128), S2 [128,256), dK [256, 256+dg), dQ [384, 384+dg).
 //
-// dQ-only kernel (deterministic two-pass mode): one CTA per query tile walks
-// the key tiles, thread = query row, dQ accumulates in TMEM and is stored
-// once; dK then comes from the fused kernel with its dQ product switched off.
+// Deterministic mode: the same kernel, with each dQ contribution scaled by
+// a per-row power of two and rounded to int32 before the reduce-add, so the
+// sums are exact in whatever order they land (bound, scale and the final
+// conversion: dq_fixed_exp, dq_fixed.cu); dK is written by one CTA anyway.
 #include "bwd_common.cuh"
 #include "kernels.cuh"
 #include "ptx.cuh"
@@ -133,7 +134,7 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
       uint32_t count = 1;  // TMA transaction barriers and tcgen05.commit targets
       if (b == L::B_SFREE || b == L::B_DSFULL) count = 8;  // one per dS warp
       if (b == L::B_DQEMPTY) count = 4;                    // one per epilogue warp
-      if (b == L::B_DSEMPTY) count = (L::kSplitIssue && a.write_dq) ? 2 : 1;  // dK (and dQ) issuers
+      if (b == L::B_DSEMPTY) count = L::kSplitIssue ? 2 : 1;  // dK (and dQ) issuers
       if (b == L::B_DONE) count = L::kSplitIssue ? 3 : 2;  // one per MMA issuer
       mbar_init(bar(b), count);
     }
@@ -235,7 +236,7 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
             mma_bf16_ss(1u, t_dk, sdesc_add(dsm, kk * 2048), sdesc_add(qgn, TG::off_n(kk)), id_dk,
                         (t > 0 || kk > 0) ? 1u : 0u);
           mma_commit(1u, bar(L::B_QGEMPTY0 + (t & 1)));  // Q_g(t) may be reloaded
-          if (kDq && a.write_dq) {
+          if (kDq) {
             // dK and the Q_g release above did not wait for the dQ accumulator
             if (!mbar_wait_polled(bar(L::B_DQEMPTY), (t & 1) ^ 1, ctl)) break;
             tc_fence_after();
@@ -245,7 +246,7 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
                           sdesc_add(kgn, TG::off_n(kk)), id_dq, kk > 0 ? 1u : 0u);
           }
           mma_commit(1u, bar(L::B_DSEMPTY));
-          if (kDq && a.write_dq) mma_commit(1u, bar(L::B_DQFULL));
+          if (kDq) mma_commit(1u, bar(L::B_DQFULL));
         }
       }
       if (n > 0 && t == n && !*abort_flag) mma_commit(1u, bar(L::B_DKFULL));
@@ -258,7 +259,7 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
         constexpr uint32_t id_dq = idesc_bf16(128, DG, 0, 1);  // A = dS K-major, B = K_g N-major
         const uint64_t dsk = sdesc_sw128(sb + L::oDS, 16, 1024);  // dS, K-major
         const uint64_t kgn = TG::desc_n(sb + (kP2 ? L::oK2 : L::oK1));
-        if (a.write_dq && n > 0 && mbar_wait_polled(bar(L::B_KFULL), 0, ctl)) {
+        if (n > 0 && mbar_wait_polled(bar(L::B_KFULL), 0, ctl)) {
           for (int t = 0; t < n; ++t) {
             if (!mbar_wait_polled(bar(L::B_DSFULL), t & 1, ctl)) break;
             wait_s_queued(s_queued, t + 1 < n ? t + 2 : 0);
@@ -337,7 +338,7 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
     const int w4 = warp - 8;
     const int row = w4 * 32 + lane;
     const uint32_t lane_off = uint32_t(w4 * 32) << 16;
-    if (a.write_dq) {
+    {
       // This thread's dQ row (DG fp32) is read from TMEM and the accumulator
       // released before most of it is staged, so the next dQ product rarely
       // waits for the reduce-adds.  The row leaves in boxes of [32 rows][32 fp32]
@@ -345,16 +346,41 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
       // full 128-byte line per row) through kDqBoxes staging boxes per warp,
       // each a bulk tensor reduce-add into the fp32 dQ.  For dg = 16 the map
       // has boxes of [32 rows][16 fp32] with the 64-byte swizzle instead
-      // (chunk c of row r at c ^ ((r / 2) % 4)).
+      // (chunk c of row r at c ^ ((r / 2) % 4)).  In the deterministic mode
+      // the row is scaled by its 2^e and rounded to int32 first, and the map
+      // adds int32 (dq_fixed_exp).
       constexpr int kChunks = DG / 32;
       const bool wide = a.dq_box == 32;
       const uint32_t stage = sb + L::oStage + w4 * (kDqBoxes * kDqBoxBytes);
       int nred = 0;
       if (lane == 0) tma_prefetch_desc(&tdq);
+      const bool fixed = a.dq_fixed != 0;
+      const float sg = kP2 ? a.scale2 : a.scale1;
+      const float kmax = fixed ? __uint_as_float(a.kmax[bh / gg] << 16) : 0.f;
+      // fixed point: dKL (and KL) of this thread's row in query tile i, loaded a tile ahead
+      float dkl_nx = 0.f, kl_nx = 0.f;
+      auto load_row = [&](int i) {
+        const int qi = (qt_lo + i) * kTile + row;
+        if (fixed && qi < a.NQ && SKL_CHECK(a.status, bh < a.BH)) {
+          const size_t idx = size_t(bh) * a.NQ + qi;
+          dkl_nx = a.dkl[idx];
+          kl_nx = kP2 ? 0.f : a.kl[idx];
+        }
+      };
+      // x 2^e as two exact multiplies (2^e itself need not be a float)
+      auto to_fixed = [&](uint32_t (&x)[32], float sc1, float sc2) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          x[j] = uint32_t(__float2int_rn(__fmul_rn(__fmul_rn(__uint_as_float(x[j]), sc1), sc2)));
+      };
+      if (n > 0) load_row(0);
       for (int i = 0; i < n; ++i) {
         if (!mbar_wait_warp(bar(L::B_DQFULL), i & 1, ctl)) break;
         tc_fence_after();
         const int r0 = (qt_lo + i) * kTile + w4 * 32;  // first query row of this warp
+        const int e = fixed ? dq_fixed_exp(MODE, sg, dkl_nx, kl_nx, kmax, a.ln_nk) : 0;
+        const float sc1 = scale_pow2(1.f, min(e, 126)), sc2 = scale_pow2(1.f, max(e - 126, 0));
+        if (i + 1 < n) load_row(i + 1);
         uint32_t v[kChunks][32];
         // one box of the dQ tile: row `lane` of this warp's 32 rows, columns [32 h, 32 h + 32)
         auto put_box = [&](int h) {
@@ -393,6 +419,7 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
         if constexpr (kChunks == 4) {
           tmem_ld2x32(t_dq + lane_off, t_dq + lane_off + 32, v[0], v[1]);
           tmem_ld32(t_dq + lane_off + 64, v[2]);
+          if (fixed) to_fixed(v[0], sc1, sc2);
           put_box(0);
           tmem_ld32(t_dq + lane_off + 96, v[3]);
         } else if constexpr (kChunks == 2) {
@@ -404,7 +431,10 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(L::B_DQEMPTY));
 #pragma unroll
-        for (int h = kChunks == 4 ? 1 : 0; h < kChunks; ++h) put_box(h);
+        for (int h = kChunks == 4 ? 1 : 0; h < kChunks; ++h) {
+          if (fixed) to_fixed(v[h], sc1, sc2);
+          put_box(h);
+        }
       }
       if (lane == 0) bulk_wait_all();  // every reduce has landed before the CTA exits
     }
@@ -443,224 +473,6 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
   }
 }
 
-// ------------------------------------------------------------------------
-// dQ-only kernel for the deterministic mode.  One CTA per 128-row query tile
-// streams the visible key tiles (like the forward kernel):
-//   warp 4     TMA: Q1, Q2 once; K1_j, K2_j into a two-stage ring
-//   warp 5     MMA: S1 = Q1 K1_j^T, S2 = Q2 K2_j^T, then dQ += dS_j K_g,j
-//              (dS K-major from shared memory, K_g N-major); S of tile j+1
-//              is issued before the dQ product of tile j
-//   warps 0-3  thread = query row: dS_j from S and the row's own
-//              LSE1/LSE2/dKL/KL (held in registers), stored bf16 as
-//              [row][key] with the 128-byte swizzle; at the end dQ is read
-//              from TMEM and stored once (no atomics: bitwise reproducible)
-// Shared memory: [K stages][Q1][Q2][dS][barriers]; TMEM: S1 [0,128),
-// S2 [128,256), dQ [256, 256+dg).
-constexpr int kDqThreads = 192;
-
-template <int D1, int D2, int MODE>
-struct DqLayout {
-  static constexpr int DG = MODE == STREAMKL_GRAD_P2 ? D2 : D1;
-  static constexpr uint32_t kQ1 = kTile * D1 * 2, kQ2 = kTile * D2 * 2;
-  static constexpr uint32_t kK1 = kTile * D1 * 2, kK2 = kTile * D2 * 2;
-  static constexpr uint32_t kStage = kK1 + kK2;
-  static constexpr int kStages = 2;
-  static constexpr uint32_t oK = 0, oQ1 = kStages * kStage, oQ2 = oQ1 + kQ1, oDS = oQ2 + kQ2;
-  static constexpr uint32_t oBar = oDS + kTile * kTile * 2;
-  enum { B_QFULL, B_KFULL0, B_KFULL1, B_KEMPTY0, B_KEMPTY1, B_SFULL, B_SFREE, B_DSFULL, B_DSEMPTY,
-         B_DQFULL, B_DONE, kNumBars };
-  static constexpr uint32_t oMisc = oBar + kNumBars * 8;
-  static constexpr uint32_t kBytes = oMisc + 16;
-  static constexpr uint32_t kAlloc = kBytes + 1024;
-  static_assert(kAlloc <= 232448, "over the 227 KB shared memory limit");
-};
-
-template <int D1, int D2, int MODE>
-__global__ void __launch_bounds__(kDqThreads, 1)
-    bwd_dq_kernel(const __grid_constant__ CUtensorMap tq1, const __grid_constant__ CUtensorMap tk1,
-                  const __grid_constant__ CUtensorMap tq2, const __grid_constant__ CUtensorMap tk2,
-                  const BwdArgs a) {
-  using L = DqLayout<D1, D2, MODE>;
-  constexpr int DG = L::DG;
-  using T1 = OpTile<D1>;
-  using T2 = OpTile<D2>;
-  using TG = OpTile<DG>;
-  constexpr bool kP2 = MODE == STREAMKL_GRAD_P2;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
-  const uint32_t sb = smem_u32(smem);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  const int nqt = (a.NQ + kTile - 1) / kTile;
-  const int qt = a.causal ? (nqt - 1 - int(blockIdx.x)) : int(blockIdx.x);
-  const int bh = blockIdx.y;
-  const int q0 = qt * kTile;
-  const int off = a.NK - a.NQ;
-  const int kend = a.causal ? min(q0 + kTile, a.NQ) + off : a.NK;
-  const int nkt = (kend + kTile - 1) / kTile;
-
-  auto bar = [&](int id) { return sb + L::oBar + 8u * id; };
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::oMisc);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::oMisc + 4);
-  const Ctl ctl{abort_flag, a.status};
-
-  if (threadIdx.x == 0) {
-    for (int b = 0; b < L::kNumBars; ++b)
-      mbar_init(bar(b), (b == L::B_SFREE || b == L::B_DSFULL) ? 4u : 1u);
-    *abort_flag = 0;
-    fence_barrier_init();
-  }
-  if (warp == 5) {
-    tmem_alloc(smem_u32(tmem_slot), 512);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  const uint32_t t_s1 = tmem, t_s2 = tmem + 128, t_dq = tmem + 256;
-
-  if (warp == 4) {
-    // ---------------------------------------------------------------- TMA producer
-    if (lane == 0) {
-      mbar_arrive_expect_tx(bar(L::B_QFULL), L::kQ1 + L::kQ2);
-      T1::load(sb + L::oQ1, &tq1, bar(L::B_QFULL), q0, bh);
-      T2::load(sb + L::oQ2, &tq2, bar(L::B_QFULL), q0, bh);
-      int issued = 0;
-      for (int j = 0; j < nkt; ++j) {
-        const int s = j & 1;
-        if (!mbar_wait_polled(bar(L::B_KEMPTY0 + s), ((j >> 1) & 1) ^ 1, ctl)) break;
-        mbar_arrive_expect_tx(bar(L::B_KFULL0 + s), L::kStage);
-        const uint32_t st = sb + L::oK + s * L::kStage;
-        T1::load(st, &tk1, bar(L::B_KFULL0 + s), j * kTile, bh / a.g1);
-        T2::load(st + L::kK1, &tk2, bar(L::B_KFULL0 + s), j * kTile, bh / a.g2);
-        issued = j + 1;
-      }
-      if (*abort_flag) {
-        mbar_drain(bar(L::B_QFULL), 0, 200000000ull);
-        for (int j = issued > 2 ? issued - 2 : 0; j < issued; ++j)
-          mbar_drain(bar(L::B_KFULL0 + (j & 1)), (j >> 1) & 1, 200000000ull);
-      }
-    }
-  } else if (warp == 5) {
-    // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t id_s = idesc_bf16(128, 128, 0, 0);
-      constexpr uint32_t id_dq = idesc_bf16(128, DG, 0, 1);  // A = dS K-major, B = K_g N-major
-      auto dq_product = [&](int t) -> bool {
-        if (!mbar_wait_polled(bar(L::B_DSFULL), t & 1, ctl)) return false;
-        tc_fence_after();
-        const uint32_t kg = sb + L::oK + (t & 1) * L::kStage + (kP2 ? L::kK1 : 0);
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint32_t ao = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
-          mma_bf16_ss(1u, t_dq, sdesc_sw128(sb + L::oDS + ao, 16, 1024),
-                      TG::desc_n(kg + TG::off_n(kk)), id_dq, (t > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(1u, bar(L::B_DSEMPTY));
-        mma_commit(1u, bar(L::B_KEMPTY0 + (t & 1)));
-        return true;
-      };
-      bool ok = mbar_wait_polled(bar(L::B_QFULL), 0, ctl);
-      for (int j = 0; ok && j < nkt; ++j) {
-        const int s = j & 1;
-        if (!mbar_wait_polled(bar(L::B_KFULL0 + s), (j >> 1) & 1, ctl)) break;
-        if (!mbar_wait_polled(bar(L::B_SFREE), (j & 1) ^ 1, ctl)) break;
-        tc_fence_after();
-        const uint32_t k1s = sb + L::oK + s * L::kStage, k2s = k1s + L::kK1;
-#pragma unroll
-        for (int kk = 0; kk < D1 / 16; ++kk) {
-          const uint32_t o = T1::off_k(kk);
-          mma_bf16_ss(1u, t_s1, T1::desc_k(sb + L::oQ1 + o), T1::desc_k(k1s + o), id_s, kk > 0);
-        }
-#pragma unroll
-        for (int kk = 0; kk < D2 / 16; ++kk) {
-          const uint32_t o = T2::off_k(kk);
-          mma_bf16_ss(1u, t_s2, T2::desc_k(sb + L::oQ2 + o), T2::desc_k(k2s + o), id_s, kk > 0);
-        }
-        mma_commit(1u, bar(L::B_SFULL));
-        if (j > 0 && !dq_product(j - 1)) {
-          ok = false;
-          break;
-        }
-      }
-      if (ok && nkt > 0 && !*abort_flag && dq_product(nkt - 1)) mma_commit(1u, bar(L::B_DQFULL));
-      mma_commit(1u, bar(L::B_DONE));
-      mbar_drain(bar(L::B_DONE), 0, 1000000000ull);
-    }
-  } else {
-    // ---------------------------------------------------------------- dS (thread = query row)
-    const int row = warp * 32 + lane;
-    const int qi = q0 + row;
-    const float c1 = a.scale1 * kLog2e, c2 = a.scale2 * kLog2e, nr = -a.scale2 / a.scale1;
-    const uint32_t lane_off = uint32_t(warp * 32) << 16;
-    const int lim = a.causal ? min(qi + off, a.NK - 1) : a.NK - 1;  // last visible key
-    float na = -INFINITY, nb = kP2 ? -INFINITY : 0.f, w = 0.f;
-    if (qi < a.NQ) {
-      const size_t idx = size_t(bh) * a.NQ + qi;
-      const float l1 = a.lse1[idx];
-      na = -l1 * kLog2e;
-      w = a.dkl[idx];
-      nb = kP2 ? -a.lse2[idx] * kLog2e : -(l1 - a.lse2[idx] + a.kl[idx]);
-    }
-    const float ws = (kP2 ? a.scale2 : a.scale1) * w;  // the gradient side's s folded into dS
-    const uint64_t C1 = f2(c1, c1), C2 = f2(c2, c2), S1 = f2(a.scale1, a.scale1), NR = f2(nr, nr);
-    const uint64_t NA = f2(na, na), NB = f2(nb, nb), WW = f2(ws, ws);
-    for (int j = 0; j < nkt; ++j) {
-      if (!mbar_wait_warp(bar(L::B_SFULL), j & 1, ctl)) break;
-      tc_fence_after();
-      const int k0 = j * kTile;
-      const bool need_mask = (k0 + kTile > a.NK) || (a.causal && k0 + kTile - 1 > q0 + off);
-      const int lim_rel = lim - k0;
-      uint32_t dsr[64];
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        uint32_t x1[32], x2[32];
-        tmem_ld2x32(t_s1 + lane_off + ch * 32, t_s2 + lane_off + ch * 32, x1, x2);
-        if (ch == 3) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(L::B_SFREE));
-        }
-        if (need_mask)
-          ds_chunk_row<MODE, true>(x1, x2, C1, C2, S1, NR, NA, NB, WW, lim_rel - ch * 32, dsr + ch * 16);
-        else
-          ds_chunk_row<MODE, false>(x1, x2, C1, C2, S1, NR, NA, NB, WW, 0, dsr + ch * 16);
-      }
-      if (!mbar_wait_warp(bar(L::B_DSEMPTY), (j & 1) ^ 1, ctl)) break;
-      store_row_sw128(sb + L::oDS, row, dsr);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(L::B_DSFULL));
-    }
-    if (nkt > 0 && mbar_wait_warp(bar(L::B_DQFULL), 0, ctl)) {
-      tc_fence_after();
-      float* dst = a.dq + (size_t(bh) * a.NQ + qi) * a.dg;
-#pragma unroll
-      for (int ch = 0; ch < DG / 32; ++ch) {
-        uint32_t v[32];
-        tmem_ld32(t_dq + lane_off + ch * 32, v);
-        if (qi < a.NQ && SKL_CHECK(a.status, bh < a.BH && a.dg <= DG)) {
-#pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            if (ch * 32 + e < a.dg)
-              *reinterpret_cast<float4*>(dst + ch * 32 + e) =
-                  make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]), __uint_as_float(v[e + 2]),
-                              __uint_as_float(v[e + 3]));
-        }
-      }
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 5) {
-    tc_fence_after();
-    tmem_dealloc(tmem, 512);
-  }
-}
-
 template <int D1, int D2, int MODE>
 static int launch_fused_t(const TMaps& m, const BwdArgs& a, cudaStream_t st) {
   using L = BwdLayout<D1, D2, MODE>;
@@ -670,17 +482,6 @@ static int launch_fused_t(const TMaps& m, const BwdArgs& a, cudaStream_t st) {
   const int gg = MODE == STREAMKL_GRAD_P2 ? a.g2 : a.g1;
   dim3 grid((a.NK + kTile - 1) / kTile, a.hsel < 0 ? a.BH : a.BH / gg);
   kern<<<grid, L::kThreads, L::kAlloc, st>>>(m.q1, m.k1, m.q2, m.k2, m.dqw, a);
-  return cudaGetLastError();
-}
-
-template <int D1, int D2, int MODE>
-static int launch_dq_t(const TMaps& m, const BwdArgs& a, cudaStream_t st) {
-  using L = DqLayout<D1, D2, MODE>;
-  auto kern = bwd_dq_kernel<D1, D2, MODE>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
-  if (e != cudaSuccess) return e;
-  dim3 grid((a.NQ + kTile - 1) / kTile, a.BH);
-  kern<<<grid, kDqThreads, L::kAlloc, st>>>(m.q1, m.k1, m.q2, m.k2, a);
   return cudaGetLastError();
 }
 
@@ -697,10 +498,6 @@ static int launch_dq_t(const TMaps& m, const BwdArgs& a, cudaStream_t st) {
 
 int launch_bwd_fused(const TMaps& m, int d1, int d2, const BwdArgs& a, cudaStream_t st) {
   SKL_DISPATCH(launch_fused_t);
-}
-
-int launch_bwd_dq(const TMaps& m, int d1, int d2, const BwdArgs& a, cudaStream_t st) {
-  SKL_DISPATCH(launch_dq_t);
 }
 
 }  // namespace skl

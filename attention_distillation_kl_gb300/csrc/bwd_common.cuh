@@ -139,4 +139,50 @@ __device__ __forceinline__ void ds_chunk_row_both(const uint32_t (&x1u)[32], con
   }
 }
 
+// Deterministic dQ in fixed point.  Every contribution to a dQ row is
+// scaled by 2^e (e per query row) and rounded to an int32; int32 sums are
+// exact whatever the order in which the reduce-adds land, and a last pass
+// divides by 2^e again.  e comes from a bound on |dQ_id| that holds for
+// every partial sum of the row:
+//   |dQ_id| <= s dKL_i kmax C_i,  kmax = max |K_g| of the key head,
+//   C_i = sum_k |dS_ik| / dKL_i, which is
+//     mode P2: sum_k |P2_ik - P1_ik| <= 2;
+//     mode P1: sum_k P1_ik |r_ik - KL_i| <= 2 H(P1_i) + 2 KL_i
+//              <= 2 ln NK + 2 KL_i
+//   (r = ln P1 - ln P2, and -ln P2 >= 0: sum P1 (-ln P2) = H(P1) + KL).
+// The bound takes slack for the bf16 rounding of dS and for the recomputed
+// statistics; 2^e times it stays below 2^29, a factor of 4 below the int32
+// limit, which also covers the roundings (half a unit per key tile).  So
+// each key tile's contribution is rounded to 2^-30 of the row's bound or
+// better, for any finite nonzero bound (e spans about [-100, 180]).
+__device__ __forceinline__ int dq_fixed_exp(int mode, float sg, float dkl, float kl, float kmax,
+                                            float ln_nk) {
+  // explicitly rounded operations: the fused kernel and the final pass must
+  // reach the same e for a row, whatever the compiler contracts elsewhere
+  const float c = mode == STREAMKL_GRAD_P2
+                      ? 2.f
+                      : __fadd_rn(__fadd_rn(__fmul_rn(2.f, ln_nk), __fmul_rn(2.f, fmaxf(kl, 0.f))), 1.f);
+  float bound = __fmul_rn(__fmul_rn(__fmul_rn(__fmul_rn(sg, fabsf(dkl)), kmax), c), 1.0078125f);
+  if (!(bound > 0.f && bound <= 3.0e38f)) return 0;  // zero (nothing to add) or not finite
+  int shift = 0;
+  if (bound < 1.0e-37f) {  // below the normal range: bring it up exactly
+    bound = __fmul_rn(bound, 18446744073709551616.f);  // 2^64
+    shift = 64;
+  }
+  const int E = int((__float_as_uint(bound) >> 23) & 255u);  // bound < 2^(E - 126)
+  return 155 - E + shift;
+}
+
+// x 2^e for |e| up to 252, in two exact steps when 2^e is not a float.
+__device__ __forceinline__ float scale_pow2(float x, int e) {
+  if (e > 126) {
+    x = __fmul_rn(x, __uint_as_float(253u << 23));  // 2^126
+    e -= 126;
+  } else if (e < -126) {
+    x = __fmul_rn(x, __uint_as_float(1u << 23));  // 2^-126
+    e += 126;
+  }
+  return __fmul_rn(x, __uint_as_float(uint32_t(e + 127) << 23));
+}
+
 }  // namespace skl

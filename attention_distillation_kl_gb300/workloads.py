@@ -130,13 +130,20 @@ def generate_dkl(w: Workload, kind: str = "ones", seed: int = 0) -> torch.Tensor
     """Upstream gradient dL/dKL, fp32 [B, H, NQ]: all ones (the gradient of
     sum(KL)), U(0.5, 1.5) to exercise per-row indexing ("uniform"), or
     U(-1.5, 1.5) with every fifth row exactly 0 ("signed": a loss that weights
-    some rows negatively or not at all)."""
+    some rows negatively or not at all), or magnitudes 10^U(-40, 30) with random
+    signs and every seventh row 0 ("wide": per-row weights over the whole fp32
+    range, subnormals included)."""
     if kind == "ones":
         return torch.ones((w.B, w.H, w.NQ), dtype=torch.float32)
     g = np.random.Generator(np.random.PCG64([w.seed, 7919, seed]))
     if kind == "signed":
         v = g.uniform(-1.5, 1.5, size=(w.B, w.H, w.NQ))
         v[..., ::5] = 0.0
+        return torch.from_numpy(v.astype(np.float32))
+    if kind == "wide":
+        shape = (w.B, w.H, w.NQ)
+        v = np.power(10.0, g.uniform(-40.0, 30.0, size=shape)) * np.where(g.random(shape) < 0.5, -1.0, 1.0)
+        v[..., ::7] = 0.0
         return torch.from_numpy(v.astype(np.float32))
     return torch.from_numpy(g.uniform(0.5, 1.5, size=(w.B, w.H, w.NQ)).astype(np.float32))
 
