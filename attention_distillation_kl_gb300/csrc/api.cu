@@ -60,18 +60,16 @@ bool make_map(CUtensorMap* m, const void* ptr, long long BH, long long N, int d)
   return r == CUDA_SUCCESS;
 }
 
-// dQ [BH][NQ][dg] fp32 (or int32: the deterministic backward's fixed-point
-// sums) as a 3-D tensor: boxes of 16 elements x 32 rows x 1, 64-byte
-// swizzle, the target of the backward's bulk reduce-adds.
-bool make_map_dq(CUtensorMap* m, void* ptr, long long BH, long long NQ, int dg, bool int32 = false) {
+// dQ [BH][NQ][dg] fp32 as a 3-D tensor: boxes of 16 elements x 32 rows x 1,
+// 64-byte swizzle, the target of the backward's bulk reduce-adds.
+bool make_map_dq(CUtensorMap* m, void* ptr, long long BH, long long NQ, int dg) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[3] = {cuuint64_t(dg), cuuint64_t(NQ), cuuint64_t(BH)};
   cuuint64_t strides[2] = {cuuint64_t(dg) * 4, cuuint64_t(NQ) * dg * 4};
   cuuint32_t box[3] = {16, 32, 1};
   cuuint32_t es[3] = {1, 1, 1};
-  CUresult r = fn(m, int32 ? CU_TENSOR_MAP_DATA_TYPE_INT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims,
-                  strides, box, es,
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -80,11 +78,10 @@ bool make_map_dq(CUtensorMap* m, void* ptr, long long BH, long long NQ, int dg, 
 // The fused backward's dQ target: boxes of 32 fp32 x 32 rows with the
 // 128-byte swizzle (one full 128-byte line per row and box: fewer, larger
 // reduce operations than 64-byte pieces), or the 16-wide map for dg = 16.
-bool make_map_dq_wide(CUtensorMap* m, void* ptr, long long BH, long long NQ, int dg, int* box_cols,
-                      bool int32 = false) {
+bool make_map_dq_wide(CUtensorMap* m, void* ptr, long long BH, long long NQ, int dg, int* box_cols) {
   if (dg < 32) {
     *box_cols = 16;
-    return make_map_dq(m, ptr, BH, NQ, dg, int32);
+    return make_map_dq(m, ptr, BH, NQ, dg);
   }
   auto fn = encode_fn();
   if (fn == nullptr) return false;
@@ -92,8 +89,8 @@ bool make_map_dq_wide(CUtensorMap* m, void* ptr, long long BH, long long NQ, int
   cuuint64_t strides[2] = {cuuint64_t(dg) * 4, cuuint64_t(NQ) * dg * 4};
   cuuint32_t box[3] = {32, 32, 1};
   cuuint32_t es[3] = {1, 1, 1};
-  CUresult r = fn(m, int32 ? CU_TENSOR_MAP_DATA_TYPE_INT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims,
-                  strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   *box_cols = 32;
   return r == CUDA_SUCCESS;
@@ -328,14 +325,14 @@ int streamkl_bwd_gqa(const void* q1, const void* k1, const void* q2, const void*
     if (gg > 1 && cudaMemsetAsync(dk, 0, dk_bytes, cs) != cudaSuccess) return STREAMKL_CUDA_ERROR;
     return as_status(skl::launch_bwd_fused(m, t1, t2, a, cs));
   }
-  // deterministic: the same fused kernel with dQ summed in int32 fixed
-  // point (exact in any order), one launch per query head of each key-head
-  // group in order (the first stores a shared key head's dK, the others
-  // add), then the int32 sums converted to fp32 in place.  The per-key-head
-  // bound on |K| lives in a stream-ordered scratch block of 4 bytes a head.
+  // deterministic: the same fused kernel with every dQ contribution rounded
+  // to its row's grid (fp32 sums exact in any order), one launch per query
+  // head of each key-head group in order (the first stores a shared key
+  // head's dK, the others add).  The per-key-head bound on |K| lives in a
+  // stream-ordered scratch block of 4 bytes a head.
   const size_t dq_bytes = size_t(B) * H * NQ * dg * 4;
   const int kg_heads = B * hkg;
-  if (!make_map_dq_wide(&m.dqw, dq, (long long)B * H, NQ, dg, &a.dq_box, true)) return STREAMKL_CUDA_ERROR;
+  if (!make_map_dq_wide(&m.dqw, dq, (long long)B * H, NQ, dg, &a.dq_box)) return STREAMKL_CUDA_ERROR;
   if (cudaMemsetAsync(dq, 0, dq_bytes, cs) != cudaSuccess) return STREAMKL_CUDA_ERROR;
   unsigned* kmax = nullptr;
   if (cudaMallocAsync(reinterpret_cast<void**>(&kmax), size_t(kg_heads) * sizeof(unsigned), cs) != cudaSuccess)
@@ -346,12 +343,10 @@ int streamkl_bwd_gqa(const void* q1, const void* k1, const void* q2, const void*
     rc = STREAMKL_CUDA_ERROR;
   a.dq_fixed = 1;
   a.kmax = kmax;
-  a.ln_nk = std::log(float(NK));
   for (int j = 0; j < gg && rc == STREAMKL_OK; ++j) {
     a.hsel = gg > 1 ? j : -1;
     if (skl::launch_bwd_fused(m, t1, t2, a, cs) != 0) rc = STREAMKL_CUDA_ERROR;
   }
-  if (rc == STREAMKL_OK && skl::launch_dq_fixed_finish(a, cs) != 0) rc = STREAMKL_CUDA_ERROR;
   if (cudaFreeAsync(kmax, cs) != cudaSuccess) rc = STREAMKL_CUDA_ERROR;
   return rc;
 }

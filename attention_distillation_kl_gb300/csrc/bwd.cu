@@ -38,10 +38,11 @@
 //              shared by several query heads: put_dk4)
 // TMEM: S1 [0,128), S2 [128,256), dK [256, 256+dg), dQ [384, 384+dg).
 //
-// Deterministic mode: the same kernel, with each dQ contribution scaled by
-// a per-row power of two and rounded to int32 before the reduce-add, so the
-// sums are exact in whatever order they land (bound, scale and the final
-// conversion: dq_fixed_exp, dq_fixed.cu); dK is written by one CTA anyway.
+// Deterministic mode: the same kernel, with each dQ contribution rounded to
+// a per-row grid of 2^-e before the reduce-add, fine enough to keep the row's
+// precision and coarse enough that the fp32 sums are exact in whatever
+// order they land (bound and grid: dq_fixed_exp; max |K| per key head:
+// dq_fixed.cu); dK is written by one CTA anyway.
 #include "bwd_common.cuh"
 #include "kernels.cuh"
 #include "ptx.cuh"
@@ -347,8 +348,8 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
       // each a bulk tensor reduce-add into the fp32 dQ.  For dg = 16 the map
       // has boxes of [32 rows][16 fp32] with the 64-byte swizzle instead
       // (chunk c of row r at c ^ ((r / 2) % 4)).  In the deterministic mode
-      // the row is scaled by its 2^e and rounded to int32 first, and the map
-      // adds int32 (dq_fixed_exp).
+      // the row is first rounded to its grid of 2^-e (dq_fixed_exp), so the
+      // fp32 sums are exact in any order.
       constexpr int kChunks = DG / 32;
       const bool wide = a.dq_box == 32;
       const uint32_t stage = sb + L::oStage + w4 * (kDqBoxes * kDqBoxBytes);
@@ -357,29 +358,35 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
       const bool fixed = a.dq_fixed != 0;
       const float sg = kP2 ? a.scale2 : a.scale1;
       const float kmax = fixed ? __uint_as_float(a.kmax[bh / gg] << 16) : 0.f;
-      // fixed point: dKL (and KL) of this thread's row in query tile i, loaded a tile ahead
+      // deterministic mode: dKL and KL of this thread's row in query tile i
+      // (the row's grid), loaded a tile ahead
       float dkl_nx = 0.f, kl_nx = 0.f;
       auto load_row = [&](int i) {
         const int qi = (qt_lo + i) * kTile + row;
         if (fixed && qi < a.NQ && SKL_CHECK(a.status, bh < a.BH)) {
           const size_t idx = size_t(bh) * a.NQ + qi;
           dkl_nx = a.dkl[idx];
-          kl_nx = kP2 ? 0.f : a.kl[idx];
+          kl_nx = a.kl[idx];
         }
       };
-      // x 2^e as two exact multiplies (2^e itself need not be a float)
-      auto to_fixed = [&](uint32_t (&x)[32], float sc1, float sc2) {
+      // each value rounded to the row's grid of 2^-e: (x + 1.5 * 2^(23 - e))
+      // - 1.5 * 2^(23 - e), two values at a time on the FMA pipe
+      auto to_fixed = [&](uint32_t (&x)[32], uint64_t ME) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          x[j] = uint32_t(__float2int_rn(__fmul_rn(__fmul_rn(__uint_as_float(x[j]), sc1), sc2)));
+        for (int j = 0; j < 32; j += 2) {
+          float q0, q1;
+          f2_split(f2_sub(f2_add(f2(__uint_as_float(x[j]), __uint_as_float(x[j + 1])), ME), ME), q0, q1);
+          x[j] = __float_as_uint(q0);
+          x[j + 1] = __float_as_uint(q1);
+        }
       };
       if (n > 0) load_row(0);
       for (int i = 0; i < n; ++i) {
         if (!mbar_wait_warp(bar(L::B_DQFULL), i & 1, ctl)) break;
         tc_fence_after();
         const int r0 = (qt_lo + i) * kTile + w4 * 32;  // first query row of this warp
-        const int e = fixed ? dq_fixed_exp(MODE, sg, dkl_nx, kl_nx, kmax, a.ln_nk) : 0;
-        const float sc1 = scale_pow2(1.f, min(e, 126)), sc2 = scale_pow2(1.f, max(e - 126, 0));
+        const float me = fixed ? 1.5f * exp2_int(23 - dq_fixed_exp(MODE, sg, dkl_nx, kl_nx, kmax)) : 0.f;
+        const uint64_t ME = f2(me, me);
         if (i + 1 < n) load_row(i + 1);
         uint32_t v[kChunks][32];
         // one box of the dQ tile: row `lane` of this warp's 32 rows, columns [32 h, 32 h + 32)
@@ -419,7 +426,7 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
         if constexpr (kChunks == 4) {
           tmem_ld2x32(t_dq + lane_off, t_dq + lane_off + 32, v[0], v[1]);
           tmem_ld32(t_dq + lane_off + 64, v[2]);
-          if (fixed) to_fixed(v[0], sc1, sc2);
+          if (fixed) to_fixed(v[0], ME);
           put_box(0);
           tmem_ld32(t_dq + lane_off + 96, v[3]);
         } else if constexpr (kChunks == 2) {
@@ -432,7 +439,7 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
         if (lane == 0) mbar_arrive(bar(L::B_DQEMPTY));
 #pragma unroll
         for (int h = kChunks == 4 ? 1 : 0; h < kChunks; ++h) {
-          if (fixed) to_fixed(v[h], sc1, sc2);
+          if (fixed) to_fixed(v[h], ME);
           put_box(h);
         }
       }

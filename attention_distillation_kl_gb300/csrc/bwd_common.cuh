@@ -139,50 +139,41 @@ __device__ __forceinline__ void ds_chunk_row_both(const uint32_t (&x1u)[32], con
   }
 }
 
-// Deterministic dQ in fixed point.  Every contribution to a dQ row is
-// scaled by 2^e (e per query row) and rounded to an int32; int32 sums are
-// exact whatever the order in which the reduce-adds land, and a last pass
-// divides by 2^e again.  e comes from a bound on |dQ_id| that holds for
-// every partial sum of the row:
-//   |dQ_id| <= s dKL_i kmax C_i,  kmax = max |K_g| of the key head,
-//   C_i = sum_k |dS_ik| / dKL_i, which is
-//     mode P2: sum_k |P2_ik - P1_ik| <= 2;
-//     mode P1: sum_k P1_ik |r_ik - KL_i| <= 2 H(P1_i) + 2 KL_i
-//              <= 2 ln NK + 2 KL_i
-//   (r = ln P1 - ln P2, and -ln P2 >= 0: sum P1 (-ln P2) = H(P1) + KL).
-// The bound takes slack for the bf16 rounding of dS and for the recomputed
-// statistics; 2^e times it stays below 2^29, a factor of 4 below the int32
-// limit, which also covers the roundings (half a unit per key tile).  So
-// each key tile's contribution is rounded to 2^-30 of the row's bound or
-// better, for any finite nonzero bound (e spans about [-100, 180]).
-__device__ __forceinline__ int dq_fixed_exp(int mode, float sg, float dkl, float kl, float kmax,
-                                            float ln_nk) {
-  // explicitly rounded operations: the fused kernel and the final pass must
-  // reach the same e for a row, whatever the compiler contracts elsewhere
-  const float c = mode == STREAMKL_GRAD_P2
-                      ? 2.f
-                      : __fadd_rn(__fadd_rn(__fmul_rn(2.f, ln_nk), __fmul_rn(2.f, fmaxf(kl, 0.f))), 1.f);
-  float bound = __fmul_rn(__fmul_rn(__fmul_rn(__fmul_rn(sg, fabsf(dkl)), kmax), c), 1.0078125f);
+// Deterministic dQ: every contribution to a dQ row is rounded to a grid of
+// 2^-e (e per query row) before its fp32 reduce-add.  A sum of multiples of
+// 2^-e is exact in fp32 while it stays below 2^24 grid steps, so the sums
+// come out the same whatever order the reduce-adds land in.  e comes from a
+// bound on |dQ_id| that holds for every partial sum of the row:
+//   |dQ_id| <= s |dKL_i| kmax C_i,  kmax = max |K_g| of the key head,
+//   C_i = sum_k |dS_ik| / |dKL_i|, with TV_i = sum_k max(P2 - P1, 0)
+//        <= min(1, sqrt(KL_i / 2)) (Pinsker):
+//     mode P2: sum_k |P2_ik - P1_ik| = 2 TV_i;
+//     mode P1: sum_k P1_ik |r_ik - KL_i| <= 2 KL_i + 2 TV_i
+//              (r = ln P1 - ln P2; E_P1 |r| = KL + 2 E_P1[max(-r, 0)] and
+//              E_P1[max(ln(P2/P1), 0)] <= sum max(P2 - P1, 0) = TV).
+// KL_i is the forward's value; the bound adds slack for its rounding, for
+// the recomputed probabilities and for the bf16 rounding of dS.  2^e times
+// the bound stays at or below 2^22, so one contribution is rounded by the
+// addend 1.5 * 2^(23 - e) (which holds it in the binade whose step is 2^-e)
+// to within 2^-22 of the bound, and partial sums keep a factor of 4 below
+// 2^24 steps: a bound off by less than that costs nothing; one off by more
+// rounds its contributions coarser, still on the grid.
+__device__ __forceinline__ int dq_fixed_exp(int mode, float sg, float dkl, float kl, float kmax) {
+  // explicitly rounded operations: every CTA that adds to a row must reach
+  // the same e for it, whatever the compiler contracts elsewhere
+  const float k = __fadd_rn(fmaxf(kl, 0.f), 1.0e-4f);
+  const float tv = __fadd_rn(fminf(1.f, __fsqrt_rn(__fmul_rn(k, 0.5f))), 1.0e-4f);
+  const float c = mode == STREAMKL_GRAD_P2 ? __fmul_rn(2.f, tv) : __fmul_rn(2.f, __fadd_rn(k, tv));
+  const float bound = __fmul_rn(__fmul_rn(__fmul_rn(__fmul_rn(sg, fabsf(dkl)), kmax), c), 1.0078125f);
   if (!(bound > 0.f && bound <= 3.0e38f)) return 0;  // zero (nothing to add) or not finite
-  int shift = 0;
-  if (bound < 1.0e-37f) {  // below the normal range: bring it up exactly
-    bound = __fmul_rn(bound, 18446744073709551616.f);  // 2^64
-    shift = 64;
-  }
   const int E = int((__float_as_uint(bound) >> 23) & 255u);  // bound < 2^(E - 126)
-  return 155 - E + shift;
+  // 2^e bound <= 2^22, with e at most 126: every nonzero grid value is then a
+  // normal float (no flushing of subnormals can enter a sum), and rows whose
+  // bound is below 2^-104 keep a grid of 2^-126
+  return max(-100, min(126, 148 - E));
 }
 
-// x 2^e for |e| up to 252, in two exact steps when 2^e is not a float.
-__device__ __forceinline__ float scale_pow2(float x, int e) {
-  if (e > 126) {
-    x = __fmul_rn(x, __uint_as_float(253u << 23));  // 2^126
-    e -= 126;
-  } else if (e < -126) {
-    x = __fmul_rn(x, __uint_as_float(1u << 23));  // 2^-126
-    e += 126;
-  }
-  return __fmul_rn(x, __uint_as_float(uint32_t(e + 127) << 23));
-}
+// 2^e as a float, for |e| <= 126.
+__device__ __forceinline__ float exp2_int(int e) { return __uint_as_float(uint32_t(e + 127) << 23); }
 
 }  // namespace skl

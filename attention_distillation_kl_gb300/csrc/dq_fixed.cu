@@ -1,7 +1,6 @@
-// Deterministic dQ of the fused backward, in int32 fixed point (the bound
-// and exponent are in dq_fixed_exp): the largest |K| of every key head
-// before the fused launches, and the conversion of the int32 sums back to
-// fp32 after them.  Both are single passes over memory.
+// Deterministic dQ of the fused backward (grid and bound: dq_fixed_exp):
+// the largest |K| of every key head, one pass over K before the fused
+// launches.
 #include <algorithm>
 
 #include "bwd_common.cuh"
@@ -38,28 +37,6 @@ __global__ void __launch_bounds__(kKmaxThreads) kmax_kernel(const uint4* k, long
   }
 }
 
-// One warp per dQ row: the row's 2^-e, then its dg int32 sums as fp32.
-__global__ void __launch_bounds__(256) dq_fixed_finish_kernel(const BwdArgs a) {
-  const bool p2 = a.mode == STREAMKL_GRAD_P2;
-  const float sg = p2 ? a.scale2 : a.scale1;
-  const int gg = p2 ? a.g2 : a.g1;
-  const int lane = threadIdx.x & 31;
-  const long long rows = (long long)a.BH * a.NQ;
-  const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
-  for (long long r = blockIdx.x * (long long)(blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += warps) {
-    const int bh = int(r / a.NQ);
-    const float kmax = __uint_as_float(a.kmax[bh / gg] << 16);
-    const int e = dq_fixed_exp(a.mode, sg, a.dkl[r], p2 ? 0.f : a.kl[r], kmax, a.ln_nk);
-    int4* row = reinterpret_cast<int4*>(a.dq + r * a.dg);
-    for (int c = lane; c < a.dg / 4; c += 32) {
-      const int4 q = row[c];
-      reinterpret_cast<float4*>(row)[c] =
-          make_float4(scale_pow2(__int2float_rn(q.x), -e), scale_pow2(__int2float_rn(q.y), -e),
-                      scale_pow2(__int2float_rn(q.z), -e), scale_pow2(__int2float_rn(q.w), -e));
-    }
-  }
-}
-
 }  // namespace
 
 int launch_kmax(const void* k, int heads, long long n, int d, unsigned* kmax, cudaStream_t st) {
@@ -72,17 +49,6 @@ int launch_kmax(const void* k, int heads, long long n, int d, unsigned* kmax, cu
   const long long need = (words + kKmaxThreads - 1) / kKmaxThreads;
   dim3 grid(unsigned(std::max(1LL, std::min(per_head, std::min(need, 4096LL)))), unsigned(heads));
   kmax_kernel<<<grid, kKmaxThreads, 0, st>>>(static_cast<const uint4*>(k), words, kmax);
-  return cudaGetLastError();
-}
-
-int launch_dq_fixed_finish(const BwdArgs& a, cudaStream_t st) {
-  const long long rows = (long long)a.BH * a.NQ;
-  if (rows <= 0) return cudaSuccess;
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 1;
-  const long long blocks = std::min((rows + 7) / 8, 8LL * sms);
-  dq_fixed_finish_kernel<<<unsigned(blocks), 256, 0, st>>>(a);
   return cudaGetLastError();
 }
 

@@ -49,13 +49,12 @@ struct BwdArgs {
   float* dq2;    // both-sides backward: dQ2, dK2 (dq, dk then hold dQ1, dK1)
   float* dk2;
   int dq_box;    // fused backward: width of the dQ reduce-add boxes, 32 (dqw, 128-byte swizzle) or 16
-  // Fused backward, deterministic mode: dQ is summed in int32 fixed point
-  // (dq_fixed_exp; dqw then maps dq as int32) and converted by
-  // launch_dq_fixed_finish.  kmax: per key head of the gradient side, the
-  // largest |K| as bf16 magnitude bits (launch_kmax); ln_nk = ln NK.
+  // Fused backward, deterministic mode: every dQ contribution rounded to its
+  // row's grid (dq_fixed_exp) so the fp32 sums are exact in any order.
+  // kmax: per key head of the gradient side, the largest |K| as bf16
+  // magnitude bits (launch_kmax).
   int dq_fixed;
   const unsigned* kmax;
-  float ln_nk;
 };
 
 // Each returns a cudaError_t value (cudaSuccess = 0).  d1, d2 and d are the
@@ -67,10 +66,8 @@ int launch_splitk_reduce(const float* partial, int rows, int num_splits, float* 
                          float* lse2, cudaStream_t st);
 int launch_bwd_fused(const TMaps& m, int d1, int d2, const BwdArgs& a, cudaStream_t st);
 // Deterministic dQ: kmax[h] = bits of max |k| over head h of k ([heads][n][d]
-// bf16), into a zeroed kmax; then, after the fused launches, dq (int32 sums)
-// converted in place to fp32.
+// bf16), into a zeroed kmax.
 int launch_kmax(const void* k, int heads, long long n, int d, unsigned* kmax, cudaStream_t st);
-int launch_dq_fixed_finish(const BwdArgs& a, cudaStream_t st);
 int launch_bwd_both(const TMaps& m, int d, const BwdArgs& a, cudaStream_t st);  // d1 = d2 = d, 32 or 64
 // Backward with a side above 128: pass 0 writes dK (ordered launches over a
 // key-head group via hsel), pass 1 writes dQ; neither uses atomics.

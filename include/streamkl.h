@@ -148,15 +148,15 @@ int streamkl_suggest_splits(int B, int H, int NQ, int NK, int causal);
  *   STREAMKL_GRAD_P1: dq = dQ1 [B, H, NQ, d1], dk = dK1 [B, H, NK, d1]
  * dq and dk are fp32 and fully overwritten.  deterministic = 0: one kernel,
  * dq accumulated with fp32 atomics after an on-stream memset (summation order
- * varies run to run).  deterministic = 1: the same kernel with dq summed in
- * int32 fixed point, so the order does not matter and the result is bitwise
- * reproducible: each contribution to row i is scaled by 2^e_i and rounded,
- * with e_i the largest exponent that keeps a bound on |dQ_i| (from dKL_i,
- * KL_i, the softmax scale and max |K| of the key head) below 2^29, so the
- * rounding is at most 2^-30 of that bound per key tile; a last pass converts
- * to fp32.  It reads K once more (the bound), and takes 4 bytes per key head
- * of the gradient side from the stream's memory pool (cudaMallocAsync),
- * released on the stream before the call returns.
+ * varies run to run).  deterministic = 1: the same kernel, bitwise
+ * reproducible: each key tile's contribution to dq row i is rounded to a
+ * grid of 2^-e_i before it is added, with 2^-e_i = 2^-22 of a bound on
+ * |dQ_i| (from dKL_i, KL_i, the softmax scale and max |K| of the key head),
+ * so the fp32 sums are exact in any order; the rounding is at most 2^-22 of
+ * that bound per key tile (and at most 2^-127 absolute).  It reads K once
+ * more (the bound), and takes 4 bytes per key head of the gradient side from
+ * the stream's memory pool (cudaMallocAsync), released on the stream before
+ * the call returns.
  * kl, lse1, lse2 must come from streamkl_fwd on the same inputs.
  */
 int streamkl_bwd(const void* q1, const void* k1, const void* q2, const void* k2,
