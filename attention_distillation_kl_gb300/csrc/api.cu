@@ -325,29 +325,35 @@ int streamkl_bwd_gqa(const void* q1, const void* k1, const void* q2, const void*
     if (gg > 1 && cudaMemsetAsync(dk, 0, dk_bytes, cs) != cudaSuccess) return STREAMKL_CUDA_ERROR;
     return as_status(skl::launch_bwd_fused(m, t1, t2, a, cs));
   }
-  // deterministic: the same fused kernel with every dQ contribution rounded
-  // to its row's grid (fp32 sums exact in any order), one launch per query
-  // head of each key-head group in order (the first stores a shared key
-  // head's dK, the others add).  The per-key-head bound on |K| lives in a
-  // stream-ordered scratch block of 4 bytes a head.
+  // deterministic: the same fused kernel in one launch, with every dQ
+  // contribution rounded to its row's grid (fp32 sums exact in any order)
+  // and, when query heads share a key head, their dK added in head order
+  // (the first stores).  Scratch, one stream-ordered block: the bound on |K|
+  // per key head, then the launch's ticket and abort word, then one dK count
+  // per (key head, key tile) when heads share key heads.
   const size_t dq_bytes = size_t(B) * H * NQ * dg * 4;
-  const int kg_heads = B * hkg;
+  const size_t kg_heads = size_t(B) * hkg;
+  const size_t key_tiles = (size_t(NK) + skl::kTile - 1) / skl::kTile;
+  const size_t words = kg_heads + 2 + (gg > 1 ? kg_heads * key_tiles : 0);
   if (!make_map_dq_wide(&m.dqw, dq, (long long)B * H, NQ, dg, &a.dq_box)) return STREAMKL_CUDA_ERROR;
   if (cudaMemsetAsync(dq, 0, dq_bytes, cs) != cudaSuccess) return STREAMKL_CUDA_ERROR;
-  unsigned* kmax = nullptr;
-  if (cudaMallocAsync(reinterpret_cast<void**>(&kmax), size_t(kg_heads) * sizeof(unsigned), cs) != cudaSuccess)
+  unsigned* scratch = nullptr;
+  if (cudaMallocAsync(reinterpret_cast<void**>(&scratch), words * sizeof(unsigned), cs) != cudaSuccess)
     return STREAMKL_CUDA_ERROR;
   int rc = STREAMKL_OK;
-  if (cudaMemsetAsync(kmax, 0, size_t(kg_heads) * sizeof(unsigned), cs) != cudaSuccess ||
-      skl::launch_kmax(mode == STREAMKL_GRAD_P2 ? k2 : k1, kg_heads, NK, dg, kmax, cs) != 0)
+  if (cudaMemsetAsync(scratch, 0, words * sizeof(unsigned), cs) != cudaSuccess ||
+      skl::launch_kmax(mode == STREAMKL_GRAD_P2 ? k2 : k1, int(kg_heads), NK, dg, scratch, cs) != 0)
     rc = STREAMKL_CUDA_ERROR;
   a.dq_fixed = 1;
-  a.kmax = kmax;
-  for (int j = 0; j < gg && rc == STREAMKL_OK; ++j) {
-    a.hsel = gg > 1 ? j : -1;
-    if (skl::launch_bwd_fused(m, t1, t2, a, cs) != 0) rc = STREAMKL_CUDA_ERROR;
+  a.kmax = scratch;
+  if (gg > 1) {
+    int* words_i = reinterpret_cast<int*>(scratch);
+    a.ticket = words_i + kg_heads;
+    a.dk_abort = words_i + kg_heads + 1;
+    a.dk_turns = words_i + kg_heads + 2;
   }
-  if (cudaFreeAsync(kmax, cs) != cudaSuccess) rc = STREAMKL_CUDA_ERROR;
+  if (rc == STREAMKL_OK && skl::launch_bwd_fused(m, t1, t2, a, cs) != 0) rc = STREAMKL_CUDA_ERROR;
+  if (cudaFreeAsync(scratch, cs) != cudaSuccess) rc = STREAMKL_CUDA_ERROR;
   return rc;
 }
 

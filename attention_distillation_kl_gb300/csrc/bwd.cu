@@ -74,7 +74,7 @@ struct BwdLayout {
     B_DSFULL, B_DSEMPTY, B_DQFULL, B_DQEMPTY, B_DKFULL, B_DONE, kNumBars
   };
   static constexpr uint32_t oMisc = oBar + kNumBars * 8;
-  static constexpr uint32_t kBytes = oMisc + 16;
+  static constexpr uint32_t kBytes = oMisc + 32;
   static constexpr uint32_t kAlloc = kBytes + 1024;
   static_assert(kAlloc <= 232448, "over the 227 KB shared memory limit");
 };
@@ -88,6 +88,29 @@ __device__ __forceinline__ void wait_s_queued(volatile int* s_queued, int want) 
   if (want <= 0 || *s_queued >= want) return;
   const uint64_t t0 = globaltimer();
   while (*s_queued < want && globaltimer() - t0 < 20000ull) {
+  }
+}
+
+// Grouped key heads, deterministic mode: waits until the count of query
+// heads that have added their dK to this (key head, key tile) reads `want`,
+// polling with a short sleep.  Gives up when this CTA or another one has
+// aborted, or after the wait limit; then this CTA aborts, and a time-out
+// also aborts the launch and is reported in the status word.
+static __device__ __noinline__ bool wait_turn(const int* turn, int want, int* launch_abort, Ctl ctl) {
+  const uint64_t t0 = globaltimer();
+  while (true) {
+    if (ld_acquire_gpu(turn) == want) return true;
+    if (*ctl.abort || *reinterpret_cast<volatile int*>(launch_abort)) {
+      *ctl.abort = 1;
+      return false;
+    }
+    if (globaltimer() - t0 > STREAMKL_WAIT_LIMIT_NS) {
+      *ctl.abort = 1;
+      atomicExch(launch_abort, 1);
+      atomicCAS(ctl.status, 0, (int)STREAMKL_DEVICE_TIMEOUT);
+      return false;
+    }
+    __nanosleep(128);
   }
 }
 
@@ -110,14 +133,6 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   const int gg = kP2 ? a.g2 : a.g1;  // query heads per gradient-side key head
-  const int kt = blockIdx.x, bh = a.hsel < 0 ? int(blockIdx.y) : int(blockIdx.y) * gg + a.hsel;
-  const int k0 = kt * kTile;
-  const int off = a.NK - a.NQ;
-  const int nqt = (a.NQ + kTile - 1) / kTile;
-  // causal: query i sees key j iff i >= j - off; the first query tile that
-  // sees any key of this tile starts at row max(0, k0 - off)
-  const int qt_lo = a.causal ? max(0, k0 - off) / kTile : 0;
-  const int n = nqt - qt_lo;
 
   auto bar = [&](int id) { return sb + L::oBar + 8u * id; };
   const CUtensorMap* tqo = kP2 ? &tq1 : &tq2;
@@ -127,9 +142,14 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
   // query tiles whose S products the S issuer has queued (a scheduling
   // hint for the gradient issuers, see below)
   volatile int* s_queued = reinterpret_cast<volatile int*>(smem + L::oMisc + 8);
+  int* unit_slot = reinterpret_cast<int*>(smem + L::oMisc + 12);
+  volatile int* turn_ok = reinterpret_cast<volatile int*>(smem + L::oMisc + 16);
   const Ctl ctl{abort_flag, a.status};
 
   if (threadIdx.x == 0) {
+    // ordered dK of grouped key heads: units (key tile fastest, then query
+    // head) in the order CTAs start, so a head waits only for CTAs that run
+    *unit_slot = a.ticket ? atomicAdd(a.ticket, 1) : int(blockIdx.y * gridDim.x + blockIdx.x);
     *s_queued = 0;
     for (int b = 0; b < L::kNumBars; ++b) {
       uint32_t count = 1;  // TMA transaction barriers and tcgen05.commit targets
@@ -151,6 +171,17 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t t_s1 = tmem, t_s2 = tmem + 128, t_dk = tmem + 256, t_dq = tmem + 384;
+
+  const int unit = *unit_slot;
+  const int kt = unit % int(gridDim.x);
+  const int bh = unit / int(gridDim.x);  // query head (batch-major)
+  const int k0 = kt * kTile;
+  const int off = a.NK - a.NQ;
+  const int nqt = (a.NQ + kTile - 1) / kTile;
+  // causal: query i sees key j iff i >= j - off; the first query tile that
+  // sees any key of this tile starts at row max(0, k0 - off)
+  const int qt_lo = a.causal ? max(0, k0 - off) / kTile : 0;
+  const int n = nqt - qt_lo;
 
   if (warp == 12) {
     // ---------------------------------------------------------------- TMA producer
@@ -447,11 +478,9 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
     }
     // dK of key head bh / gg: stored, or (grouped key heads) added to what
     // the other query heads of the group contribute
-    const int dk_how = (gg == 1 || a.hsel == 0) ? kDkStore : (a.hsel < 0 ? kDkAtomic : kDkAdd);
     const int kj = k0 + row;
     float* dst = a.dk + (size_t(bh / gg) * a.NK + kj) * a.dg;
-    if (n > 0 && mbar_wait_warp(bar(L::B_DKFULL), 0, ctl)) {
-      tc_fence_after();
+    auto write_dk = [&](int how) {
 #pragma unroll
       for (int ch = 0; ch < DG / 32; ++ch) {
         uint32_t v[32];
@@ -463,12 +492,51 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
               put_dk4(dst + ch * 32 + e,
                       make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]), __uint_as_float(v[e + 2]),
                                   __uint_as_float(v[e + 3])),
-                      dk_how);
+                      how);
         }
       }
-    } else if (n == 0 && dk_how == kDkStore && kj < a.NK) {
-      // no query row sees this key tile: its dK is zero
-      for (int e = 0; e < a.dg; e += 4) *reinterpret_cast<float4*>(dst + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+    };
+    auto zero_dk = [&]() {  // no query row sees this key tile
+      if (kj < a.NK)
+        for (int e = 0; e < a.dg; e += 4) *reinterpret_cast<float4*>(dst + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+    };
+    if (a.dk_turns == nullptr) {
+      const int dk_how = gg == 1 ? kDkStore : kDkAtomic;  // atomics: a shared key head, any order
+      if (n > 0 && mbar_wait_warp(bar(L::B_DKFULL), 0, ctl)) {
+        tc_fence_after();
+        write_dk(dk_how);
+      } else if (n == 0 && dk_how == kDkStore) {
+        zero_dk();
+      }
+    } else {
+      // Deterministic, grouped key heads: the query heads of a group add in
+      // head order.  Head m of the group waits until the (key head, key
+      // tile) count reads m, then stores (m = 0) or adds, and the count
+      // moves on once all four warps' rows are written.  Every epilogue
+      // warp reaches both barriers whatever happened (each wait before them
+      // is bounded); the count is not moved by a CTA that gave up.
+      const int member = bh % gg;
+      int* turn = a.dk_turns + size_t(bh / gg) * gridDim.x + kt;
+      const bool have = n > 0 && mbar_wait_warp(bar(L::B_DKFULL), 0, ctl);
+      if (warp == 8 && lane == 0) *turn_ok = wait_turn(turn, member, a.dk_abort, ctl) ? 1 : 0;
+      named_bar_sync(1, 128);
+      if (*turn_ok) {
+        if (have) {
+          tc_fence_after();
+          write_dk(member == 0 ? kDkStore : kDkAdd);
+        } else if (n == 0 && member == 0) {
+          zero_dk();
+        }
+      }
+      named_bar_sync(1, 128);
+      if (warp == 8 && lane == 0) {
+        if (*turn_ok && !*abort_flag) {
+          __threadfence();
+          st_release_gpu(turn, member + 1);
+        } else {
+          atomicExch(a.dk_abort, 1);
+        }
+      }
     }
   }
 
@@ -486,8 +554,7 @@ static int launch_fused_t(const TMaps& m, const BwdArgs& a, cudaStream_t st) {
   auto kern = bwd_fused_kernel<D1, D2, MODE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
-  const int gg = MODE == STREAMKL_GRAD_P2 ? a.g2 : a.g1;
-  dim3 grid((a.NK + kTile - 1) / kTile, a.hsel < 0 ? a.BH : a.BH / gg);
+  dim3 grid((a.NK + kTile - 1) / kTile, a.BH);
   kern<<<grid, L::kThreads, L::kAlloc, st>>>(m.q1, m.k1, m.q2, m.k2, m.dqw, a);
   return cudaGetLastError();
 }

@@ -17,6 +17,8 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // How a dK row chunk reaches global memory: plain store (the CTA owns the
 // key head), atomic add (several CTAs of a key-head group at once) or
 // read-add-write (the launches of a group run one after the other).
+// (The read in the read-add-write bypasses L1: within one launch the
+// previous value may have been written from another SM.)
 enum { kDkStore = 0, kDkAtomic = 1, kDkAdd = 2 };
 
 __device__ __forceinline__ void put_dk4(float* p, float4 v, int how) {
@@ -26,7 +28,7 @@ __device__ __forceinline__ void put_dk4(float* p, float4 v, int how) {
   } else if (how == kDkAtomic) {
     atomicAdd(q, v);
   } else {
-    const float4 o = *q;
+    const float4 o = __ldcg(q);
     *q = make_float4(o.x + v.x, o.y + v.y, o.z + v.z, o.w + v.w);
   }
 }

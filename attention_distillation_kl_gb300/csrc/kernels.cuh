@@ -33,10 +33,10 @@ struct BwdArgs {
   int BH, NQ, NK, causal, mode;
   int dg;  // the gradient side's head dim: row length of dq, dk (at most the kernel's tile width)
   int g1, g2;  // query heads per key head of each side; dk has BH / g_grad heads
-  // Query heads of the fused kernel: -1 = every head (grid.y = BH), dK of a
-  // shared key head added with atomics into a zeroed dk; j >= 0 = head
-  // j of every group only (grid.y = BH / g_grad), dK stored (j = 0) or added
-  // in place (j > 0), so launches j = 0, 1, ... sum in a fixed order.
+  // Query heads of the wide-head dK pass: -1 = every head (grid.y = BH);
+  // j >= 0 = head j of every key-head group only (grid.y = BH / g_grad), dK
+  // stored (j = 0) or added in place (j > 0), so launches j = 0, 1, ... sum
+  // in a fixed order.  (The fused kernel always takes every head.)
   int hsel;
   float scale1, scale2;
   const float* kl;
@@ -55,6 +55,15 @@ struct BwdArgs {
   // magnitude bits (launch_kmax).
   int dq_fixed;
   const unsigned* kmax;
+  // Deterministic mode with grouped key heads, one launch for all query
+  // heads (all null otherwise): ticket (zeroed) hands out the CTAs' units
+  // (key tile, query head) in launch order; dk_turns [B * HK_g][key tiles]
+  // (zeroed) counts the query heads of a group that have added their dK to
+  // a key tile, which they do in head order; dk_abort (zeroed) is set by a
+  // CTA that gave up, so the later heads do not wait for it.
+  int* ticket;
+  int* dk_turns;
+  int* dk_abort;
 };
 
 // Each returns a cudaError_t value (cudaSuccess = 0).  d1, d2 and d are the

@@ -198,9 +198,14 @@ int streamkl_bwd_scaled(const void* q1, const void* k1, const void* q2, const vo
  * count (HK2 in mode P2, HK1 in mode P1): the sum over the query heads
  * that read each key head.  With deterministic = 0 a shared head's dK is
  * added up with fp32 atomics (order not fixed); with deterministic = 1 the
- * query heads of a group are taken one launch after another in head order,
- * so the result is bitwise repeatable.  Otherwise as the *_scaled calls,
- * which are these with HK1 = HK2 = H.
+ * query heads of a group add their dK to each key tile in head order (still
+ * one launch: a CTA takes its turn from a counter per key head and key
+ * tile, which it waits for only when the previous head's CTA for the same
+ * key tile is still running), so the result is bitwise repeatable; the
+ * counters add 4 bytes per key head and key tile to the scratch block.  Heads
+ * above 128 take two passes without atomics (dK, then dQ) whatever
+ * `deterministic` says.  Otherwise as the *_scaled calls, which are these
+ * with HK1 = HK2 = H.
  */
 int streamkl_fwd_gqa(const void* q1, const void* k1, const void* q2, const void* k2,
                      int B, int H, int HK1, int HK2, int NQ, int NK, int d1, int d2,

@@ -92,3 +92,25 @@ def test_gqa_fixed_point_repeatable_and_close():
         kg = kg.repeat_interleave(w.H // kg.shape[1], dim=1)  # key head of each query head
         bound = row_bound(mode, w.scale, np_(dkl), np_(kl), kg)
         compare_modes(np_(f[0]), np_(a[0]), bound, (w.NK + 127) // 128)
+        # dK of a shared key head: ordered adds against atomics in any order
+        dk_f, dk_d = np_(f[1]), np_(a[1])
+        assert np.linalg.norm(dk_d - dk_f) <= 1e-5 * np.linalg.norm(dk_f)
+
+
+def test_mqa_ordered_dk_single_launch():
+    """Eight query heads on one key head per side, causal with NQ < NK."""
+    w = Workload("fxm", 1, 8, 200, 600, 64, 64, True, 0.125, "independent", 0.0, 1.0, 213)
+    dev = [t.cuda() for t in generate_gqa(w, 1, 1)]
+    dkl = generate_dkl(w, "signed").cuda()
+    kl, l1, l2 = skl.streamkl_fwd_gqa(*dev, w.scale, w.scale, w.causal)
+    for mode in MODES:
+        runs = [skl.streamkl_bwd_gqa(*dev, w.scale, w.scale, w.causal, kl, l1, l2, dkl, mode, True)
+                for _ in range(3)]
+        f = skl.streamkl_bwd_gqa(*dev, w.scale, w.scale, w.causal, kl, l1, l2, dkl, mode, False)
+        torch.cuda.synchronize()
+        assert skl.streamkl_get_device_status() == skl.STREAMKL_OK
+        for r in runs[1:]:
+            assert torch.equal(r[0], runs[0][0]) and torch.equal(r[1], runs[0][1])
+        dk_f, dk_d = np_(f[1]), np_(runs[0][1])
+        assert np.all(np.isfinite(dk_d))
+        assert np.linalg.norm(dk_d - dk_f) <= 1e-5 * np.linalg.norm(dk_f)
