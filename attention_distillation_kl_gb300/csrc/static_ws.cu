@@ -13,9 +13,7 @@
 // so every GPU on which the library's module is loaded holds that much memory
 // until the process exits.  In host code its name is only a host-side stand-in
 // for the symbol, never a device address: the device address is looked up
-// with cudaGetSymbolAddress, once per device, while that device is current.
-#include <mutex>
-
+// with cudaGetSymbolAddress on every call, on the current device.
 #include <cuda_runtime.h>
 
 #include "streamkl.h"
@@ -27,26 +25,14 @@ constexpr size_t kStaticFloats = STREAMKL_STATIC_WORKSPACE_BYTES / sizeof(float)
 // Shared by every call on a device; the contents of the last call remain.
 static __device__ __align__(256) float g_splitk_static_ws[kStaticFloats];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_ws_addr[kMaxDevices] = {};
-
 // Device address of g_splitk_static_ws on the current device, looked up on
-// the first call for that device.  Returns STREAMKL_OK and sets *out.  The
-// cache outlives a cudaDeviceReset (which unloads the module and may move
-// the array), so the entry point is documented as unusable after one.
+// every call (cheap, and never stale: a cudaDeviceReset reloads the module
+// and may move the array).  Returns STREAMKL_OK and sets *out.
 int static_ws_address(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return STREAMKL_CUDA_ERROR;
-  if (dev < 0 || dev >= kMaxDevices) return STREAMKL_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (g_ws_addr[dev] == nullptr) {
-    void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_splitk_static_ws);
-    if (e != cudaSuccess || p == nullptr) return STREAMKL_CUDA_ERROR;
-    g_ws_addr[dev] = p;
-  }
-  *out = g_ws_addr[dev];
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_splitk_static_ws);
+  if (e != cudaSuccess || p == nullptr) return STREAMKL_CUDA_ERROR;
+  *out = p;
   return STREAMKL_OK;
 }
 

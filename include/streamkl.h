@@ -114,11 +114,10 @@ size_t streamkl_fwd_splitk_workspace_bytes(int B, int H, int NQ, int num_splits)
  * Limits: streamkl_fwd_splitk_workspace_bytes(B, H, NQ, num_splits) must not
  *   exceed STREAMKL_STATIC_WORKSPACE_BYTES, else STREAMKL_INVALID_ARG and
  *   nothing is enqueued.
- * Set-up: the first call on a device (with that device current) looks up the
- *   array's device address and caches it; make that first call before any
- *   stream capture on the device.  cudaDeviceReset unloads the library's
- *   module, so the cached address is stale afterwards: do not call this
- *   entry point on a device after resetting it in the same process.
+ * Set-up: every call looks the array's device address up afresh (so a
+ *   cudaDeviceReset, which reloads the library's module and may move the
+ *   array, does no harm); the first call on a device may load the module,
+ *   so make it before any stream capture on that device.
  * Sharing: all calls on a device share the array, which keeps the last
  *   call's contents (nothing in it needs to start at zero).  Calls that
  *   overlap on the GPU -- on different streams, or from different host
