@@ -579,10 +579,12 @@ def run_mine(args, rank, world, local):
         if k > 0:  # the first is warm-up
             p1_ms.append(a.elapsed_time(b_))
     p1_ms = float(np.median(p1_ms))
-    # the deterministic (atomic-free, two-pass) P2 backward on the same inputs
+    # the deterministic P2 backward (dQ on the per-row grid) on the same inputs
     det_ms = timed(lambda: skl.streamkl_bwd(*dev, w.scale, w.causal, kl, l1, l2, dkl, skl.STREAMKL_GRAD_P2, True,
                                             dq, dk), stream, reps=3)
-    # the library allocates nothing: device memory free before and after the calls must agree
+    # the library holds no device memory across calls (the deterministic
+    # backward's scratch block comes from the stream's pool and goes back to
+    # it): device memory free before and after the calls must agree
     extra_bytes = free0 - torch.cuda.mem_get_info()[0]
     f_p1 = (2 * (w.d1 + w.d2) + 4 * w.d1) * w.pairs
 
