@@ -34,8 +34,9 @@
 //              -> 32 x 32 fp32 boxes in 128-byte-swizzled
 //              shared memory (two per warp, round robin) -> TMA bulk tensor
 //              reduce-add into global dQ (rows past NQ are clipped by the
-//              tensor map); finally dK (stored, or added when a key head is
-//              shared by several query heads: put_dk4)
+//              tensor map); finally dK (stored; when several query heads
+//              share a key head, added with atomics, or in the deterministic
+//              mode in head order, see wait_turn)
 // TMEM: S1 [0,128), S2 [128,256), dK [256, 256+dg), dQ [384, 384+dg).
 //
 // Deterministic mode: the same kernel, with each dQ contribution rounded to

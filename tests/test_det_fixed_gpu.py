@@ -114,3 +114,32 @@ def test_mqa_ordered_dk_single_launch():
         dk_f, dk_d = np_(f[1]), np_(runs[0][1])
         assert np.all(np.isfinite(dk_d))
         assert np.linalg.norm(dk_d - dk_f) <= 1e-5 * np.linalg.norm(dk_f)
+
+
+def test_headline_size_deterministic_matches_fused():
+    """64K x 32 heads, causal, d = 128 (the benchmark's workload and launch):
+    every row of the deterministic dQ within its rounding bound of the fused
+    one, dK equal bit for bit, and two deterministic runs identical."""
+    from attention_distillation_kl_gb300.workloads import WORKLOADS
+    w = WORKLOADS["c4"]
+    _, dev = inputs(w)
+    dkl = generate_dkl(w, "uniform").cuda()
+    kl, l1, l2 = skl.streamkl_fwd(*dev, w.scale, w.causal)
+    fused = skl.streamkl_bwd(*dev, w.scale, w.causal, kl, l1, l2, dkl, skl.STREAMKL_GRAD_P2, False)
+    det = skl.streamkl_bwd(*dev, w.scale, w.causal, kl, l1, l2, dkl, skl.STREAMKL_GRAD_P2, True)
+    det2 = skl.streamkl_bwd(*dev, w.scale, w.causal, kl, l1, l2, dkl, skl.STREAMKL_GRAD_P2, True)
+    torch.cuda.synchronize()
+    assert skl.streamkl_get_device_status() == skl.STREAMKL_OK
+    assert torch.equal(det[0], det2[0]) and torch.equal(det[1], det2[1])
+    assert torch.equal(det[1], fused[1])
+    # the bound of each row, on the device (same formula as row_bound)
+    kmax = dev[3].float().abs().amax(dim=(2, 3))  # [B, H]
+    k = kl.clamp_min(0.0).double() + 1e-4
+    tv = torch.clamp(torch.sqrt(k / 2), max=1.0) + 1e-4
+    bound = w.scale * dkl.double().abs() * kmax.double()[:, :, None] * 2.0 * tv * 1.0078125
+    tiles = (w.NK + 127) // 128
+    tol = (tiles + 1) * (2.0 ** -24 + 2.0 ** -21) * bound + tiles * 2.0 ** -126
+    err = (det[0] - fused[0]).abs().amax(dim=-1).double()
+    assert bool(torch.all(torch.isfinite(det[0])))
+    worst = torch.argmax(err - tol)
+    assert bool(torch.all(err <= tol)), f"row {worst.item()}: {err.flatten()[worst].item()} > {tol.flatten()[worst].item()}"
