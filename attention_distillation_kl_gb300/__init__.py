@@ -21,6 +21,7 @@ __all__ = [
     "streamkl_fwd_gqa", "streamkl_fwd_splitk_gqa", "streamkl_bwd_gqa", "streamkl_bwd_both",
     "status_string", "STREAMKL_STATIC_WORKSPACE_BYTES",
     "streamkl_get_device_status", "streamkl_probe_ex2", "streamkl_selftest_wait_timeout",
+    "streamkl_selftest_turn_timeout",
     "STREAMKL_OK", "STREAMKL_INVALID_ARG", "STREAMKL_UNSUPPORTED", "STREAMKL_CUDA_ERROR",
     "STREAMKL_DEVICE_TIMEOUT", "STREAMKL_DEBUG_BOUNDS", "STREAMKL_GRAD_P2", "STREAMKL_GRAD_P1",
 ]
@@ -69,6 +70,7 @@ _SIGS = {
     "streamkl_get_device_status": (_I, []),
     "streamkl_probe_ex2": (_I, [_P, _I, _I, _P]),
     "streamkl_selftest_wait_timeout": (_I, [_I, _P]),
+    "streamkl_selftest_turn_timeout": (_I, [_I, _P, _P]),
 }
 
 
@@ -375,3 +377,10 @@ def streamkl_selftest_wait_timeout(limit_us, stream=None):
     """Runs a kernel whose barrier wait must time out (see the header)."""
     _check(lib().streamkl_selftest_wait_timeout(int(limit_us), _stream(stream)),
            "streamkl_selftest_wait_timeout")
+
+
+def streamkl_selftest_turn_timeout(limit_us, words, stream=None):
+    """Runs a kernel whose turn wait must time out (see the header); `words`
+    is a CUDA int32 tensor of at least 5 elements."""
+    _check(lib().streamkl_selftest_turn_timeout(int(limit_us), words.data_ptr(), _stream(stream)),
+           "streamkl_selftest_turn_timeout")

@@ -439,6 +439,17 @@ int streamkl_selftest_wait_timeout(int limit_us, streamkl_stream_t stream) {
                                              reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int streamkl_selftest_turn_timeout(int limit_us, int* words, streamkl_stream_t stream) {
+  if (limit_us < 1 || limit_us > 1000000 || !words || !aligned16(words)) return STREAMKL_INVALID_ARG;
+  int s = device_ok();
+  if (s != STREAMKL_OK) return s;
+  int* st = status_ptr();
+  if (!st) return STREAMKL_CUDA_ERROR;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(words, 0, 5 * sizeof(int), cs) != cudaSuccess) return STREAMKL_CUDA_ERROR;
+  return as_status(skl::launch_turn_selftest(words, st, uint64_t(limit_us) * 1000u, cs));
+}
+
 int streamkl_probe_ex2(float* out, int blocks, int iters, streamkl_stream_t stream) {
   if (!out || blocks < 1 || iters < 1 || blocks > (1 << 20)) return STREAMKL_INVALID_ARG;
   return as_status(skl::launch_ex2_probe(out, blocks, iters, reinterpret_cast<cudaStream_t>(stream)));

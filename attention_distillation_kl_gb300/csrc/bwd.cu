@@ -95,9 +95,10 @@ __device__ __forceinline__ void wait_s_queued(volatile int* s_queued, int want) 
 // Grouped key heads, deterministic mode: waits until the count of query
 // heads that have added their dK to this (key head, key tile) reads `want`,
 // polling with a short sleep.  Gives up when this CTA or another one has
-// aborted, or after the wait limit; then this CTA aborts, and a time-out
-// also aborts the launch and is reported in the status word.
-static __device__ __noinline__ bool wait_turn(const int* turn, int want, int* launch_abort, Ctl ctl) {
+// aborted, or after `limit_ns`; then this CTA aborts, and a time-out also
+// aborts the launch and is reported in the status word.
+static __device__ __noinline__ bool wait_turn(const int* turn, int want, int* launch_abort, Ctl ctl,
+                                              uint64_t limit_ns = STREAMKL_WAIT_LIMIT_NS) {
   const uint64_t t0 = globaltimer();
   while (true) {
     if (ld_acquire_gpu(turn) == want) return true;
@@ -105,7 +106,7 @@ static __device__ __noinline__ bool wait_turn(const int* turn, int want, int* la
       *ctl.abort = 1;
       return false;
     }
-    if (globaltimer() - t0 > STREAMKL_WAIT_LIMIT_NS) {
+    if (globaltimer() - t0 > limit_ns) {
       *ctl.abort = 1;
       atomicExch(launch_abort, 1);
       atomicCAS(ctl.status, 0, (int)STREAMKL_DEVICE_TIMEOUT);
@@ -557,6 +558,28 @@ static int launch_fused_t(const TMaps& m, const BwdArgs& a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   dim3 grid((a.NK + kTile - 1) / kTile, a.BH);
   kern<<<grid, L::kThreads, L::kAlloc, st>>>(m.q1, m.k1, m.q2, m.k2, m.dqw, a);
+  return cudaGetLastError();
+}
+
+// Self-test of the turn wait (one thread, no fault): words = {count, launch
+// abort, out[0..2]}, zeroed.  Waits for a count nothing moves, which must
+// give up after limit_ns, report a time-out and set the launch abort word;
+// then, as another CTA would, waits again, which must give up at once on
+// the abort word.  out = {first wait returned, second returned, second
+// gave up within a tenth of the limit}.
+__global__ void turn_selftest_kernel(int* words, int* status, uint64_t limit_ns) {
+  __shared__ int abort_flag;
+  abort_flag = 0;
+  Ctl ctl{&abort_flag, status};
+  words[2] = wait_turn(words, 1, words + 1, ctl, limit_ns) ? 1 : 0;
+  abort_flag = 0;
+  const uint64_t t0 = globaltimer();
+  words[3] = wait_turn(words, 1, words + 1, ctl, limit_ns) ? 1 : 0;
+  words[4] = globaltimer() - t0 < limit_ns / 10 ? 1 : 0;
+}
+
+int launch_turn_selftest(int* words, int* status, uint64_t limit_ns, cudaStream_t st) {
+  turn_selftest_kernel<<<1, 1, 0, st>>>(words, status, limit_ns);
   return cudaGetLastError();
 }
 

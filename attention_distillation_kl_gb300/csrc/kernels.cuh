@@ -84,5 +84,6 @@ int launch_bwd_wide_pass0(const TMaps& m, int d1, int d2, const BwdArgs& a, cuda
 int launch_bwd_wide_pass1(const TMaps& m, int d1, int d2, const BwdArgs& a, cudaStream_t st);
 int launch_ex2_probe(float* out, int blocks, int iters, cudaStream_t st);
 int launch_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t st);
+int launch_turn_selftest(int* words, int* status, uint64_t limit_ns, cudaStream_t st);
 
 }  // namespace skl

@@ -263,6 +263,21 @@ int streamkl_get_device_status(void);
 int streamkl_selftest_wait_timeout(int limit_us, streamkl_stream_t stream);
 
 /*
+ * Self-test of the other bounded wait, the one the deterministic backward
+ * uses when query heads share a key head (a CTA waits for a counter in
+ * global memory to reach its turn).  `words`: device memory of at least 5
+ * ints, 16-byte aligned, owned by the caller and overwritten.  One thread
+ * waits for a counter nothing moves; after `limit_us` microseconds (1 ..
+ * 1e6) it must give up, set the device status word to
+ * STREAMKL_DEVICE_TIMEOUT and set the launch's abort word; a second wait,
+ * as another CTA of that launch would make, must then give up at once.
+ * Results in words[2..4]: first wait succeeded (0 expected), second wait
+ * succeeded (0 expected), second wait returned within a tenth of the limit
+ * (1 expected).  Returns INVALID_ARG for a bad limit or pointer.
+ */
+int streamkl_selftest_turn_timeout(int limit_us, int* words, streamkl_stream_t stream);
+
+/*
  * Device probe used for the roofline denominator: runs `blocks` CTAs of 256
  * threads, each thread evaluating `iters` x 8 independent ex2.approx.f32
  * chains, and writes a checksum to out[0] (device pointer) so the work is

@@ -34,3 +34,26 @@ def test_selftest_argument_checks():
         skl.streamkl_selftest_wait_timeout(0)
     with pytest.raises(skl.StreamKLError):
         skl.streamkl_selftest_wait_timeout(2_000_000)
+
+
+def test_turn_wait_reports_timeout_and_releases_the_launch():
+    """The counter wait of the deterministic backward with shared key heads:
+    it gives up after the limit, reports a time-out, sets the launch's abort
+    word, and a later wait of the same launch gives up at once."""
+    assert skl.streamkl_get_device_status() == skl.STREAMKL_OK
+    words = torch.full((8,), -1, dtype=torch.int32, device="cuda")
+    skl.streamkl_selftest_turn_timeout(20000, words)  # 20 ms
+    torch.cuda.synchronize()
+    w = words.cpu().tolist()
+    assert w[0] == 0 and w[1] == 1, w          # the count never moved; the launch was aborted
+    assert w[2] == 0 and w[3] == 0 and w[4] == 1, w
+    assert skl.streamkl_get_device_status() == skl.STREAMKL_DEVICE_TIMEOUT
+    assert skl.streamkl_get_device_status() == skl.STREAMKL_OK
+
+
+def test_turn_selftest_argument_checks():
+    words = torch.zeros(8, dtype=torch.int32, device="cuda")
+    with pytest.raises(skl.StreamKLError):
+        skl.streamkl_selftest_turn_timeout(0, words)
+    with pytest.raises(skl.StreamKLError):
+        skl.streamkl_selftest_turn_timeout(2_000_000, words)
