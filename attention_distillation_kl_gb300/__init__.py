@@ -19,6 +19,7 @@ __all__ = [
     "streamkl_suggest_splits", "streamkl_fwd_splitk_noalloc", "streamkl_bwd", "streamkl_status_string",
     "streamkl_fwd_scaled", "streamkl_fwd_splitk_scaled", "streamkl_bwd_scaled",
     "streamkl_fwd_gqa", "streamkl_fwd_splitk_gqa", "streamkl_bwd_gqa", "streamkl_bwd_both",
+    "streamkl_bwd_workspace_bytes", "streamkl_bwd_gqa_ws",
     "status_string", "STREAMKL_STATIC_WORKSPACE_BYTES",
     "streamkl_get_device_status", "streamkl_probe_ex2", "streamkl_selftest_wait_timeout",
     "streamkl_selftest_turn_timeout",
@@ -66,6 +67,9 @@ _SIGS = {
                               _I, _P, _P, _P]),
     "streamkl_bwd_both": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _F, _I, _P, _P, _P, _P, _I,
                                _P, _P, _P, _P, _P]),
+    "streamkl_bwd_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I, _I, _I, _I]),
+    "streamkl_bwd_gqa_ws": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _F, _I, _P, _P, _P, _P, _I,
+                                 _I, _P, _P, _P, _SZ, _P]),
     "streamkl_status_string": (ctypes.c_char_p, [_I]),
     "streamkl_get_device_status": (_I, []),
     "streamkl_probe_ex2": (_I, [_P, _I, _I, _P]),
@@ -342,6 +346,33 @@ def streamkl_bwd_gqa(q1, k1, q2, k2, scale1, scale2, causal, kl, lse1, lse2, dkl
                                   int(mode), int(bool(deterministic)), dq.data_ptr(), dk.data_ptr(),
                                   _stream(stream)),
            "streamkl_bwd_gqa")
+    return dq, dk
+
+
+def streamkl_bwd_workspace_bytes(B, H, HK1, HK2, NK, d1, d2, mode=STREAMKL_GRAD_P2, deterministic=True):
+    """Scratch bytes streamkl_bwd_gqa_ws needs (see the header)."""
+    return int(lib().streamkl_bwd_workspace_bytes(B, H, HK1, HK2, NK, d1, d2, int(mode), int(bool(deterministic))))
+
+
+def streamkl_bwd_gqa_ws(q1, k1, q2, k2, scale1, scale2, causal, kl, lse1, lse2, dkl, workspace,
+                        mode=STREAMKL_GRAD_P2, deterministic=True, dq=None, dk=None, stream=None):
+    """streamkl_bwd_gqa with the deterministic mode's scratch in `workspace`
+    (a CUDA tensor of at least streamkl_bwd_workspace_bytes bytes, or None
+    when that is 0)."""
+    B, H, HK1, HK2, NQ, NK, d1, d2 = _dims_gqa(q1, k1, q2, k2)
+    dg, hkg = (d2, HK2) if mode == STREAMKL_GRAD_P2 else (d1, HK1)
+    for name, t in (("kl", kl), ("lse1", lse1), ("lse2", lse2), ("dkl", dkl)):
+        _out(t, (B, H, NQ), q1.device, name)
+    dq = _out(dq, (B, H, NQ, dg), q1.device, "dq")
+    dk = _out(dk, (B, hkg, NK, dg), q1.device, "dk")
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().streamkl_bwd_gqa_ws(q1.data_ptr(), k1.data_ptr(), q2.data_ptr(), k2.data_ptr(),
+                                     B, H, HK1, HK2, NQ, NK, d1, d2, float(scale1), float(scale2),
+                                     int(bool(causal)), kl.data_ptr(), lse1.data_ptr(), lse2.data_ptr(),
+                                     dkl.data_ptr(), int(mode), int(bool(deterministic)), dq.data_ptr(),
+                                     dk.data_ptr(), ws_ptr, ws_bytes, _stream(stream)),
+           "streamkl_bwd_gqa_ws")
     return dq, dk
 
 

@@ -273,10 +273,31 @@ int streamkl_suggest_splits(int B, int H, int NQ, int NK, int causal) {
   return best;
 }
 
-int streamkl_bwd_gqa(const void* q1, const void* k1, const void* q2, const void* k2, int B, int H, int HK1,
-                     int HK2, int NQ, int NK, int d1, int d2, float scale1, float scale2, int causal,
-                     const float* kl, const float* lse1, const float* lse2, const float* dkl, int mode,
-                     int deterministic, float* dq, float* dk, streamkl_stream_t stream) {
+size_t streamkl_bwd_workspace_bytes(int B, int H, int HK1, int HK2, int NK, int d1, int d2, int mode,
+                                    int deterministic) {
+  if (B < 0 || H < 0 || NK < 0 || HK1 <= 0 || HK2 <= 0 || H % HK1 != 0 || H % HK2 != 0) return 0;
+  if (mode != STREAMKL_GRAD_P2 && mode != STREAMKL_GRAD_P1) return 0;
+  if (deterministic != 1 || !head_dim_ok(d1) || !head_dim_ok(d2)) return 0;
+  if (tile_dim(d1) > 128 || tile_dim(d2) > 128) return 0;  // the wide-head passes need none
+  const int hkg = mode == STREAMKL_GRAD_P2 ? HK2 : HK1;
+  const size_t kg_heads = size_t(B) * hkg;
+  const size_t key_tiles = (size_t(NK) + skl::kTile - 1) / skl::kTile;
+  const size_t words = kg_heads + 2 + (H / hkg > 1 ? kg_heads * key_tiles : 0);
+  return (words * 4 + 15) / 16 * 16;
+}
+
+}  // extern "C"
+
+namespace {
+
+// The backward behind both entry points.  caller_ws: the scratch of a
+// deterministic call is the caller's `workspace` (checked against
+// streamkl_bwd_workspace_bytes); otherwise it comes from the stream's memory
+// pool and goes back to it on the stream.
+int bwd_impl(const void* q1, const void* k1, const void* q2, const void* k2, int B, int H, int HK1, int HK2,
+             int NQ, int NK, int d1, int d2, float scale1, float scale2, int causal, const float* kl,
+             const float* lse1, const float* lse2, const float* dkl, int mode, int deterministic, float* dq,
+             float* dk, bool caller_ws, void* workspace, size_t workspace_bytes, streamkl_stream_t stream) {
   bool empty = false;
   int s = check_problem(q1, k1, q2, k2, B, H, HK1, HK2, NQ, NK, d1, d2, scale1, causal, &empty);
   if (s == STREAMKL_OK && !scale_ok(scale2)) s = STREAMKL_INVALID_ARG;
@@ -328,20 +349,22 @@ int streamkl_bwd_gqa(const void* q1, const void* k1, const void* q2, const void*
   // deterministic: the same fused kernel in one launch, with every dQ
   // contribution rounded to its row's grid (fp32 sums exact in any order)
   // and, when query heads share a key head, their dK added in head order
-  // (the first stores).  Scratch, one stream-ordered block: the bound on |K|
-  // per key head, then the launch's ticket and abort word, then one dK count
-  // per (key head, key tile) when heads share key heads.
+  // (the first stores).  Scratch, one block: the bound on |K| per key head,
+  // then the launch's ticket and abort word, then one dK count per (key
+  // head, key tile) when heads share key heads.
   const size_t dq_bytes = size_t(B) * H * NQ * dg * 4;
   const size_t kg_heads = size_t(B) * hkg;
-  const size_t key_tiles = (size_t(NK) + skl::kTile - 1) / skl::kTile;
-  const size_t words = kg_heads + 2 + (gg > 1 ? kg_heads * key_tiles : 0);
+  const size_t ws_bytes = streamkl_bwd_workspace_bytes(B, H, HK1, HK2, NK, d1, d2, mode, 1);
+  if (caller_ws && (workspace == nullptr || !aligned16(workspace) || workspace_bytes < ws_bytes))
+    return STREAMKL_INVALID_ARG;
   if (!make_map_dq_wide(&m.dqw, dq, (long long)B * H, NQ, dg, &a.dq_box)) return STREAMKL_CUDA_ERROR;
   if (cudaMemsetAsync(dq, 0, dq_bytes, cs) != cudaSuccess) return STREAMKL_CUDA_ERROR;
-  unsigned* scratch = nullptr;
-  if (cudaMallocAsync(reinterpret_cast<void**>(&scratch), words * sizeof(unsigned), cs) != cudaSuccess)
+  unsigned* scratch = caller_ws ? static_cast<unsigned*>(workspace) : nullptr;
+  const bool pooled = !caller_ws;
+  if (pooled && cudaMallocAsync(reinterpret_cast<void**>(&scratch), ws_bytes, cs) != cudaSuccess)
     return STREAMKL_CUDA_ERROR;
   int rc = STREAMKL_OK;
-  if (cudaMemsetAsync(scratch, 0, words * sizeof(unsigned), cs) != cudaSuccess ||
+  if (cudaMemsetAsync(scratch, 0, ws_bytes, cs) != cudaSuccess ||
       skl::launch_kmax(mode == STREAMKL_GRAD_P2 ? k2 : k1, int(kg_heads), NK, dg, scratch, cs) != 0)
     rc = STREAMKL_CUDA_ERROR;
   a.dq_fixed = 1;
@@ -353,8 +376,29 @@ int streamkl_bwd_gqa(const void* q1, const void* k1, const void* q2, const void*
     a.dk_turns = words_i + kg_heads + 2;
   }
   if (rc == STREAMKL_OK && skl::launch_bwd_fused(m, t1, t2, a, cs) != 0) rc = STREAMKL_CUDA_ERROR;
-  if (cudaFreeAsync(scratch, cs) != cudaSuccess) rc = STREAMKL_CUDA_ERROR;
+  if (pooled && cudaFreeAsync(scratch, cs) != cudaSuccess) rc = STREAMKL_CUDA_ERROR;
   return rc;
+}
+
+}  // namespace
+
+extern "C" {
+
+int streamkl_bwd_gqa(const void* q1, const void* k1, const void* q2, const void* k2, int B, int H, int HK1,
+                     int HK2, int NQ, int NK, int d1, int d2, float scale1, float scale2, int causal,
+                     const float* kl, const float* lse1, const float* lse2, const float* dkl, int mode,
+                     int deterministic, float* dq, float* dk, streamkl_stream_t stream) {
+  return bwd_impl(q1, k1, q2, k2, B, H, HK1, HK2, NQ, NK, d1, d2, scale1, scale2, causal, kl, lse1, lse2, dkl,
+                  mode, deterministic, dq, dk, false, nullptr, 0, stream);
+}
+
+int streamkl_bwd_gqa_ws(const void* q1, const void* k1, const void* q2, const void* k2, int B, int H, int HK1,
+                        int HK2, int NQ, int NK, int d1, int d2, float scale1, float scale2, int causal,
+                        const float* kl, const float* lse1, const float* lse2, const float* dkl, int mode,
+                        int deterministic, float* dq, float* dk, void* workspace, size_t workspace_bytes,
+                        streamkl_stream_t stream) {
+  return bwd_impl(q1, k1, q2, k2, B, H, HK1, HK2, NQ, NK, d1, d2, scale1, scale2, causal, kl, lse1, lse2, dkl,
+                  mode, deterministic, dq, dk, true, workspace, workspace_bytes, stream);
 }
 
 int streamkl_bwd_scaled(const void* q1, const void* k1, const void* q2, const void* k2, int B, int H,

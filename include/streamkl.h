@@ -153,9 +153,10 @@ int streamkl_suggest_splits(int B, int H, int NQ, int NK, int causal);
  * |dQ_i| (from dKL_i, KL_i, the softmax scale and max |K| of the key head),
  * so the fp32 sums are exact in any order; the rounding is at most 2^-22 of
  * that bound per key tile (and at most 2^-127 absolute).  It reads K once
- * more (the bound), and takes 4 bytes per key head of the gradient side from
- * the stream's memory pool (cudaMallocAsync), released on the stream before
- * the call returns.
+ * more (the bound), and takes a few bytes of scratch (4 per key head of the
+ * gradient side, streamkl_bwd_workspace_bytes) from the stream's memory pool
+ * (cudaMallocAsync), released on the stream before the call returns;
+ * streamkl_bwd_gqa_ws takes it from the caller instead.
  * kl, lse1, lse2 must come from streamkl_fwd on the same inputs.
  */
 int streamkl_bwd(const void* q1, const void* k1, const void* q2, const void* k2,
@@ -220,6 +221,28 @@ int streamkl_bwd_gqa(const void* q1, const void* k1, const void* q2, const void*
                      float scale1, float scale2, int causal, const float* kl, const float* lse1,
                      const float* lse2, const float* dkl, int mode, int deterministic, float* dq,
                      float* dk, streamkl_stream_t stream);
+
+/*
+ * The deterministic backward's scratch from the caller instead of the
+ * stream's memory pool, for callers that must not let the library allocate.
+ * streamkl_bwd_workspace_bytes returns the bytes it needs: 0 unless
+ * deterministic = 1 with both head dims at most 128, else 4 per key head of
+ * the gradient side (B * HK_g), 8 more, and 4 per key head and key tile
+ * when query heads share key heads (H > HK_g), rounded up to 16; 0 for
+ * arguments the backward would reject.  streamkl_bwd_gqa_ws is
+ * streamkl_bwd_gqa with `workspace` (device memory, 16-byte aligned, owned
+ * by the caller, contents overwritten; may be null when 0 bytes are
+ * needed): INVALID_ARG when it is null, misaligned or smaller than needed.
+ * The results are bitwise those of streamkl_bwd_gqa.  Calls that overlap on
+ * the GPU must not share a workspace.
+ */
+size_t streamkl_bwd_workspace_bytes(int B, int H, int HK1, int HK2, int NK, int d1, int d2, int mode,
+                                    int deterministic);
+int streamkl_bwd_gqa_ws(const void* q1, const void* k1, const void* q2, const void* k2,
+                        int B, int H, int HK1, int HK2, int NQ, int NK, int d1, int d2,
+                        float scale1, float scale2, int causal, const float* kl, const float* lse1,
+                        const float* lse2, const float* dkl, int mode, int deterministic, float* dq,
+                        float* dk, void* workspace, size_t workspace_bytes, streamkl_stream_t stream);
 
 /*
  * Both-sides backward: the gradients of sum_i dkl_i * KL_i with respect to

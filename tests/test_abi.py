@@ -212,3 +212,19 @@ def test_gqa_empty_backward_zeroes_key_heads_only(L):
     # NQ = 0: nothing to compute, and with no dk buffer (size 0) nothing to zero
     assert L.streamkl_bwd_gqa(0, 0, 0, 0, 0, 8, 2, 2, 0, 128, 64, 64, 0.125, 0.125, 0, 0, 0, 0, 0, 0, 0, 0, 0,
                               None) == skl.STREAMKL_OK
+
+
+def test_backward_workspace_bytes():
+    # the deterministic backward's scratch: 4 bytes per gradient-side key head,
+    # 8 more, and 4 per key head and key tile when query heads share key heads
+    assert skl.streamkl_bwd_workspace_bytes(1, 32, 32, 32, 65536, 128, 128) == 144
+    assert skl.streamkl_bwd_workspace_bytes(1, 32, 8, 8, 16384, 128, 128) == (8 + 2 + 8 * 128) * 4 + 8
+    assert skl.streamkl_bwd_workspace_bytes(2, 4, 4, 1, 300, 64, 64, skl.STREAMKL_GRAD_P1) == 48
+    assert skl.streamkl_bwd_workspace_bytes(2, 4, 4, 1, 300, 64, 64, skl.STREAMKL_GRAD_P2) == \
+        (2 + 2 + 2 * 3) * 4 + 8
+    # none: the atomic mode, heads above 128 (two passes without atomics), bad arguments
+    assert skl.streamkl_bwd_workspace_bytes(1, 32, 32, 32, 4096, 128, 128, deterministic=False) == 0
+    assert skl.streamkl_bwd_workspace_bytes(1, 8, 8, 8, 4096, 256, 256) == 0
+    assert skl.streamkl_bwd_workspace_bytes(1, 6, 4, 4, 4096, 64, 64) == 0   # 4 does not divide 6
+    assert skl.streamkl_bwd_workspace_bytes(1, 4, 4, 4, 4096, 72, 64) == 0   # not a multiple of 16
+    assert skl.streamkl_bwd_workspace_bytes(1, 4, 4, 4, 4096, 64, 64, mode=2) == 0

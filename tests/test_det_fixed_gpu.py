@@ -143,3 +143,27 @@ def test_headline_size_deterministic_matches_fused():
     assert bool(torch.all(torch.isfinite(det[0])))
     worst = torch.argmax(err - tol)
     assert bool(torch.all(err <= tol)), f"row {worst.item()}: {err.flatten()[worst].item()} > {tol.flatten()[worst].item()}"
+
+
+def test_caller_workspace_gives_the_same_bits():
+    """streamkl_bwd_gqa_ws with the caller's scratch equals the pooled call bit
+    for bit, and rejects a missing or short workspace before enqueuing."""
+    w = Workload("fxw", 1, 4, 400, 400, 64, 64, True, 0.125, "independent", 0.0, 1.0, 214)
+    dev = [t.cuda() for t in generate_gqa(w, 2, 2)]
+    dkl = generate_dkl(w, "signed").cuda()
+    kl, l1, l2 = skl.streamkl_fwd_gqa(*dev, w.scale, w.scale, w.causal)
+    for mode in MODES:
+        need = skl.streamkl_bwd_workspace_bytes(w.B, w.H, 2, 2, w.NK, w.d1, w.d2, mode)
+        assert need > 0
+        ws = torch.full((need,), 0x5A, dtype=torch.uint8, device="cuda")  # contents must not matter
+        a = skl.streamkl_bwd_gqa(*dev, w.scale, w.scale, w.causal, kl, l1, l2, dkl, mode, True)
+        b = skl.streamkl_bwd_gqa_ws(*dev, w.scale, w.scale, w.causal, kl, l1, l2, dkl, ws, mode, True)
+        torch.cuda.synchronize()
+        assert skl.streamkl_get_device_status() == skl.STREAMKL_OK
+        assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+        with pytest.raises(skl.StreamKLError):
+            skl.streamkl_bwd_gqa_ws(*dev, w.scale, w.scale, w.causal, kl, l1, l2, dkl, ws[:need - 16], mode, True)
+        with pytest.raises(skl.StreamKLError):
+            skl.streamkl_bwd_gqa_ws(*dev, w.scale, w.scale, w.causal, kl, l1, l2, dkl, None, mode, True)
+        # the atomic mode needs no scratch
+        skl.streamkl_bwd_gqa_ws(*dev, w.scale, w.scale, w.causal, kl, l1, l2, dkl, None, mode, False)
