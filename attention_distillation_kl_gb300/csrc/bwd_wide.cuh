@@ -23,9 +23,11 @@
 // S2 [128,256), the accumulator [256, 256 + DG).  Warps 0-7 form dS (thread =
 // query row, as in the fused kernel) and at the end store the accumulator;
 // warp 8 issues the TMA loads; warp 9 owns TMEM and runs the MMA loop (one
-// elected lane issues).  Within a visitor tile the steps are serial (S, then
-// dS, then the gradient product), which is what the 512 TMEM columns allow at
-// these widths.
+// elected lane issues).  The 512 TMEM columns hold one S pair, so the dS
+// warps take their whole share of S into registers and release it at once:
+// the S products of tile v then run while dS of tile v - 1 is formed, and
+// the gradient product of tile v - 1 follows them (the ring carries the
+// blocks in that order).
 #pragma once
 
 #include "bwd_common.cuh"
@@ -49,7 +51,8 @@ struct WideLayout {
   static constexpr int kNb1 = OpTile<D1>::kBlocks, kNb2 = OpTile<D2>::kBlocks, kNbg = OpTile<DG>::kBlocks;
   static constexpr int kPerVisit = kNb1 + kNb2 + kNbg;  // ring blocks per visited tile
   static constexpr uint32_t oBar = oRing + kSlots * kSlot;
-  enum { B_OFULL = 0, B_VFULL = 1, B_VEMPTY = 9, B_SFULL = 17, B_DSFULL, B_GFULL, B_DONE, kNumBars };
+  enum { B_OFULL = 0, B_VFULL = 1, B_VEMPTY = 9, B_SFULL = 17, B_SFREE, B_DSFULL, B_DSEMPTY, B_GFULL, B_DONE,
+         kNumBars };
   static constexpr uint32_t oMisc = oBar + kNumBars * 8;
   static constexpr uint32_t kBytes = oMisc + 16;
   static constexpr uint32_t kAlloc = kBytes + 1024;
@@ -101,7 +104,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
   const Ctl ctl{abort_flag, a.status};
 
   if (threadIdx.x == 0) {
-    for (int b = 0; b < L::kNumBars; ++b) mbar_init(bar(b), b == L::B_DSFULL ? 8u : 1u);
+    for (int b = 0; b < L::kNumBars; ++b) mbar_init(bar(b), (b == L::B_DSFULL || b == L::B_SFREE) ? 8u : 1u);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -138,11 +141,14 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       const int z1 = kDK ? bh : bh / a.g1, z2 = kDK ? bh : bh / a.g2, zg = kP2 ? z2 : z1;
       int issued = 0;
       bool go = true;
-      for (int v = 0; v < nv && go; ++v) {
+      // one visited tile's blocks: its S operands (side 1, side 2) or its
+      // gradient operand, into the ring in the order the MMA loop takes them
+      auto put_blocks = [&](int v, bool grad) {
         const int r0 = kDK ? (qt_lo + v) * kTile : v * kTile;  // first row of the visited tile
+        const int b0 = grad ? L::kNb1 + L::kNb2 : 0, b1 = grad ? L::kPerVisit : L::kNb1 + L::kNb2;
 #pragma unroll 1
-        for (int blk = 0; blk < L::kPerVisit; ++blk) {
-          const int u = v * L::kPerVisit + blk, s = u % L::kSlots;
+        for (int blk = b0; blk < b1 && go; ++blk) {
+          const int u = issued, s = u % L::kSlots;
           if (!mbar_wait_polled(bar(L::B_VEMPTY + s), ((u / L::kSlots) & 1) ^ 1, ctl)) {
             go = false;
             break;
@@ -164,7 +170,13 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           }
           issued = u + 1;
         }
+      };
+      // the S products of tile v go before the gradient product of tile v - 1
+      for (int v = 0; v < nv && go; ++v) {
+        put_blocks(v, false);
+        if (v > 0) put_blocks(v - 1, true);
       }
+      if (go) put_blocks(nv - 1, true);
       if (*abort_flag) {  // let the copies already started land before the CTA exits
         const uint64_t lim = 200000000ull;
         mbar_drain(bar(L::B_OFULL), 0, lim);
@@ -183,61 +195,67 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     const uint64_t dsm = sdesc_sw128(sb + L::oDS, kTile * 128, 1024);  // dS^T, M-major
     const uint64_t dsk = sdesc_sw128(sb + L::oDS, 16, 1024);           // dS, K-major
     bool done = false;
-    if (nv > 0 && mbar_wait_warp(bar(L::B_OFULL), 0, ctl)) {
-      int v = 0;
-      for (; v < nv; ++v) {
-        bool go = true;
+    int u = 0;  // ring blocks taken, in the producer's order
+    // S1, S2 of visited tile v into TMEM (the dS warps have read the previous S)
+    auto s_products = [&](int v) {
+      (void)v;
 #pragma unroll 1
-        for (int blk = 0; blk < L::kNb1 + L::kNb2 && go; ++blk) {
-          const int u = v * L::kPerVisit + blk, s = u % L::kSlots;
-          if (!mbar_wait_warp(bar(L::B_VFULL + s), (u / L::kSlots) & 1, ctl)) {
-            go = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t vs = sb + L::oRing + s * L::kSlot;  // visitor block
-          // owner operand block kk / steps at offset off_k(kk); visitor block step jj at jj * 32
-          auto s_steps = [&](auto tile, uint32_t d, uint32_t owner, int b) {
-            using T = decltype(tile);
-            constexpr int kSteps = T::kBox / 16;
-#pragma unroll
-            for (int jj = 0; jj < kSteps; ++jj) {
-              const int kk = b * kSteps + jj;
-              const uint64_t od = T::desc_k(owner + T::off_k(kk)), vd = T::desc_k(vs + jj * 32);
-              // S = Q K^T with queries as M: pass 0 visits Q (A), pass 1 visits K (B)
-              if constexpr (kDK) mma_bf16_ss(leader, d, vd, od, id_s, kk > 0);
-              else mma_bf16_ss(leader, d, od, vd, id_s, kk > 0);
-            }
-          };
-          if (blk < L::kNb1) s_steps(T1{}, t_s1, sb + L::oO1, blk);
-          else s_steps(T2{}, t_s2, sb + L::oO2, blk - L::kNb1);
-          mma_commit(leader, bar(L::B_VEMPTY + s));
-        }
-        if (!go) break;
-        mma_commit(leader, bar(L::B_SFULL));  // also orders the previous gradient product before new dS
-        if (!mbar_wait_warp(bar(L::B_DSFULL), v & 1, ctl)) break;
+      for (int blk = 0; blk < L::kNb1 + L::kNb2; ++blk, ++u) {
+        const int s = u % L::kSlots;
+        if (!mbar_wait_warp(bar(L::B_VFULL + s), (u / L::kSlots) & 1, ctl)) return false;
         tc_fence_after();
-#pragma unroll 1
-        for (int c = 0; c < L::kNbg && go; ++c) {
-          const int u = v * L::kPerVisit + L::kNb1 + L::kNb2 + c, s = u % L::kSlots;
-          if (!mbar_wait_warp(bar(L::B_VFULL + s), (u / L::kSlots) & 1, ctl)) {
-            go = false;
-            break;
-          }
-          tc_fence_after();
-          const uint64_t gd = TG::desc_n(sb + L::oRing + s * L::kSlot);
+        const uint32_t vs = sb + L::oRing + s * L::kSlot;  // visitor block
+        // owner operand block kk / steps at offset off_k(kk); visitor block step jj at jj * 32
+        auto s_steps = [&](auto tile, uint32_t d, uint32_t owner, int b) {
+          using T = decltype(tile);
+          constexpr int kSteps = T::kBox / 16;
 #pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk) {
-            const uint64_t ad = kDK ? sdesc_add(dsm, kk * 2048)
-                                    : sdesc_add(dsk, (kk >> 2) * (kTile * 128) + (kk & 3) * 32);
-            mma_bf16_ss(leader, t_g + c * TG::kBox, ad, sdesc_add(gd, TG::off_n(kk)), id_g,
-                        (v > 0 || kk > 0) ? 1u : 0u);
+          for (int jj = 0; jj < kSteps; ++jj) {
+            const int kk = b * kSteps + jj;
+            const uint64_t od = T::desc_k(owner + T::off_k(kk)), vd = T::desc_k(vs + jj * 32);
+            // S = Q K^T with queries as M: pass 0 visits Q (A), pass 1 visits K (B)
+            if constexpr (kDK) mma_bf16_ss(leader, d, vd, od, id_s, kk > 0);
+            else mma_bf16_ss(leader, d, od, vd, id_s, kk > 0);
           }
-          mma_commit(leader, bar(L::B_VEMPTY + s));
-        }
-        if (!go) break;
+        };
+        if (blk < L::kNb1) s_steps(T1{}, t_s1, sb + L::oO1, blk);
+        else s_steps(T2{}, t_s2, sb + L::oO2, blk - L::kNb1);
+        mma_commit(leader, bar(L::B_VEMPTY + s));
       }
-      done = v == nv && !*abort_flag;
+      mma_commit(leader, bar(L::B_SFULL));
+      return true;
+    };
+    // the gradient product of visited tile v, once its dS is in shared memory;
+    // the dS tile is free again when these products are done
+    auto grad_product = [&](int v) {
+      if (!mbar_wait_warp(bar(L::B_DSFULL), v & 1, ctl)) return false;
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < L::kNbg; ++c, ++u) {
+        const int s = u % L::kSlots;
+        if (!mbar_wait_warp(bar(L::B_VFULL + s), (u / L::kSlots) & 1, ctl)) return false;
+        tc_fence_after();
+        const uint64_t gd = TG::desc_n(sb + L::oRing + s * L::kSlot);
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          const uint64_t ad = kDK ? sdesc_add(dsm, kk * 2048)
+                                  : sdesc_add(dsk, (kk >> 2) * (kTile * 128) + (kk & 3) * 32);
+          mma_bf16_ss(leader, t_g + c * TG::kBox, ad, sdesc_add(gd, TG::off_n(kk)), id_g,
+                      (v > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(leader, bar(L::B_VEMPTY + s));
+      }
+      mma_commit(leader, bar(L::B_DSEMPTY));
+      return true;
+    };
+    if (nv > 0 && mbar_wait_warp(bar(L::B_OFULL), 0, ctl) && s_products(0)) {
+      bool go = true;
+      for (int v = 1; v < nv && go; ++v) {
+        // S of tile v as soon as the dS warps hold S of tile v - 1 in
+        // registers, so it runs while they form dS of tile v - 1
+        go = mbar_wait_warp(bar(L::B_SFREE), (v - 1) & 1, ctl) && s_products(v) && grad_product(v - 1);
+      }
+      done = go && grad_product(nv - 1) && !*abort_flag;
     }
     if (done) mma_commit(leader, bar(L::B_GFULL));
     // every MMA this warp issued has finished before TMEM is released
@@ -276,23 +294,27 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       tc_fence_after();
       const int lim = (a.causal ? min(tq0 + row + off, a.NK - 1) : a.NK - 1) - tk0;  // last visible key
       const bool need_mask = (tk0 + kTile > a.NK) || (a.causal && tq0 < tk0 + kTile - 1 - off);
+      // this warp's 64 columns of S1 and S2 into registers, then S is free
+      // for the next tile's products while dS is formed
+      const int col = wg * 64;
+      uint32_t x1a[32], x2a[32], x1b[32], x2b[32];
+      tmem_ld2x32(t_s1 + lane_off + col, t_s2 + lane_off + col, x1a, x2a);
+      tmem_ld2x32(t_s1 + lane_off + col + 32, t_s2 + lane_off + col + 32, x1b, x2b);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::B_SFREE));
       uint32_t dsr[32];
-#pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        const int col = wg * 64 + ch * 32;
-        uint32_t x1[32], x2[32];
-        tmem_ld2x32(t_s1 + lane_off + col, t_s2 + lane_off + col, x1, x2);
-        if (need_mask)
-          ds_chunk_row<MODE, true>(x1, x2, C1, C2, S1, NR, NA, NB, WW, lim - col, dsr + ch * 16);
-        else
-          ds_chunk_row<MODE, false>(x1, x2, C1, C2, S1, NR, NA, NB, WW, 0, dsr + ch * 16);
+      if (need_mask) {
+        ds_chunk_row<MODE, true>(x1a, x2a, C1, C2, S1, NR, NA, NB, WW, lim - col, dsr);
+        ds_chunk_row<MODE, true>(x1b, x2b, C1, C2, S1, NR, NA, NB, WW, lim - col - 32, dsr + 16);
+      } else {
+        ds_chunk_row<MODE, false>(x1a, x2a, C1, C2, S1, NR, NA, NB, WW, 0, dsr);
+        ds_chunk_row<MODE, false>(x1b, x2b, C1, C2, S1, NR, NA, NB, WW, 0, dsr + 16);
       }
-      // S may be overwritten once every dS warp has read it; the previous
-      // gradient product finished before S of this step was committed, so
-      // the dS tile is free
+      // the previous tile's gradient product is done reading the dS tile
+      if (v > 0 && !mbar_wait_warp(bar(L::B_DSEMPTY), (v - 1) & 1, ctl)) break;
       store_half_row_sw128(sb + L::oDS, row, wg, dsr);
       fence_proxy_async_smem();
-      tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(L::B_DSFULL));
     }
