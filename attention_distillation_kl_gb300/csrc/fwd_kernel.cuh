@@ -194,6 +194,63 @@ __device__ __forceinline__ void fold_pair(RowStats& st, const uint32_t (&xa1)[32
   st.l2 = fmaf(st.l2, a2, l2a + l2b);
 }
 
+// Fast path of fold_pair: the 64 columns exponentiated against the running
+// maxima as they stand, with no maximum pass and no rescale.  The online
+// recurrence holds for any reference at or above the values seen so far, and
+// fp32 keeps its relative precision at any scale, so a reference that is
+// not the exact maximum changes nothing as long as no term overflows.
+// Returns false -- the state untouched -- when a partial sum reaches 2^64
+// (a logit above the reference by more than 64 / c, the first tile of a row
+// whose reference is still kNegBig, or a non-finite input): the caller then
+// folds the tile exactly with fold_pair.
+template <bool kMask>
+__device__ __forceinline__ bool fold_pair_fast(RowStats& st, const uint32_t (&xa1)[32], const uint32_t (&xa2)[32],
+                                               const uint32_t (&xb1)[32], const uint32_t (&xb2)[32], float c1,
+                                               float c2, float nrho, int lim_rel) {
+  const uint64_t C1 = f2(c1, c1), C2 = f2(c2, c2), NR = f2(nrho, nrho);
+  const float nb1 = -st.m1 * c1, nb2 = -st.m2 * c2;
+  const uint64_t NB1 = f2(nb1, nb1), NB2 = f2(nb2, nb2);
+  uint64_t L1a = f2(0.f, 0.f), L2a = L1a, ACCa = L1a, L1b = L1a, L2b = L1a, ACCb = L1a;
+#pragma unroll
+  for (int k = 0; k < 32; k += 2) {
+    const uint64_t XA1 = f2(__uint_as_float(xa1[k]), __uint_as_float(xa1[k + 1]));
+    const uint64_t XA2 = f2(__uint_as_float(xa2[k]), __uint_as_float(xa2[k + 1]));
+    const uint64_t XB1 = f2(__uint_as_float(xb1[k]), __uint_as_float(xb1[k + 1]));
+    const uint64_t XB2 = f2(__uint_as_float(xb2[k]), __uint_as_float(xb2[k + 1]));
+    float e1a, e1b, e2a, e2b, g1a, g1b, g2a, g2b;
+    f2_split(f2_fma(XA1, C1, NB1), e1a, e1b);
+    f2_split(f2_fma(XA2, C2, NB2), e2a, e2b);
+    f2_split(f2_fma(XB1, C1, NB1), g1a, g1b);
+    f2_split(f2_fma(XB2, C2, NB2), g2a, g2b);
+    float p1a = ex2(e1a), p1b = ex2(e1b), p2a = ex2(e2a), p2b = ex2(e2b);
+    float q1a = ex2(g1a), q1b = ex2(g1b), q2a = ex2(g2a), q2b = ex2(g2b);
+    if (kMask) {
+      if (k > lim_rel) { p1a = 0.f; p2a = 0.f; }
+      if (k + 1 > lim_rel) { p1b = 0.f; p2b = 0.f; }
+      if (k + 32 > lim_rel) { q1a = 0.f; q2a = 0.f; }
+      if (k + 33 > lim_rel) { q1b = 0.f; q2b = 0.f; }
+    }
+    const uint64_t P1 = f2(p1a, p1b), Q1 = f2(q1a, q1b);
+    L1a = f2_add(L1a, P1);
+    L2a = f2_add(L2a, f2(p2a, p2b));
+    ACCa = f2_fma(P1, f2_fma(XA2, NR, XA1), ACCa);
+    L1b = f2_add(L1b, Q1);
+    L2b = f2_add(L2b, f2(q2a, q2b));
+    ACCb = f2_fma(Q1, f2_fma(XB2, NR, XB1), ACCb);
+  }
+  const uint64_t L1 = f2_add(L1a, L1b), L2 = f2_add(L2a, L2b), ACC = f2_add(ACCa, ACCb);
+  float l1a, l1b, l2a, l2b, aca, acb;
+  f2_split(L1, l1a, l1b);
+  f2_split(L2, l2a, l2b);
+  f2_split(ACC, aca, acb);
+  const float l1 = l1a + l1b, l2 = l2a + l2b;
+  if (!(l1 < 18446744073709551616.f && l2 < 18446744073709551616.f)) return false;  // 2^64
+  st.l1 += l1;
+  st.acc += aca + acb;
+  st.l2 += l2;
+  return true;
+}
+
 template <int D1, int D2>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tq1, const __grid_constant__ CUtensorMap tk1,
@@ -394,21 +451,30 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tc_fence_after();
       const int k0 = (kt_lo + j) * kTile;
       const bool need_mask = (k0 + kTile > a.NK) || (a.causal && k0 + kTile - 1 > q0 + off);
-      // this warpgroup's 64 columns of S1 and S2 in one go; S is released
-      // before the fold, so the MMA of the next tile but one can start
+      // this warpgroup's 64 columns of S1 and S2 in one go, folded against
+      // the running maxima; a row that finds a new maximum (rare after its
+      // first tile) reads its columns again and folds them exactly.  S is
+      // released after the fold: the other buffer keeps the MMA a tile ahead
       static_assert(kColsPerWG == 64, "fold_pair takes 64 columns");
       const int col = wg * kColsPerWG;
       uint32_t xa1[32], xa2[32], xb1[32], xb2[32];
       const uint32_t t = tmem + lane_off + uint32_t(b * 256 + col);
       tmem_ld2x32(t, t + 128, xa1, xa2);
       tmem_ld2x32(t + 32, t + 160, xb1, xb2);
+      const int lr = need_mask ? lim - (k0 + col) : 0;
+      const bool fast = need_mask ? fold_pair_fast<true>(st, xa1, xa2, xb1, xb2, c1, c2, nrho, lr)
+                                  : fold_pair_fast<false>(st, xa1, xa2, xb1, xb2, c1, c2, nrho, 0);
+      if (__any_sync(0xffffffffu, !fast)) {  // the TMEM loads are warp-wide
+        tmem_ld2x32(t, t + 128, xa1, xa2);
+        tmem_ld2x32(t + 32, t + 160, xb1, xb2);
+        if (!fast) {
+          if (need_mask) fold_pair<true>(st, xa1, xa2, xb1, xb2, c1, c2, nrho, lr);
+          else fold_pair<false>(st, xa1, xa2, xb1, xb2, c1, c2, nrho, 0);
+        }
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_sempty(b));
-      if (need_mask)
-        fold_pair<true>(st, xa1, xa2, xb1, xb2, c1, c2, nrho, lim - (k0 + col));
-      else
-        fold_pair<false>(st, xa1, xa2, xb1, xb2, c1, c2, nrho, 0);
     }
     // merge the column shares of every row (warpgroups 1.. -> warpgroup 0)
     // with the same algebra as the key-split reduce
