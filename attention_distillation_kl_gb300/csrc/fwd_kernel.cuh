@@ -82,59 +82,14 @@ struct RowStats {
   float m1, m2, l1, l2, acc;
 };
 
-// Folds 32 consecutive key columns into the running state.  Columns k with
-// k > lim_rel are masked (causal or past NK): they neither move the maxima
-// nor add to the sums.  Pairs of columns go through the packed FP32 pipe.
-// c1, c2: s log2 e of each side; nrho = -s2 / s1 (x1 - rho x2 is one fma,
-// exactly x1 - x2 when the scales are equal).
-template <bool kMask>
-__device__ __forceinline__ void fold_chunk(RowStats& st, const uint32_t (&x1u)[32],
-                                           const uint32_t (&x2u)[32], float c1, float c2, float nrho,
-                                           int lim_rel) {
-  float t1 = st.m1, t2 = st.m2;
-#pragma unroll
-  for (int k = 0; k < 32; k += 2) {
-    const bool oa = !kMask || k <= lim_rel, ob = !kMask || k + 1 <= lim_rel;
-    t1 = max3(t1, oa ? __uint_as_float(x1u[k]) : kNegBig, ob ? __uint_as_float(x1u[k + 1]) : kNegBig);
-    t2 = max3(t2, oa ? __uint_as_float(x2u[k]) : kNegBig, ob ? __uint_as_float(x2u[k + 1]) : kNegBig);
-  }
-  const float a1 = ex2((st.m1 - t1) * c1);
-  const float a2 = ex2((st.m2 - t2) * c2);
-  st.m1 = t1;
-  st.m2 = t2;
-  const uint64_t C1 = f2(c1, c1), C2 = f2(c2, c2), NR = f2(nrho, nrho);
-  const uint64_t NB1 = f2(-t1 * c1, -t1 * c1), NB2 = f2(-t2 * c2, -t2 * c2);
-  uint64_t L1 = f2(0.f, 0.f), L2 = L1, ACC = L1;
-#pragma unroll
-  for (int k = 0; k < 32; k += 2) {
-    const uint64_t X1 = f2(__uint_as_float(x1u[k]), __uint_as_float(x1u[k + 1]));
-    const uint64_t X2 = f2(__uint_as_float(x2u[k]), __uint_as_float(x2u[k + 1]));
-    float e1a, e1b, e2a, e2b;
-    f2_split(f2_fma(X1, C1, NB1), e1a, e1b);
-    f2_split(f2_fma(X2, C2, NB2), e2a, e2b);
-    float p1a = ex2(e1a), p1b = ex2(e1b), p2a = ex2(e2a), p2b = ex2(e2b);
-    if (kMask) {
-      if (k > lim_rel) { p1a = 0.f; p2a = 0.f; }
-      if (k + 1 > lim_rel) { p1b = 0.f; p2b = 0.f; }
-    }
-    const uint64_t P1 = f2(p1a, p1b);
-    L1 = f2_add(L1, P1);
-    L2 = f2_add(L2, f2(p2a, p2b));
-    ACC = f2_fma(P1, f2_fma(X2, NR, X1), ACC);
-  }
-  float l1a, l1b, l2a, l2b, aca, acb;
-  f2_split(L1, l1a, l1b);
-  f2_split(L2, l2a, l2b);
-  f2_split(ACC, aca, acb);
-  st.l1 = fmaf(st.l1, a1, l1a + l1b);
-  st.acc = fmaf(st.acc, a1, aca + acb);
-  st.l2 = fmaf(st.l2, a2, l2a + l2b);
-}
-
-// Folds two 32-column chunks (64 consecutive key columns) into the running
-// state at once: the two chunks' maxima and sums run as independent chains
-// (twice the instruction-level parallelism of two fold_chunk calls) and the
-// state is rescaled once.  lim_rel as in fold_chunk, for the first chunk.
+// Folds 64 consecutive key columns (two 32-column chunks) into the running
+// state exactly: the chunks' maxima and sums run as independent chains (for
+// instruction-level parallelism) and the state is rescaled once.  Columns k
+// with k > lim_rel (relative to the first chunk; causal, or past NK) are
+// masked: they neither move the maxima nor add to the sums.  Pairs of
+// columns go through the packed FP32 pipe.  c1, c2: s log2 e of each side;
+// nrho = -s2 / s1 (x1 - rho x2 is one fma, exactly x1 - x2 when the scales
+// are equal).
 template <bool kMask>
 __device__ __forceinline__ void fold_pair(RowStats& st, const uint32_t (&xa1)[32], const uint32_t (&xa2)[32],
                                           const uint32_t (&xb1)[32], const uint32_t (&xb2)[32], float c1,

@@ -41,7 +41,7 @@ UNIT = "TFLOP/s"
 TRAFFIC = {
     # dram__bytes_read.sum + dram__bytes_write.sum of one full-size launch
     "bwd_fused": {"bytes": 3297298688 + 2138713600, "src_sha": "e5c4ca92ededa74c"},
-    "fwd": {"bytes": 2159809280 + 28598272, "src_sha": "33eeba01c9bfe0ab"},
+    "fwd": {"bytes": 2159809280 + 28598272, "src_sha": "eeff81aff37aff83"},
 }
 
 
