@@ -13,7 +13,7 @@
 // query/key tile pair, dQ through atomics).  One CTA owns a 128-key tile and
 // walks the query tiles that can see it.  GB300 mapping, 15 or 16 warps:
 //   warp 12    TMA: K1, K2 once; per query tile Q_o (single buffer) and Q_g
-//              (double buffer; it is read again by the dK product)
+//              (two or three buffers; it is read again by the dK product)
 //   warp 13    TMEM owner, S issuer:
 //                S1 = Q1 K1^T, S2 = Q2 K2^T      (M = queries, N = keys)
 //   warp 14    dK issuer:   dK += dS^T Q_g       (accumulates in TMEM)
@@ -67,13 +67,21 @@ struct BwdLayout {
   static constexpr uint32_t kDS = kTile * kTile * 2;
   static constexpr uint32_t kK1 = kTile * D1 * 2, kK2 = kTile * D2 * 2;
   static constexpr uint32_t kQo = kTile * DO * 2, kQg = kTile * DG * 2;
-  static constexpr uint32_t oDS = 0, oK1 = kDS, oK2 = oK1 + kK1, oQo = oK2 + kK2, oQg = oQo + kQo;
-  static constexpr uint32_t oStage = oQg + 2 * kQg;  // dQ staging: 4 warps x kDqBoxes x kDqBoxBytes
-  static constexpr uint32_t oBar = oStage + 4 * kDqBoxes * kDqBoxBytes;
   enum {
-    B_KFULL, B_QOFULL, B_QOEMPTY, B_QGFULL0, B_QGFULL1, B_QGEMPTY0, B_QGEMPTY1, B_SFULL, B_SFREE,
-    B_DSFULL, B_DSEMPTY, B_DQFULL, B_DQEMPTY, B_DKFULL, B_DONE, kNumBars
+    B_KFULL, B_QOFULL, B_QOEMPTY, B_QGFULL0, B_QGFULL1, B_QGFULL2, B_QGEMPTY0, B_QGEMPTY1, B_QGEMPTY2,
+    B_SFULL, B_SFREE, B_DSFULL, B_DSEMPTY, B_DQFULL, B_DQEMPTY, B_DKFULL, B_DONE, kNumBars
   };
+  // Q_g buffers: its buffer of tile t is free again only when the dK
+  // product of tile t has run, and that product comes late in the tile (it
+  // waits for dS and for the next tile's S to be queued), so two buffers
+  // chain the reload of tile t + 2 to the dK of tile t; a third buffer,
+  // where it fits (every pair of head dims but 128 and 128), takes the
+  // reload off that chain
+  static constexpr uint32_t kFixed = kDS + kK1 + kK2 + kQo + 4 * kDqBoxes * kDqBoxBytes + kNumBars * 8 + 32;
+  static constexpr int kQgBufs = kFixed + 3 * kQg + 1024 <= 232448 ? 3 : 2;
+  static constexpr uint32_t oDS = 0, oK1 = kDS, oK2 = oK1 + kK1, oQo = oK2 + kK2, oQg = oQo + kQo;
+  static constexpr uint32_t oStage = oQg + kQgBufs * kQg;  // dQ staging: 4 warps x kDqBoxes x kDqBoxBytes
+  static constexpr uint32_t oBar = oStage + 4 * kDqBoxes * kDqBoxBytes;
   static constexpr uint32_t oMisc = oBar + kNumBars * 8;
   static constexpr uint32_t kBytes = oMisc + 32;
   static constexpr uint32_t kAlloc = kBytes + 1024;
@@ -201,8 +209,8 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
         if (!mbar_wait_polled(bar(L::B_QOEMPTY), (i & 1) ^ 1, ctl)) break;
         mbar_arrive_expect_tx(bar(L::B_QOFULL), L::kQo);
         TO::load(sb + L::oQo, tqo, bar(L::B_QOFULL), q0, bh);
-        const int g = i & 1;
-        if (!mbar_wait_polled(bar(L::B_QGEMPTY0 + g), ((i >> 1) & 1) ^ 1, ctl)) break;
+        const int g = i % L::kQgBufs;
+        if (!mbar_wait_polled(bar(L::B_QGEMPTY0 + g), ((i / L::kQgBufs) & 1) ^ 1, ctl)) break;
         mbar_arrive_expect_tx(bar(L::B_QGFULL0 + g), L::kQg);
         TG::load(sb + L::oQg + g * L::kQg, tqg, bar(L::B_QGFULL0 + g), q0, bh);
         issued = i + 1;
@@ -211,8 +219,8 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
         const uint64_t lim = 200000000ull;
         mbar_drain(bar(L::B_KFULL), 0, lim);
         if (issued > 0) mbar_drain(bar(L::B_QOFULL), (issued - 1) & 1, lim);
-        for (int i = issued > 2 ? issued - 2 : 0; i < issued; ++i)
-          mbar_drain(bar(L::B_QGFULL0 + (i & 1)), (i >> 1) & 1, lim);
+        for (int i = issued > L::kQgBufs ? issued - L::kQgBufs : 0; i < issued; ++i)
+          mbar_drain(bar(L::B_QGFULL0 + i % L::kQgBufs), (i / L::kQgBufs) & 1, lim);
       }
     }
   } else if (warp == 13) {
@@ -238,10 +246,10 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
         if constexpr (kP2) s_product(T1{}, t_s1, sb + L::oQo, sb + L::oK1);
         else s_product(T2{}, t_s2, sb + L::oQo, sb + L::oK2);
         mma_commit(1u, bar(L::B_QOEMPTY));
-        if (!mbar_wait_polled(bar(L::B_QGFULL0 + (i & 1)), (i >> 1) & 1, ctl)) break;
+        if (!mbar_wait_polled(bar(L::B_QGFULL0 + i % L::kQgBufs), (i / L::kQgBufs) & 1, ctl)) break;
         tc_fence_after();
-        if constexpr (kP2) s_product(T2{}, t_s2, sb + L::oQg + (i & 1) * L::kQg, sb + L::oK2);
-        else s_product(T1{}, t_s1, sb + L::oQg + (i & 1) * L::kQg, sb + L::oK1);
+        if constexpr (kP2) s_product(T2{}, t_s2, sb + L::oQg + (i % L::kQgBufs) * L::kQg, sb + L::oK2);
+        else s_product(T1{}, t_s1, sb + L::oQg + (i % L::kQgBufs) * L::kQg, sb + L::oK1);
         mma_commit(1u, bar(L::B_SFULL));
         *s_queued = i + 1;
       }
@@ -264,12 +272,12 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
           if (!mbar_wait_polled(bar(L::B_DSFULL), t & 1, ctl)) break;
           wait_s_queued(s_queued, t + 1 < n ? t + 2 : 0);
           tc_fence_after();
-          const uint64_t qgn = TG::desc_n(sb + L::oQg + (t & 1) * L::kQg);
+          const uint64_t qgn = TG::desc_n(sb + L::oQg + (t % L::kQgBufs) * L::kQg);
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk)
             mma_bf16_ss(1u, t_dk, sdesc_add(dsm, kk * 2048), sdesc_add(qgn, TG::off_n(kk)), id_dk,
                         (t > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(1u, bar(L::B_QGEMPTY0 + (t & 1)));  // Q_g(t) may be reloaded
+          mma_commit(1u, bar(L::B_QGEMPTY0 + t % L::kQgBufs));  // Q_g(t) may be reloaded
           if (kDq) {
             // dK and the Q_g release above did not wait for the dQ accumulator
             if (!mbar_wait_polled(bar(L::B_DQEMPTY), (t & 1) ^ 1, ctl)) break;
