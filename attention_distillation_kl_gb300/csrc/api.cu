@@ -426,7 +426,7 @@ int streamkl_bwd_both(const void* q1, const void* k1, const void* q2, const void
   if (s == STREAMKL_OK && !scale_ok(scale2)) s = STREAMKL_INVALID_ARG;
   if (s != STREAMKL_OK) return s;
   if (deterministic != 0 && deterministic != 1) return STREAMKL_INVALID_ARG;
-  if (d1 != d2 || tile_dim(d1) > 64 || deterministic || empty) {
+  if (d1 != d2 || tile_dim(d1) > 64 || empty) {
     // one recompute per side (the single-side kernels; they also handle empty problems)
     s = streamkl_bwd_scaled(q1, k1, q2, k2, B, H, NQ, NK, d1, d2, scale1, scale2, causal, kl, lse1, lse2,
                             dkl, STREAMKL_GRAD_P2, deterministic, dq2, dk2, stream);
@@ -451,7 +451,23 @@ int streamkl_bwd_both(const void* q1, const void* k1, const void* q2, const void
     return STREAMKL_CUDA_ERROR;
   skl::BwdArgs a{B * H, NQ, NK, causal, STREAMKL_GRAD_P2, d1, 1, 1, -1, scale1, scale2, kl, lse1, lse2,
                  dkl, dq1, dk1, st, dq2, dk2};
-  return as_status(skl::launch_bwd_both(m, tile_dim(d1), a, cs));
+  if (!deterministic) return as_status(skl::launch_bwd_both(m, tile_dim(d1), a, cs));
+  // deterministic: both dQ sides on their rows' grids (dK is stored by one
+  // CTA per key tile anyway); the bound on |K| of both sides' key heads in
+  // a scratch block from the stream's pool
+  const size_t kbytes = size_t(2) * B * H * sizeof(unsigned);
+  unsigned* kmax = nullptr;
+  if (cudaMallocAsync(reinterpret_cast<void**>(&kmax), kbytes, cs) != cudaSuccess) return STREAMKL_CUDA_ERROR;
+  int rc = STREAMKL_OK;
+  if (cudaMemsetAsync(kmax, 0, kbytes, cs) != cudaSuccess ||
+      skl::launch_kmax(k1, B * H, NK, d1, kmax, cs) != 0 ||
+      skl::launch_kmax(k2, B * H, NK, d2, kmax + size_t(B) * H, cs) != 0)
+    rc = STREAMKL_CUDA_ERROR;
+  a.dq_fixed = 1;
+  a.kmax = kmax;
+  if (rc == STREAMKL_OK && skl::launch_bwd_both(m, tile_dim(d1), a, cs) != 0) rc = STREAMKL_CUDA_ERROR;
+  if (cudaFreeAsync(kmax, cs) != cudaSuccess) rc = STREAMKL_CUDA_ERROR;
+  return rc;
 }
 
 const char* streamkl_status_string(int status) {

@@ -284,6 +284,33 @@ __global__ void __launch_bounds__(kBothThreads, 1)
     const uint32_t stage = sb + L::oStage + w4 * (kBothBoxes * 2048);
     const uint32_t swz = (lane >> 1) & 3;
     int nred = 0;
+    // deterministic mode: every value rounded to its row's grid before it is
+    // staged (dq_fixed_exp: mode P1's bound for dQ1, mode P2's for dQ2), so
+    // the fp32 reduce-adds are exact in any order; dKL and KL of this
+    // thread's row are loaded a tile ahead
+    const bool fixed = a.dq_fixed != 0;
+    const float kmax1 = fixed ? __uint_as_float(a.kmax[bh] << 16) : 0.f;
+    const float kmax2 = fixed ? __uint_as_float(a.kmax[a.BH + bh] << 16) : 0.f;
+    float dkl_nx = 0.f, kl_nx = 0.f;
+    auto load_row = [&](int i) {
+      const int qi = (qt_lo + i) * kTile + row;
+      if (fixed && qi < a.NQ && SKL_CHECK(a.status, bh < a.BH)) {
+        const size_t idx = size_t(bh) * a.NQ + qi;
+        dkl_nx = a.dkl[idx];
+        kl_nx = a.kl[idx];
+      }
+    };
+    auto to_grid = [&](uint32_t (&x)[32], float me) {  // (x + me) - me, two values at a time
+      const uint64_t ME = f2(me, me);
+#pragma unroll
+      for (int j = 0; j < 32; j += 2) {
+        float q0, q1;
+        f2_split(f2_sub(f2_add(f2(__uint_as_float(x[j]), __uint_as_float(x[j + 1])), ME), ME), q0, q1);
+        x[j] = __float_as_uint(q0);
+        x[j + 1] = __float_as_uint(q1);
+      }
+    };
+    if (n > 0) load_row(0);
     if (lane == 0) {
       tma_prefetch_desc(&tdq1);
       tma_prefetch_desc(&tdq2);
@@ -292,6 +319,12 @@ __global__ void __launch_bounds__(kBothThreads, 1)
       if (!mbar_wait_warp(bar(L::B_DQFULL), i & 1, ctl)) break;
       tc_fence_after();
       const int r0 = (qt_lo + i) * kTile + w4 * 32;  // first query row of this warp
+      float me[2] = {0.f, 0.f};
+      if (fixed) {
+        me[0] = 1.5f * exp2_int(23 - dq_fixed_exp(STREAMKL_GRAD_P1, a.scale1, dkl_nx, kl_nx, kmax1));
+        me[1] = 1.5f * exp2_int(23 - dq_fixed_exp(STREAMKL_GRAD_P2, a.scale2, dkl_nx, kl_nx, kmax2));
+      }
+      if (i + 1 < n) load_row(i + 1);
 #pragma unroll
       for (int side = 0; side < 2; ++side) {
         uint32_t v[kHalves][32];
@@ -301,6 +334,10 @@ __global__ void __launch_bounds__(kBothThreads, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(L::B_DQEMPTY));
+        }
+        if (fixed) {
+#pragma unroll
+          for (int x = 0; x < kHalves; ++x) to_grid(v[x], me[side]);
         }
 #pragma unroll
         for (int h = 0; h < 2 * kHalves; ++h) {

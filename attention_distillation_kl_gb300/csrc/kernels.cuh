@@ -52,7 +52,8 @@ struct BwdArgs {
   // Fused backward, deterministic mode: every dQ contribution rounded to its
   // row's grid (dq_fixed_exp) so the fp32 sums are exact in any order.
   // kmax: per key head of the gradient side, the largest |K| as bf16
-  // magnitude bits (launch_kmax).
+  // magnitude bits (launch_kmax); the both-sides kernel reads side 1's at
+  // [0, BH) and side 2's at [BH, 2 BH).
   int dq_fixed;
   const unsigned* kmax;
   // Deterministic mode with grouped key heads, one launch for all query

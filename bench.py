@@ -381,8 +381,9 @@ def gqa_timing(skl, stream):
 
 
 def both_sides_timing(skl, stream, d=64):
-    """Both-sides backward in one pass against the two single-side passes,
-    on a d1 = d2 = d problem (16K tokens x 32 heads, causal)."""
+    """Both-sides backward in one pass (atomic and deterministic) against the
+    two single-side passes, on a d1 = d2 = d problem (16K tokens x 32 heads,
+    causal)."""
     from attention_distillation_kl_gb300.workloads import Workload
     w = Workload(f"both-d{d}", 1, 32, 16384, 16384, d, d, True, 1 / np.sqrt(d), "independent", 0.0, 1.0, 1006)
     dev = [t.cuda() for t in generate(w)]
@@ -396,6 +397,8 @@ def both_sides_timing(skl, stream, d=64):
                                                       skl.STREAMKL_GRAD_P1, False, bufs[0], bufs[1]), stream)
     out["bwd_both_ms"] = timed(lambda: skl.streamkl_bwd_both(*dev, w.scale, w.scale, w.causal, kl, l1, l2, dkl,
                                                              False, *bufs), stream)
+    out["bwd_both_det_ms"] = timed(lambda: skl.streamkl_bwd_both(*dev, w.scale, w.scale, w.causal, kl, l1, l2, dkl,
+                                                                 True, *bufs), stream)
     # two S products and four gradient products, 2 d flops each per pair
     out["bwd_both_tflops"] = 12 * d * w.pairs / (out["bwd_both_ms"] * 1e-3) / 1e12
     del dev, bufs

@@ -248,10 +248,12 @@ int streamkl_bwd_gqa_ws(const void* q1, const void* k1, const void* q2, const vo
  * Both-sides backward: the gradients of sum_i dkl_i * KL_i with respect to
  * both distributions (dq1, dk1 with head dim d1; dq2, dk2 with d2; fp32,
  * fully overwritten), from one recompute of S1 and S2 per tile pair when
- * d1 = d2 <= 64 and deterministic = 0.  (A widening of the method: the
- * article's two modes share P1 and P2.)  Other head-dimension pairs (above
- * 64 the four accumulators do not fit beside S1 and S2 in tensor memory;
- * unequal pairs have no one-pass kernel) and the deterministic mode run the
+ * d1 = d2 <= 64.  (A widening of the method: the article's two modes share
+ * P1 and P2.)  deterministic = 1 rounds both sides' dQ contributions to
+ * their rows' grids as streamkl_bwd does (mode P1's bound for dq1, mode
+ * P2's for dq2; scratch of 8 bytes per head from the stream's pool).  Other
+ * head-dimension pairs (above 64 the four accumulators do not fit beside S1
+ * and S2 in tensor memory; unequal pairs have no one-pass kernel) run the
  * single-side backward twice (mode P2, then mode P1) and return what those
  * return.  Arguments, ownership and errors are otherwise those of
  * streamkl_bwd_scaled; kl, lse1, lse2 must come from a forward with the

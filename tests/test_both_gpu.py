@@ -1,9 +1,9 @@
 """Both-sides backward (streamkl_bwd_both): dQ1, dK1, dQ2, dK2 against the
 float64 oracle's two gradient modes on the same inputs.  d1 = d2 = 64 and
-d1 = d2 = 32 run the one-recompute kernel; other head dimensions and the
-deterministic mode
-run the single-side backward twice; both must match the oracle with the
-single-side tolerances."""
+d1 = d2 = 32 run the one-recompute kernel (its deterministic mode too, with
+both dQ sides on their rows' grids); other head dimensions run the
+single-side backward twice; both must match the oracle with the single-side
+tolerances, and the deterministic mode must repeat bit for bit."""
 
 import numpy as np
 import pytest
@@ -26,6 +26,9 @@ CASES = [
     (1, 1, 700, 200, 64, 64, False, 0.125, 0.125, False),
     (1, 1, 5, 333, 64, 64, True, 0.125, 0.125, False),
     (1, 2, 257, 257, 64, 64, True, 0.125, 0.125, True),
+    (2, 1, 130, 390, 64, 64, False, 0.2, 0.125, True),
+    (1, 2, 300, 300, 32, 32, True, 1 / np.sqrt(32), 0.15, True),
+    (1, 2, 300, 300, 128, 64, True, 1 / np.sqrt(128), 1 / np.sqrt(64), True),
     (1, 2, 300, 300, 32, 32, True, 1 / np.sqrt(32), 0.15, False),
     (2, 1, 130, 390, 32, 32, False, 0.2, 1 / np.sqrt(32), False),
     (1, 1, 1000, 1000, 32, 32, True, 1 / np.sqrt(32), 1 / np.sqrt(32), False),
@@ -90,3 +93,38 @@ def test_both_sides_with_signed_upstream_gradient():
             fl = grad_floor(w.scale, d64[0, h], f64[g][0, h], f64[g + 1][0, h])
             grad_close(np_(out[0])[0, h], want[0][0, h], fl)
             grad_close(np_(out[1])[0, h], want[1][0, h], fl)
+
+
+@pytest.mark.parametrize("d", [64, 32])
+def test_deterministic_one_pass_repeats_and_agrees(d):
+    """The one-pass deterministic form: bitwise repeatable; each dQ row within
+    its grid rounding of the atomic one-pass form (the same kernel, so the
+    same per-tile contributions), over upstream gradients spanning the fp32
+    range; dK equal bit for bit; and close to the two deterministic
+    single-side calls (another kernel: bf16-level agreement)."""
+    from test_det_fixed_gpu import compare_modes, row_bound
+    w = Workload("both", 1, 4, 1536, 1536, d, d, True, 1 / np.sqrt(d), "independent", 0.0, 1.2, 98)
+    host, dev = inputs(w)
+    dkl = generate_dkl(w, "wide").cuda()
+    kl, l1, l2 = skl.streamkl_fwd(*dev, w.scale, w.causal)
+    a = skl.streamkl_bwd_both(*dev, w.scale, w.scale, w.causal, kl, l1, l2, dkl, True)
+    b = skl.streamkl_bwd_both(*dev, w.scale, w.scale, w.causal, kl, l1, l2, dkl, True)
+    f = skl.streamkl_bwd_both(*dev, w.scale, w.scale, w.causal, kl, l1, l2, dkl, False)
+    torch.cuda.synchronize()
+    assert skl.streamkl_get_device_status() == skl.STREAMKL_OK
+    for x, y in zip(a, b):
+        assert torch.equal(x, y), "not bitwise repeatable"
+    assert torch.equal(a[1], f[1]) and torch.equal(a[3], f[3])  # dK1, dK2
+    tiles = (w.NK + 127) // 128
+    for side, mode, kg in ((0, skl.STREAMKL_GRAD_P1, host[1]), (2, skl.STREAMKL_GRAD_P2, host[3])):
+        assert np.all(np.isfinite(np_(a[side])))
+        bound = row_bound(mode, w.scale, np_(dkl), np_(kl), kg)
+        compare_modes(np_(f[side]), np_(a[side]), bound, tiles)
+    dklu = generate_dkl(w, "uniform").cuda()
+    a = skl.streamkl_bwd_both(*dev, w.scale, w.scale, w.causal, kl, l1, l2, dklu, True)
+    s2 = skl.streamkl_bwd(*dev, w.scale, w.causal, kl, l1, l2, dklu, skl.STREAMKL_GRAD_P2, True)
+    s1 = skl.streamkl_bwd(*dev, w.scale, w.causal, kl, l1, l2, dklu, skl.STREAMKL_GRAD_P1, True)
+    torch.cuda.synchronize()
+    for got, want in ((a[0], s1[0]), (a[1], s1[1]), (a[2], s2[0]), (a[3], s2[1])):
+        g, r = np_(got), np_(want)
+        assert np.linalg.norm(g - r) <= 1e-3 * np.linalg.norm(r) + 1e-30
