@@ -414,14 +414,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const int col = wg * kColsPerWG;
       uint32_t xa1[32], xa2[32], xb1[32], xb2[32];
       const uint32_t t = tmem + lane_off + uint32_t(b * 256 + col);
-      tmem_ld2x32(t, t + 128, xa1, xa2);
-      tmem_ld2x32(t + 32, t + 160, xb1, xb2);
+      tmem_ld4x32(t, t + 128, t + 32, t + 160, xa1, xa2, xb1, xb2);
       const int lr = need_mask ? lim - (k0 + col) : 0;
       const bool fast = need_mask ? fold_pair_fast<true>(st, xa1, xa2, xb1, xb2, c1, c2, nrho, lr)
                                   : fold_pair_fast<false>(st, xa1, xa2, xb1, xb2, c1, c2, nrho, 0);
       if (__any_sync(0xffffffffu, !fast)) {  // the TMEM loads are warp-wide
-        tmem_ld2x32(t, t + 128, xa1, xa2);
-        tmem_ld2x32(t + 32, t + 160, xb1, xb2);
+        tmem_ld4x32(t, t + 128, t + 32, t + 160, xa1, xa2, xb1, xb2);
         if (!fast) {
           if (need_mask) fold_pair<true>(st, xa1, xa2, xb1, xb2, c1, c2, nrho, lr);
           else fold_pair<false>(st, xa1, xa2, xb1, xb2, c1, c2, nrho, 0);

@@ -379,6 +379,32 @@ __device__ __forceinline__ void tmem_ld2x32(uint32_t ta, uint32_t tb, uint32_t (
       : "memory");
 }
 
+// Four 32-column loads and one wait: one round trip to TMEM for a
+// warpgroup's 64 columns of both logit matrices.
+__device__ __forceinline__ void tmem_ld4x32(uint32_t ta, uint32_t tb, uint32_t tc, uint32_t td,
+                                            uint32_t (&a)[32], uint32_t (&b)[32], uint32_t (&c)[32],
+                                            uint32_t (&d)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%128];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%129];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,"
+      "%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95}, [%130];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,"
+      "%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%131];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : SKL_R8(a, 0), SKL_R8(a, 8), SKL_R8(a, 16), SKL_R8(a, 24), SKL_R8(b, 0), SKL_R8(b, 8),
+        SKL_R8(b, 16), SKL_R8(b, 24), SKL_R8(c, 0), SKL_R8(c, 8), SKL_R8(c, 16), SKL_R8(c, 24),
+        SKL_R8(d, 0), SKL_R8(d, 8), SKL_R8(d, 16), SKL_R8(d, 24)
+      : "r"(ta), "r"(tb), "r"(tc), "r"(td)
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld32(uint32_t ta, uint32_t (&a)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
