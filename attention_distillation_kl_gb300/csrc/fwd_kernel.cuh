@@ -13,20 +13,20 @@
 // (s1 (x1 - rho x2) = S1 - S2, so s1 acc / l1 is the P1-weighted mean of
 // S1 - S2).
 //
-// GB300 mapping (10 warps, 1 CTA per SM):
-//   warp 8      TMA producer: Q1/Q2 once, then K1_j/K2_j (key head h / G) into a ring
-//   warp 9      TMEM owner and MMA issuer: S1 = Q1 K1_j^T and S2 = Q2 K2_j^T
+// GB300 mapping (one CTA per SM):
+//   TMA producer warp: Q1/Q2 once, then K1_j/K2_j (key head h / G) into a ring
+//   MMA warp: TMEM owner and MMA issuer: S1 = Q1 K1_j^T and S2 = Q2 K2_j^T
 //               (tcgen05, M = N = 128, bf16 -> fp32) into one of two TMEM
 //               buffers of 256 columns, so tile j+1 is multiplied while the
 //               statistics of tile j are reduced.  The whole warp runs the
 //               loop and one elected lane issues (see elect_one).
-//   warps 0-7   statistics: thread = query row (TMEM lane); warps 0-3 take
-//               key columns 0-63 of every tile, warps 4-7 columns 64-127, and
-//               the two partial states are merged at the end with the same
-//               algebra as the key-split reduce.  (Four warpgroups of 32
-//               columns each were timed slower: the statistics loop is close
-//               to the one-instruction-per-cycle issue limit, and more warps
-//               only add per-tile overhead.)
+//   statistics warps (the first 4 x FwdLayout::kWGs): thread = query row
+//               (TMEM lane); warpgroup w takes key columns [w kCols, (w+1)
+//               kCols) of every tile, and the partial states are merged at
+//               the end with the same algebra as the key-split reduce.  Four
+//               warpgroups of 32 columns (four warps per SM sub-partition)
+//               hide the latency of the ex2 and FMA chains better than two
+//               of 64; the loop is close to the issue and ex2 limits.
 // Head dims above 128 (tile widths 192, 256): the K ring carries 64-column
 // operand blocks instead of whole key tiles (see FwdLayout); the MMA warp
 // multiplies each block as it lands.
@@ -41,16 +41,6 @@
 
 namespace skl {
 
-// Statistics warpgroups: each takes kTile / kStatWGs key columns of every
-// tile (32-column chunks), so every SM sub-partition runs kStatWGs warps
-// of row statistics; then one producer warp and one MMA warp.
-constexpr int kStatWGs = 2;
-constexpr int kStatWarps = 4 * kStatWGs;
-constexpr int kColsPerWG = kTile / kStatWGs;
-constexpr int kProdWarp = kStatWarps, kMmaWarp = kStatWarps + 1;
-constexpr int kFwdThreads = 32 * (kStatWarps + 2);
-static_assert(kColsPerWG % 32 == 0, "whole 32-column chunks per warpgroup");
-
 // Shared memory: Q1, Q2 resident, then the K ring.  Up to tile width 128 on
 // both sides a ring stage holds a whole key tile (K1 and K2); wider heads
 // (192, 256) leave no room for two such stages next to Q, so the ring then
@@ -59,6 +49,17 @@ static_assert(kColsPerWG % 32 == 0, "whole 32-column chunks per warpgroup");
 template <int D1, int D2>
 struct FwdLayout {
   static constexpr bool kRing = D1 > 128 || D2 > 128;
+  // Statistics warpgroups: each takes kCols key columns of every tile.  Up
+  // to tile width 128, four warpgroups of one 32-column chunk each (four
+  // statistics warps per SM sub-partition to hide the latency of the ex2
+  // and FMA chains, 96 registers a thread); with the block ring, whose MMA
+  // warp issues block by block and is slowed by more warps beside it, two
+  // warpgroups of 64 columns.  Then one producer warp and one MMA warp.
+  static constexpr int kWGs = kRing ? 2 : 4;
+  static constexpr int kStatWarps = 4 * kWGs;
+  static constexpr int kCols = kTile / kWGs;
+  static constexpr int kProdWarp = kStatWarps, kMmaWarp = kStatWarps + 1;
+  static constexpr int kThreads = 32 * (kStatWarps + 2);
   static constexpr uint32_t kQ1 = kTile * D1 * 2, kQ2 = kTile * D2 * 2;
   static constexpr uint32_t kK1 = kTile * D1 * 2, kK2 = kTile * D2 * 2;
   static constexpr int kNb1 = OpTile<D1>::kBlocks, kNb2 = OpTile<D2>::kBlocks;  // ring blocks per key tile
@@ -71,7 +72,7 @@ struct FwdLayout {
   static constexpr int kNumBars = 1 + 2 * kStages + 4 + 1;
   static constexpr uint32_t oMisc = oBar + kNumBars * 8;  // tmem base, abort flag
   static constexpr uint32_t oMerge = (oMisc + 8 + 15) / 16 * 16;
-  static constexpr uint32_t kBytes = oMerge + (kStatWGs - 1) * kTile * 5 * 4;
+  static constexpr uint32_t kBytes = oMerge + (kWGs - 1) * kTile * 5 * 4;
   static constexpr uint32_t kAlloc = kBytes + 1024;
   static_assert(kStages >= 2, "shared memory ring needs two stages");
   static_assert(kAlloc <= 232448, "over the 227 KB shared memory limit");
@@ -206,8 +207,83 @@ __device__ __forceinline__ bool fold_pair_fast(RowStats& st, const uint32_t (&xa
   return true;
 }
 
+// The sums of one 32-column chunk against the reference nb = -c m of each
+// side: l1 = sum 2^(c1 x1 + nb1), l2 = sum 2^(c2 x2 + nb2) and
+// acc = sum 2^(c1 x1 + nb1) (x1 - rho x2), columns past lim_rel masked.  Two
+// chains (pairs k, k + 1 and k + 2, k + 3) for instruction-level parallelism.
+template <bool kMask>
+__device__ __forceinline__ void chunk_sums(const uint32_t (&x1)[32], const uint32_t (&x2)[32], uint64_t C1,
+                                           uint64_t C2, uint64_t NR, uint64_t NB1, uint64_t NB2, int lim_rel,
+                                           float& l1, float& l2, float& acc) {
+  uint64_t L1a = f2(0.f, 0.f), L2a = L1a, ACa = L1a, L1b = L1a, L2b = L1a, ACb = L1a;
+#pragma unroll
+  for (int k = 0; k < 32; k += 4) {
+    const uint64_t XA1 = f2(__uint_as_float(x1[k]), __uint_as_float(x1[k + 1]));
+    const uint64_t XA2 = f2(__uint_as_float(x2[k]), __uint_as_float(x2[k + 1]));
+    const uint64_t XB1 = f2(__uint_as_float(x1[k + 2]), __uint_as_float(x1[k + 3]));
+    const uint64_t XB2 = f2(__uint_as_float(x2[k + 2]), __uint_as_float(x2[k + 3]));
+    float e1a, e1b, e2a, e2b, g1a, g1b, g2a, g2b;
+    f2_split(f2_fma(XA1, C1, NB1), e1a, e1b);
+    f2_split(f2_fma(XA2, C2, NB2), e2a, e2b);
+    f2_split(f2_fma(XB1, C1, NB1), g1a, g1b);
+    f2_split(f2_fma(XB2, C2, NB2), g2a, g2b);
+    float p1a = ex2(e1a), p1b = ex2(e1b), p2a = ex2(e2a), p2b = ex2(e2b);
+    float q1a = ex2(g1a), q1b = ex2(g1b), q2a = ex2(g2a), q2b = ex2(g2b);
+    if (kMask) {
+      if (k > lim_rel) { p1a = 0.f; p2a = 0.f; }
+      if (k + 1 > lim_rel) { p1b = 0.f; p2b = 0.f; }
+      if (k + 2 > lim_rel) { q1a = 0.f; q2a = 0.f; }
+      if (k + 3 > lim_rel) { q1b = 0.f; q2b = 0.f; }
+    }
+    const uint64_t P1 = f2(p1a, p1b), Q1 = f2(q1a, q1b);
+    L1a = f2_add(L1a, P1);
+    L2a = f2_add(L2a, f2(p2a, p2b));
+    ACa = f2_fma(P1, f2_fma(XA2, NR, XA1), ACa);
+    L1b = f2_add(L1b, Q1);
+    L2b = f2_add(L2b, f2(q2a, q2b));
+    ACb = f2_fma(Q1, f2_fma(XB2, NR, XB1), ACb);
+  }
+  float u, v;
+  f2_split(f2_add(L1a, L1b), u, v);
+  l1 = u + v;
+  f2_split(f2_add(L2a, L2b), u, v);
+  l2 = u + v;
+  f2_split(f2_add(ACa, ACb), u, v);
+  acc = u + v;
+}
+
+// Folds one 32-column chunk into the running state exactly: the maxima move
+// to the chunk's, the state is rescaled once, and the chunk's sums are taken
+// against the new maxima.  Masked columns (k > lim_rel) move nothing.
+template <bool kMask>
+__device__ __forceinline__ void fold_one(RowStats& st, const uint32_t (&x1)[32], const uint32_t (&x2)[32],
+                                         uint64_t C1, uint64_t C2, uint64_t NR, float c1, float c2,
+                                         int lim_rel) {
+  float ta1 = st.m1, ta2 = st.m2, tb1 = kNegBig, tb2 = kNegBig;
+#pragma unroll
+  for (int k = 0; k < 32; k += 4) {
+    const bool o0 = !kMask || k <= lim_rel, o1 = !kMask || k + 1 <= lim_rel;
+    const bool o2 = !kMask || k + 2 <= lim_rel, o3 = !kMask || k + 3 <= lim_rel;
+    ta1 = max3(ta1, o0 ? __uint_as_float(x1[k]) : kNegBig, o1 ? __uint_as_float(x1[k + 1]) : kNegBig);
+    ta2 = max3(ta2, o0 ? __uint_as_float(x2[k]) : kNegBig, o1 ? __uint_as_float(x2[k + 1]) : kNegBig);
+    tb1 = max3(tb1, o2 ? __uint_as_float(x1[k + 2]) : kNegBig, o3 ? __uint_as_float(x1[k + 3]) : kNegBig);
+    tb2 = max3(tb2, o2 ? __uint_as_float(x2[k + 2]) : kNegBig, o3 ? __uint_as_float(x2[k + 3]) : kNegBig);
+  }
+  const float t1 = fmaxf(ta1, tb1), t2 = fmaxf(ta2, tb2);
+  const float a1 = ex2((st.m1 - t1) * c1);
+  const float a2 = ex2((st.m2 - t2) * c2);
+  st.m1 = t1;
+  st.m2 = t2;
+  const float nb1 = -t1 * c1, nb2 = -t2 * c2;
+  float l1, l2, acc;
+  chunk_sums<kMask>(x1, x2, C1, C2, NR, f2(nb1, nb1), f2(nb2, nb2), lim_rel, l1, l2, acc);
+  st.l1 = fmaf(st.l1, a1, l1);
+  st.acc = fmaf(st.acc, a1, acc);
+  st.l2 = fmaf(st.l2, a2, l2);
+}
+
 template <int D1, int D2>
-__global__ void __launch_bounds__(kFwdThreads, 1)
+__global__ void __launch_bounds__(FwdLayout<D1, D2>::kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tq1, const __grid_constant__ CUtensorMap tk1,
                const __grid_constant__ CUtensorMap tq2, const __grid_constant__ CUtensorMap tk2,
                const FwdArgs a) {
@@ -250,13 +326,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar_sfull(b), 1);
-      mbar_init(bar_sempty(b), kStatWarps);
+      mbar_init(bar_sempty(b), L::kStatWarps);
     }
     mbar_init(bar_done, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == kMmaWarp) {
+  if (warp == L::kMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
@@ -265,7 +341,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == kProdWarp) {
+  if (warp == L::kProdWarp) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0 && nkt > 0) {
       tma_prefetch_desc(&tq1);
@@ -321,7 +397,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           mbar_drain(bar_kfull(j % L::kStages), (j / L::kStages) & 1, 200000000ull);  // (ring fills)
       }
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == L::kMmaWarp) {
     // ---------------------------------------------------------------- MMA issuer
     // (the whole warp runs the loop; the elected lane issues)
     const uint32_t leader = elect_one();
@@ -398,36 +474,76 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const float c1 = a.scale1 * kLog2e, c2 = a.scale2 * kLog2e, nrho = -a.scale2 / a.scale1;
     const int lim = a.causal ? min(grow + off, a.NK - 1) : a.NK - 1;  // last visible key
     const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
+    const uint64_t C1 = f2(c1, c1), C2 = f2(c2, c2), NR = f2(nrho, nrho);
     RowStats st{kNegBig, kNegBig, 0.f, 0.f, 0.f};
-    for (int j = 0; j < nkt; ++j) {
-      const int b = j & 1;
-      const uint32_t bph = (j >> 1) & 1;
-      if (!mbar_wait_warp(bar_sfull(b), bph, ctl)) break;
-      tc_fence_after();
-      const int k0 = (kt_lo + j) * kTile;
-      const bool need_mask = (k0 + kTile > a.NK) || (a.causal && k0 + kTile - 1 > q0 + off);
-      // this warpgroup's 64 columns of S1 and S2 in one go, folded against
-      // the running maxima; a row that finds a new maximum (rare after its
-      // first tile) reads its columns again and folds them exactly.  S is
-      // released after the fold: the other buffer keeps the MMA a tile ahead
-      static_assert(kColsPerWG == 64, "fold_pair takes 64 columns");
-      const int col = wg * kColsPerWG;
-      uint32_t xa1[32], xa2[32], xb1[32], xb2[32];
-      const uint32_t t = tmem + lane_off + uint32_t(b * 256 + col);
-      tmem_ld4x32(t, t + 128, t + 32, t + 160, xa1, xa2, xb1, xb2);
-      const int lr = need_mask ? lim - (k0 + col) : 0;
-      const bool fast = need_mask ? fold_pair_fast<true>(st, xa1, xa2, xb1, xb2, c1, c2, nrho, lr)
-                                  : fold_pair_fast<false>(st, xa1, xa2, xb1, xb2, c1, c2, nrho, 0);
-      if (__any_sync(0xffffffffu, !fast)) {  // the TMEM loads are warp-wide
-        tmem_ld4x32(t, t + 128, t + 32, t + 160, xa1, xa2, xb1, xb2);
-        if (!fast) {
-          if (need_mask) fold_pair<true>(st, xa1, xa2, xb1, xb2, c1, c2, nrho, lr);
-          else fold_pair<false>(st, xa1, xa2, xb1, xb2, c1, c2, nrho, 0);
+    const int col = wg * L::kCols;
+    if constexpr (L::kCols == 32) {
+      for (int j = 0; j < nkt; ++j) {
+        const int b = j & 1;
+        const uint32_t bph = (j >> 1) & 1;
+        if (!mbar_wait_warp(bar_sfull(b), bph, ctl)) break;
+        tc_fence_after();
+        // this warpgroup's 32 columns of S1 and S2, summed against the
+        // running maxima; a row whose sums reach 2^64 (rare after its first
+        // tile) reads its columns again and folds them exactly.  S is
+        // released after the fold: the other buffer keeps the MMA a tile ahead
+        uint32_t x1[32], x2[32];
+        const uint32_t t = tmem + lane_off + uint32_t(b * 256 + col);
+        tmem_ld2x32(t, t + 128, x1, x2);
+        const int k0 = (kt_lo + j) * kTile;
+        const bool need_mask = (k0 + kTile > a.NK) || (a.causal && k0 + kTile - 1 > q0 + off);
+        const int lr = need_mask ? lim - (k0 + col) : 0;
+        const float nb1 = -st.m1 * c1, nb2 = -st.m2 * c2;
+        float l1, l2, acc;
+        if (need_mask) chunk_sums<true>(x1, x2, C1, C2, NR, f2(nb1, nb1), f2(nb2, nb2), lr, l1, l2, acc);
+        else chunk_sums<false>(x1, x2, C1, C2, NR, f2(nb1, nb1), f2(nb2, nb2), 0, l1, l2, acc);
+        const bool fast = l1 < 18446744073709551616.f && l2 < 18446744073709551616.f;  // 2^64
+        if (fast) {
+          st.l1 += l1;
+          st.acc += acc;
+          st.l2 += l2;
         }
+        if (__any_sync(0xffffffffu, !fast)) {  // the TMEM loads are warp-wide
+          tmem_ld2x32(t, t + 128, x1, x2);
+          if (!fast) {
+            if (need_mask) fold_one<true>(st, x1, x2, C1, C2, NR, c1, c2, lr);
+            else fold_one<false>(st, x1, x2, C1, C2, NR, c1, c2, 0);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_sempty(b));
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_sempty(b));
+    } else {
+      static_assert(L::kCols == 64, "fold_pair takes 64 columns");
+      for (int j = 0; j < nkt; ++j) {
+        const int b = j & 1;
+        const uint32_t bph = (j >> 1) & 1;
+        if (!mbar_wait_warp(bar_sfull(b), bph, ctl)) break;
+        tc_fence_after();
+        const int k0 = (kt_lo + j) * kTile;
+        const bool need_mask = (k0 + kTile > a.NK) || (a.causal && k0 + kTile - 1 > q0 + off);
+        // this warpgroup's 64 columns of S1 and S2 in one go, folded against
+        // the running maxima; a row that finds a new maximum (rare after its
+        // first tile) reads its columns again and folds them exactly.  S is
+        // released after the fold: the other buffer keeps the MMA a tile ahead
+        uint32_t xa1[32], xa2[32], xb1[32], xb2[32];
+        const uint32_t t = tmem + lane_off + uint32_t(b * 256 + col);
+        tmem_ld4x32(t, t + 128, t + 32, t + 160, xa1, xa2, xb1, xb2);
+        const int lr = need_mask ? lim - (k0 + col) : 0;
+        const bool fast = need_mask ? fold_pair_fast<true>(st, xa1, xa2, xb1, xb2, c1, c2, nrho, lr)
+                                    : fold_pair_fast<false>(st, xa1, xa2, xb1, xb2, c1, c2, nrho, 0);
+        if (__any_sync(0xffffffffu, !fast)) {  // the TMEM loads are warp-wide
+          tmem_ld4x32(t, t + 128, t + 32, t + 160, xa1, xa2, xb1, xb2);
+          if (!fast) {
+            if (need_mask) fold_pair<true>(st, xa1, xa2, xb1, xb2, c1, c2, nrho, lr);
+            else fold_pair<false>(st, xa1, xa2, xb1, xb2, c1, c2, nrho, 0);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_sempty(b));
+      }
     }
     // merge the column shares of every row (warpgroups 1.. -> warpgroup 0)
     // with the same algebra as the key-split reduce
@@ -440,18 +556,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       o[3] = st.m2;
       o[4] = st.l2;
     }
-    named_bar_sync(1, 32 * kStatWarps);
+    named_bar_sync(1, 32 * L::kStatWarps);
     if (wg == 0 && !*abort_flag && grow < a.NQ) {
       float M1 = st.m1, M2 = st.m2;
 #pragma unroll
-      for (int w = 0; w < kStatWGs - 1; ++w) {
+      for (int w = 0; w < L::kWGs - 1; ++w) {
         M1 = fmaxf(M1, mg[w * kTile * 5 + row * 5 + 0]);
         M2 = fmaxf(M2, mg[w * kTile * 5 + row * 5 + 3]);
       }
       const float e1 = ex2((st.m1 - M1) * c1), e2 = ex2((st.m2 - M2) * c2);
       float L1 = st.l1 * e1, A = st.acc * e1, L2 = st.l2 * e2;
 #pragma unroll
-      for (int w = 0; w < kStatWGs - 1; ++w) {
+      for (int w = 0; w < L::kWGs - 1; ++w) {
         const float* o = mg + w * kTile * 5 + row * 5;
         const float g1 = ex2((o[0] - M1) * c1), g2 = ex2((o[3] - M2) * c2);
         L1 = fmaf(o[1], g1, L1);
@@ -481,7 +597,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == L::kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -496,7 +612,7 @@ inline int launch_fwd_t(const TMaps& m, const FwdArgs& a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   const int nqt = (a.NQ + kTile - 1) / kTile;
   dim3 grid(nqt, a.BH, a.num_splits);
-  kern<<<grid, kFwdThreads, L::kAlloc, st>>>(m.q1, m.k1, m.q2, m.k2, a);
+  kern<<<grid, L::kThreads, L::kAlloc, st>>>(m.q1, m.k1, m.q2, m.k2, a);
   return cudaGetLastError();
 }
 
