@@ -493,21 +493,26 @@ __global__ void __launch_bounds__(FwdLayout<D1, D2>::kThreads, 1)
         const int k0 = (kt_lo + j) * kTile;
         const bool need_mask = (k0 + kTile > a.NK) || (a.causal && k0 + kTile - 1 > q0 + off);
         const int lr = need_mask ? lim - (k0 + col) : 0;
-        const float nb1 = -st.m1 * c1, nb2 = -st.m2 * c2;
-        float l1, l2, acc;
-        if (need_mask) chunk_sums<true>(x1, x2, C1, C2, NR, f2(nb1, nb1), f2(nb2, nb2), lr, l1, l2, acc);
-        else chunk_sums<false>(x1, x2, C1, C2, NR, f2(nb1, nb1), f2(nb2, nb2), 0, l1, l2, acc);
-        const bool fast = l1 < 18446744073709551616.f && l2 < 18446744073709551616.f;  // 2^64
-        if (fast) {
-          st.l1 += l1;
-          st.acc += acc;
-          st.l2 += l2;
-        }
-        if (__any_sync(0xffffffffu, !fast)) {  // the TMEM loads are warp-wide
-          tmem_ld2x32(t, t + 128, x1, x2);
-          if (!fast) {
-            if (need_mask) fold_one<true>(st, x1, x2, C1, C2, NR, c1, c2, lr);
-            else fold_one<false>(st, x1, x2, C1, C2, NR, c1, c2, 0);
+        if (j == 0) {  // no reference yet: every row folds its first tile exactly
+          if (need_mask) fold_one<true>(st, x1, x2, C1, C2, NR, c1, c2, lr);
+          else fold_one<false>(st, x1, x2, C1, C2, NR, c1, c2, 0);
+        } else {
+          const float nb1 = -st.m1 * c1, nb2 = -st.m2 * c2;
+          float l1, l2, acc;
+          if (need_mask) chunk_sums<true>(x1, x2, C1, C2, NR, f2(nb1, nb1), f2(nb2, nb2), lr, l1, l2, acc);
+          else chunk_sums<false>(x1, x2, C1, C2, NR, f2(nb1, nb1), f2(nb2, nb2), 0, l1, l2, acc);
+          const bool fast = l1 < 18446744073709551616.f && l2 < 18446744073709551616.f;  // 2^64
+          if (fast) {
+            st.l1 += l1;
+            st.acc += acc;
+            st.l2 += l2;
+          }
+          if (__any_sync(0xffffffffu, !fast)) {  // the TMEM loads are warp-wide
+            tmem_ld2x32(t, t + 128, x1, x2);
+            if (!fast) {
+              if (need_mask) fold_one<true>(st, x1, x2, C1, C2, NR, c1, c2, lr);
+              else fold_one<false>(st, x1, x2, C1, C2, NR, c1, c2, 0);
+            }
           }
         }
         tc_fence_before();
@@ -531,9 +536,13 @@ __global__ void __launch_bounds__(FwdLayout<D1, D2>::kThreads, 1)
         const uint32_t t = tmem + lane_off + uint32_t(b * 256 + col);
         tmem_ld4x32(t, t + 128, t + 32, t + 160, xa1, xa2, xb1, xb2);
         const int lr = need_mask ? lim - (k0 + col) : 0;
-        const bool fast = need_mask ? fold_pair_fast<true>(st, xa1, xa2, xb1, xb2, c1, c2, nrho, lr)
-                                    : fold_pair_fast<false>(st, xa1, xa2, xb1, xb2, c1, c2, nrho, 0);
-        if (__any_sync(0xffffffffu, !fast)) {  // the TMEM loads are warp-wide
+        // no reference yet on the first tile: every row folds it exactly
+        const bool fast = j > 0 && (need_mask ? fold_pair_fast<true>(st, xa1, xa2, xb1, xb2, c1, c2, nrho, lr)
+                                              : fold_pair_fast<false>(st, xa1, xa2, xb1, xb2, c1, c2, nrho, 0));
+        if (j == 0) {
+          if (need_mask) fold_pair<true>(st, xa1, xa2, xb1, xb2, c1, c2, nrho, lr);
+          else fold_pair<false>(st, xa1, xa2, xb1, xb2, c1, c2, nrho, 0);
+        } else if (__any_sync(0xffffffffu, !fast)) {  // the TMEM loads are warp-wide
           tmem_ld4x32(t, t + 128, t + 32, t + 160, xa1, xa2, xb1, xb2);
           if (!fast) {
             if (need_mask) fold_pair<true>(st, xa1, xa2, xb1, xb2, c1, c2, nrho, lr);
