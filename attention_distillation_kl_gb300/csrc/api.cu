@@ -149,6 +149,18 @@ int make_maps(skl::TMaps* m, const void* q1, const void* k1, const void* q2, con
 
 int as_status(int cuda_err) { return cuda_err == 0 ? STREAMKL_OK : STREAMKL_CUDA_ERROR; }
 
+// Heads whose CTAs interleave (FwdArgs::head_group): as many as keep the
+// operand every CTA of a head re-reads (`bytes_per_head`: K for the
+// forward; Q and the fp32 dQ for the backward) within half of L2, so that
+// interleaving the heads' longest tiles first costs no extra DRAM traffic.
+int head_group_for(int BH, double bytes_per_head) {
+  int dev = 0, l2 = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess)
+    return 1;
+  const double g = 0.5 * double(l2) / (bytes_per_head > 1.0 ? bytes_per_head : 1.0);
+  return g < 1.0 ? 1 : (g >= double(BH) ? BH : int(g));
+}
+
 }  // namespace
 
 extern "C" {
@@ -168,6 +180,7 @@ int streamkl_fwd_gqa(const void* q1, const void* k1, const void* q2, const void*
   int* st = status_ptr();
   if (!st) return STREAMKL_CUDA_ERROR;
   skl::FwdArgs a{B * H, NQ, NK, causal, 1, H / HK1, H / HK2, scale1, scale2, kl, lse1, lse2, nullptr, st};
+  a.head_group = head_group_for(B * H, 2.0 * NK * (d1 + d2));
   return as_status(skl::launch_fwd(m, tile_dim(d1), tile_dim(d2), a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -212,6 +225,7 @@ int streamkl_fwd_splitk_gqa(const void* q1, const void* k1, const void* q2, cons
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   float* part = static_cast<float*>(workspace);
   skl::FwdArgs a{B * H, NQ, NK, causal, num_splits, H / HK1, H / HK2, scale1, scale2, kl, lse1, lse2, part, st};
+  a.head_group = head_group_for(B * H, 2.0 * NK * (d1 + d2));
   int e = skl::launch_fwd(m, tile_dim(d1), tile_dim(d2), a, cs);
   if (e != 0) return STREAMKL_CUDA_ERROR;
   return as_status(skl::launch_splitk_reduce(part, B * H * NQ, num_splits, kl, lse1, lse2, cs));
@@ -338,6 +352,10 @@ int bwd_impl(const void* q1, const void* k1, const void* q2, const void* k2, int
     a.hsel = -1;
     return as_status(skl::launch_bwd_wide_pass1(m, t1, t2, a, cs));
   }
+  // CTA order: key-head groups interleave within L2's reach (not with the
+  // ordered dK of the deterministic grouped-head mode, whose ticket order
+  // is fixed)
+  a.head_group = head_group_for(B * H, 2.0 * NQ * (d1 + d2) + 4.0 * NQ * dg);
   if (!deterministic) {
     const size_t dq_bytes = size_t(B) * H * NQ * dg * 4;
     if (!make_map_dq_wide(&m.dqw, dq, (long long)B * H, NQ, dg, &a.dq_box)) return STREAMKL_CUDA_ERROR;
@@ -371,6 +389,7 @@ int bwd_impl(const void* q1, const void* k1, const void* q2, const void* k2, int
   a.kmax = scratch;
   if (gg > 1) {
     int* words_i = reinterpret_cast<int*>(scratch);
+    a.head_group = 1;
     a.ticket = words_i + kg_heads;
     a.dk_abort = words_i + kg_heads + 1;
     a.dk_turns = words_i + kg_heads + 2;

@@ -158,7 +158,8 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
 
   if (threadIdx.x == 0) {
     // ordered dK of grouped key heads: units (key tile fastest, then query
-    // head) in the order CTAs start, so a head waits only for CTAs that run
+    // head; head_group is 1) in the order CTAs start, so a head waits only
+    // for CTAs that run
     *unit_slot = a.ticket ? atomicAdd(a.ticket, 1) : int(blockIdx.y * gridDim.x + blockIdx.x);
     *s_queued = 0;
     for (int b = 0; b < L::kNumBars; ++b) {
@@ -182,9 +183,10 @@ __global__ void __launch_bounds__(BwdLayout<D1, D2, MODE>::kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const uint32_t t_s1 = tmem, t_s2 = tmem + 128, t_dk = tmem + 256, t_dq = tmem + 384;
 
-  const int unit = *unit_slot;
-  const int kt = unit % int(gridDim.x);
-  const int bh = unit / int(gridDim.x);  // query head (batch-major)
+  // unit -> (query head (batch-major), key tile): heads in groups of
+  // head_group whose key tiles interleave, the longest sweeps first
+  int bh, kt;
+  grouped_unit(*unit_slot, a.BH, int(gridDim.x), a.head_group, bh, kt);
   const int k0 = kt * kTile;
   const int off = a.NK - a.NQ;
   const int nqt = (a.NQ + kTile - 1) / kTile;

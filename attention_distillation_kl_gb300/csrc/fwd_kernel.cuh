@@ -297,8 +297,10 @@ __global__ void __launch_bounds__(FwdLayout<D1, D2>::kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   const int nqt = (a.NQ + kTile - 1) / kTile;
-  const int qt = a.causal ? (nqt - 1 - int(blockIdx.x)) : int(blockIdx.x);  // longest rows first
-  const int bh = blockIdx.y, split = blockIdx.z;
+  int bh, t;
+  grouped_unit(int(blockIdx.y) * int(gridDim.x) + int(blockIdx.x), a.BH, nqt, a.head_group, bh, t);
+  const int qt = a.causal ? (nqt - 1 - t) : t;  // longest rows first
+  const int split = blockIdx.z;
   const int q0 = qt * kTile;
   const int off = a.NK - a.NQ;
   const int kend = a.causal ? min(q0 + kTile, a.NQ) + off : a.NK;

@@ -27,6 +27,11 @@ struct FwdArgs {
   float* lse2;
   float* partial;  // key-split partials [num_splits][5][BH*NQ], or null
   int* status;
+  // CTA order: heads in groups of head_group whose query tiles interleave,
+  // longest first (causal), so the long CTAs of every head in a group start
+  // early; groups follow one another (1 = head after head).  The group is
+  // sized so that its heads' re-read operands stay in L2 (head_group_for).
+  int head_group = 1;
 };
 
 struct BwdArgs {
@@ -65,7 +70,20 @@ struct BwdArgs {
   int* ticket;
   int* dk_turns;
   int* dk_abort;
+  // CTA order of the fused backward, as FwdArgs::head_group (key tiles
+  // instead of query tiles; 1 whenever ticket is set).
+  int head_group = 1;
 };
+
+// Unit u of a launch over BH heads x n tiles, heads in groups of G whose
+// tiles interleave: (head, tile index).  A bijection of [0, BH n).
+__host__ __device__ inline void grouped_unit(int u, int BH, int n, int G, int& head, int& tile) {
+  const int g0 = u / (G * n) * G;       // first head of u's group
+  const int gs = BH - g0 < G ? BH - g0 : G;  // heads in that group
+  const int r = u - g0 * n;             // in [0, gs n)
+  tile = r / gs;
+  head = g0 + r % gs;
+}
 
 // Each returns a cudaError_t value (cudaSuccess = 0).  d1, d2 and d are the
 // kernels' tile widths (32, 64, 128, 192 or 256): a head dim below its tile width is
