@@ -345,11 +345,15 @@ int bwd_impl(const void* q1, const void* k1, const void* q2, const void* k2, int
     // a head above 128: dK by key tiles (the launches of a key-head group in
     // order, the first storing), then dQ by query tiles; no atomics, so both
     // values of `deterministic` take this path
+    // (CTA order: heads interleaved in groups that keep the re-read Q, then
+    // K, of a group within half of L2)
+    a.head_group = head_group_for(B * H, 2.0 * NQ * (d1 + d2));
     for (int j = 0; j < gg; ++j) {
       a.hsel = gg > 1 ? j : -1;
       if (skl::launch_bwd_wide_pass0(m, t1, t2, a, cs) != 0) return STREAMKL_CUDA_ERROR;
     }
     a.hsel = -1;
+    a.head_group = head_group_for(B * H, 2.0 * NK * (d1 + d2));
     return as_status(skl::launch_bwd_wide_pass1(m, t1, t2, a, cs));
   }
   // CTA order: key-head groups interleave within L2's reach (not with the
@@ -470,6 +474,7 @@ int streamkl_bwd_both(const void* q1, const void* k1, const void* q2, const void
     return STREAMKL_CUDA_ERROR;
   skl::BwdArgs a{B * H, NQ, NK, causal, STREAMKL_GRAD_P2, d1, 1, 1, -1, scale1, scale2, kl, lse1, lse2,
                  dkl, dq1, dk1, st, dq2, dk2};
+  a.head_group = head_group_for(B * H, 12.0 * NQ * d1);  // Q1, Q2 and both fp32 dQ
   if (!deterministic) return as_status(skl::launch_bwd_both(m, tile_dim(d1), a, cs));
   // deterministic: both dQ sides on their rows' grids (dK is stored by one
   // CTA per key tile anyway); the bound on |K| of both sides' key heads in

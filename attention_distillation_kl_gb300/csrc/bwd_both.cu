@@ -65,7 +65,8 @@ __global__ void __launch_bounds__(kBothThreads, 1)
   const uint32_t sb = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  const int kt = blockIdx.x, bh = blockIdx.y;
+  int bh, kt;  // heads in groups whose key tiles interleave, longest sweeps first
+  grouped_unit(int(blockIdx.y) * int(gridDim.x) + int(blockIdx.x), a.BH, int(gridDim.x), a.head_group, bh, kt);
   const int k0 = kt * kTile;
   const int off = a.NK - a.NQ;
   const int nqt = (a.NQ + kTile - 1) / kTile;

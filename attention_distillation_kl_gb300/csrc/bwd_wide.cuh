@@ -84,15 +84,19 @@ __global__ void __launch_bounds__(kWideThreads, 1)
   const int nqt = (a.NQ + kTile - 1) / kTile;
   // pass 0: key tile kt, visitors = query tiles qt_lo .. nqt - 1
   // pass 1: query tile qt (longest rows first), visitors = key tiles 0 .. nv - 1
+  // the launch's heads in groups whose tiles interleave, longest first
+  int hy, tx;
+  grouped_unit(int(blockIdx.y) * int(gridDim.x) + int(blockIdx.x), int(gridDim.y), int(gridDim.x), a.head_group,
+               hy, tx);
   int bh, k0 = 0, q0 = 0, qt_lo = 0, nv;
   if constexpr (kDK) {
-    bh = a.hsel < 0 ? int(blockIdx.y) : int(blockIdx.y) * gg + a.hsel;
-    k0 = int(blockIdx.x) * kTile;
+    bh = a.hsel < 0 ? hy : hy * gg + a.hsel;
+    k0 = tx * kTile;
     qt_lo = a.causal ? max(0, k0 - off) / kTile : 0;
     nv = nqt - qt_lo;
   } else {
-    bh = blockIdx.y;
-    const int qt = a.causal ? (nqt - 1 - int(blockIdx.x)) : int(blockIdx.x);
+    bh = hy;
+    const int qt = a.causal ? (nqt - 1 - tx) : tx;
     q0 = qt * kTile;
     const int kend = a.causal ? min(q0 + kTile, a.NQ) + off : a.NK;
     nv = (kend + kTile - 1) / kTile;

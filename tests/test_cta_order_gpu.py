@@ -56,3 +56,55 @@ def test_grouped_heads_match_head_by_head(causal):
             assert torch.equal(kk_[0, 0], dk[b, h]), (b, h)
     torch.cuda.synchronize()
     assert skl.streamkl_get_device_status() == 0
+
+
+def _per_head_equal(batched, per_head, B, H):
+    for b in range(B):
+        for h in range(H):
+            got = per_head(b, h)
+            for x, y in zip(got, batched):
+                assert torch.equal(x[0, 0], y[b, h]), (b, h)
+
+
+def test_grouped_heads_both_sides_deterministic():
+    """The both-sides kernel (d = 64), deterministic: eight heads of 16K make
+    groups of about five."""
+    B, H, N, d = 2, 4, 16384, 64
+    q1, k1, q2, k2 = _inputs(B, H, N, d, 11)
+    scale = 1.0 / np.sqrt(d)
+    kl, l1, l2 = skl.streamkl_fwd(q1, k1, q2, k2, scale, True)
+    dkl = torch.rand(B, H, N, device="cuda") - 0.25
+    out = skl.streamkl_bwd_both(q1, k1, q2, k2, scale, scale, True, kl, l1, l2, dkl, True)
+    torch.cuda.synchronize()
+    assert skl.streamkl_get_device_status() == 0
+
+    def one(b, h):
+        s = (slice(b, b + 1), slice(h, h + 1))
+        x = [t[s].contiguous() for t in (q1, k1, q2, k2)]
+        return skl.streamkl_bwd_both(*x, scale, scale, True, kl[s].contiguous(), l1[s].contiguous(),
+                                     l2[s].contiguous(), dkl[s].contiguous(), True)
+
+    _per_head_equal(out, one, B, H)
+
+
+def test_grouped_heads_wide_head_dim():
+    """Head dim 256 on both sides (block-ring forward, two-pass backward,
+    no atomics): eight heads of 16K make groups of about three."""
+    B, H, N, d = 1, 8, 16384, 256
+    q1, k1, q2, k2 = _inputs(B, H, N, d, 13)
+    scale = 1.0 / np.sqrt(d)
+    fwd = skl.streamkl_fwd(q1, k1, q2, k2, scale, True)
+    dkl = torch.rand(B, H, N, device="cuda") - 0.25
+    bwd = skl.streamkl_bwd(q1, k1, q2, k2, scale, True, *fwd, dkl, skl.STREAMKL_GRAD_P2, False)
+    torch.cuda.synchronize()
+    assert skl.streamkl_get_device_status() == 0
+
+    def one(b, h):
+        s = (slice(b, b + 1), slice(h, h + 1))
+        x = [t[s].contiguous() for t in (q1, k1, q2, k2)]
+        f = skl.streamkl_fwd(*x, scale, True)
+        g = skl.streamkl_bwd(*x, scale, True, *(t[s].contiguous() for t in fwd), dkl[s].contiguous(),
+                             skl.STREAMKL_GRAD_P2, False)
+        return (*f, *g)
+
+    _per_head_equal((*fwd, *bwd), one, B, H)
