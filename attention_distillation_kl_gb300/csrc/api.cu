@@ -151,13 +151,15 @@ int as_status(int cuda_err) { return cuda_err == 0 ? STREAMKL_OK : STREAMKL_CUDA
 
 // Heads whose CTAs interleave (FwdArgs::head_group): as many as keep the
 // operand every CTA of a head re-reads (`bytes_per_head`: K for the
-// forward; Q and the fp32 dQ for the backward) within half of L2, so that
-// interleaving the heads' longest tiles first costs no extra DRAM traffic.
+// forward; Q and the fp32 dQ for the backward) within a quarter of L2, so
+// that interleaving the heads' longest tiles first costs no extra DRAM
+// traffic.  (Half of L2 let two heads of 64K tokens share it, 32 MB of K
+// each, and the forward then read 1 GB more from DRAM.)
 int head_group_for(int BH, double bytes_per_head) {
   int dev = 0, l2 = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess)
     return 1;
-  const double g = 0.5 * double(l2) / (bytes_per_head > 1.0 ? bytes_per_head : 1.0);
+  const double g = 0.25 * double(l2) / (bytes_per_head > 1.0 ? bytes_per_head : 1.0);
   return g < 1.0 ? 1 : (g >= double(BH) ? BH : int(g));
 }
 
@@ -346,7 +348,7 @@ int bwd_impl(const void* q1, const void* k1, const void* q2, const void* k2, int
     // order, the first storing), then dQ by query tiles; no atomics, so both
     // values of `deterministic` take this path
     // (CTA order: heads interleaved in groups that keep the re-read Q, then
-    // K, of a group within half of L2)
+    // K, of a group within a quarter of L2)
     a.head_group = head_group_for(B * H, 2.0 * NQ * (d1 + d2));
     for (int j = 0; j < gg; ++j) {
       a.hsel = gg > 1 ? j : -1;
@@ -356,7 +358,7 @@ int bwd_impl(const void* q1, const void* k1, const void* q2, const void* k2, int
     a.head_group = head_group_for(B * H, 2.0 * NK * (d1 + d2));
     return as_status(skl::launch_bwd_wide_pass1(m, t1, t2, a, cs));
   }
-  // CTA order: key-head groups interleave within L2's reach (not with the
+  // CTA order: heads interleave in groups within L2's reach (not with the
   // ordered dK of the deterministic grouped-head mode, whose ticket order
   // is fixed)
   a.head_group = head_group_for(B * H, 2.0 * NQ * (d1 + d2) + 4.0 * NQ * dg);

@@ -40,8 +40,8 @@ UNIT = "TFLOP/s"
 # only while its source is unchanged (sha256 of the file it lives in).
 TRAFFIC = {
     # dram__bytes_read.sum + dram__bytes_write.sum of one full-size launch
-    "bwd_fused": {"bytes": 3295012096 + 2136818688, "src_sha": "2e7eaa250e678dd8"},
-    "fwd": {"bytes": 2160868096 + 28844800, "src_sha": "d7da1cc91499a902"},
+    "bwd_fused": {"bytes": 3294571264 + 2136466432, "src_sha": "cdaacbf38a1b7730"},
+    "fwd": {"bytes": 2158700544 + 28129280, "src_sha": "0269f1cb4c4f4883"},
 }
 
 
@@ -522,40 +522,54 @@ def run_mine(args, rank, world, local):
     # pinned host memory and reads its KL back, inside the timed region.  The
     # inputs are double-buffered and copied on a second stream, so the copy
     # for step k+1 overlaps the kernels of step k (each buffer is refilled
-    # only after the step that used it has finished).
+    # only after the step that used it has finished).  The loop runs three
+    # times and the median is reported: the host link is shared with the
+    # machine's other GPUs, and its rate during each copy is recorded too.
     e2e_steps = max(3, min(args.steps, 6))
     sets = [(dev, dkl), ([torch.empty_like(t) for t in dev], torch.empty_like(dkl))]
     copy_stream = torch.cuda.Stream()
-    copied = [torch.cuda.Event() for _ in range(e2e_steps)]
-    consumed = [torch.cuda.Event() for _ in range(e2e_steps)]
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    in_bytes = sum(t.numel() * t.element_size() for t in host) + dkl_h.numel() * 4
 
-    def issue_copy(j):
-        with torch.cuda.stream(copy_stream):
-            if j >= 2:
-                copy_stream.wait_event(consumed[j - 2])
-            bufs, g = sets[j % 2]
-            for d, h in zip(bufs, host):
-                d.copy_(h, non_blocking=True)
-            g.copy_(dkl_h, non_blocking=True)
-            copied[j].record(copy_stream)
+    def e2e_loop():
+        copied = [torch.cuda.Event() for _ in range(e2e_steps)]
+        consumed = [torch.cuda.Event() for _ in range(e2e_steps)]
+        c_on = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(e2e_steps)]
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
-    torch.cuda.synchronize()
-    e0.record(stream)
-    copy_stream.wait_event(e0)
-    issue_copy(0)
-    for k in range(e2e_steps):
-        if k + 1 < e2e_steps:
-            issue_copy(k + 1)
-        stream.wait_event(copied[k])
-        step(inp=sets[k % 2][0], dkl_in=sets[k % 2][1])
-        consumed[k].record(stream)
-        kl_h.copy_(kl, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    # the host-to-device rate on its own, after the loop (reported: it bounds
-    # the pipelined loop once it is slower than the kernels)
+        def issue_copy(j):
+            with torch.cuda.stream(copy_stream):
+                if j >= 2:
+                    copy_stream.wait_event(consumed[j - 2])
+                c_on[j][0].record(copy_stream)
+                bufs, g = sets[j % 2]
+                for d, h in zip(bufs, host):
+                    d.copy_(h, non_blocking=True)
+                g.copy_(dkl_h, non_blocking=True)
+                c_on[j][1].record(copy_stream)
+                copied[j].record(copy_stream)
+
+        torch.cuda.synchronize()
+        e0.record(stream)
+        copy_stream.wait_event(e0)
+        issue_copy(0)
+        for k in range(e2e_steps):
+            if k + 1 < e2e_steps:
+                issue_copy(k + 1)
+            stream.wait_event(copied[k])
+            step(inp=sets[k % 2][0], dkl_in=sets[k % 2][1])
+            consumed[k].record(stream)
+            kl_h.copy_(kl, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        rates = [in_bytes / (c[0].elapsed_time(c[1]) * 1e-3) / 1e9 for c in c_on]
+        return e0.elapsed_time(e1) / e2e_steps, rates
+
+    loops = [e2e_loop() for _ in range(3)]
+    e2e_runs = [ms for ms, _ in loops]
+    e2e_ms = float(np.median(e2e_runs))
+    h2d_in_loop = float(np.median([r for _, rates in loops for r in rates]))
+    # the host-to-device rate on its own, after the loops (reported: it
+    # bounds the pipelined loop once it is slower than the kernels)
     c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     c0.record(copy_stream)
     with torch.cuda.stream(copy_stream):
@@ -650,9 +664,11 @@ def run_mine(args, rank, world, local):
                          "frac_of_burst": (bwd_tf if dom == "bwd" else fwd_tf) / burst},
             "e2e": {"value": job_tflops(world, f_fwd + f_bwd, e2e_ms), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                    "loops": 3, "reported": "median loop",
                     "copies": "pinned host -> device on a second stream, double-buffered, overlapping "
                               "the previous step; KL read back every step",
                     "h2d_gbs_alone": sum(t.numel() * t.element_size() for t in host) / (h2d_ms * 1e-3) / 1e9,
+                    "h2d_gbs_in_loop": h2d_in_loop, "loops_ms_per_step": e2e_runs,
                     "numa": numa},
             "gpu_launches": 2 * args.steps,
             "clocks": clk.summary(),

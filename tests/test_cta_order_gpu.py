@@ -6,11 +6,11 @@ the L2 size and the problem (a pure permutation of the units).  Each row's
 forward statistics and each key tile's dK depend only on that head's data,
 and the deterministic backward's dQ sums are exact in any order, so a
 batched call must reproduce, bit for bit, the same call made head by head
-(one head: a single group, head after head).  Eight heads of 16K tokens
-make groups that do not divide the heads (about 7 for the forward and 3
-for the backward with a 129 MB L2), so a unit lost or taken twice at a
-group boundary would show.  Outputs start as NaN where the library does
-not clear them first.
+(one head: a single group, head after head).  Seven heads of 16K tokens:
+a prime count, so any group size from 2 to 6 (the sizes a GB300's L2 gives
+these shapes) leaves a partial last group, and a unit lost or taken twice
+at a group boundary would show.  Outputs start as NaN where the library
+does not clear them first.
 """
 
 import numpy as np
@@ -31,7 +31,7 @@ def _inputs(B, H, N, d, seed):
 
 @pytest.mark.parametrize("causal", [True, False])
 def test_grouped_heads_match_head_by_head(causal):
-    B, H, N, d = 2, 4, 16384, 128
+    B, H, N, d = 1, 7, 16384, 128
     q1, k1, q2, k2 = _inputs(B, H, N, d, 7 + int(causal))
     scale = 1.0 / np.sqrt(d)
     nan = lambda *s: torch.full(s, float("nan"), device="cuda")
@@ -67,9 +67,8 @@ def _per_head_equal(batched, per_head, B, H):
 
 
 def test_grouped_heads_both_sides_deterministic():
-    """The both-sides kernel (d = 64), deterministic: eight heads of 16K make
-    groups of about five."""
-    B, H, N, d = 2, 4, 16384, 64
+    """The both-sides kernel (d = 64), deterministic."""
+    B, H, N, d = 1, 7, 16384, 64
     q1, k1, q2, k2 = _inputs(B, H, N, d, 11)
     scale = 1.0 / np.sqrt(d)
     kl, l1, l2 = skl.streamkl_fwd(q1, k1, q2, k2, scale, True)
@@ -89,8 +88,8 @@ def test_grouped_heads_both_sides_deterministic():
 
 def test_grouped_heads_wide_head_dim():
     """Head dim 256 on both sides (block-ring forward, two-pass backward,
-    no atomics): eight heads of 16K make groups of about three."""
-    B, H, N, d = 1, 8, 16384, 256
+    no atomics)."""
+    B, H, N, d = 1, 7, 16384, 256
     q1, k1, q2, k2 = _inputs(B, H, N, d, 13)
     scale = 1.0 / np.sqrt(d)
     fwd = skl.streamkl_fwd(q1, k1, q2, k2, scale, True)
