@@ -359,8 +359,9 @@ int bwd_impl(const void* q1, const void* k1, const void* q2, const void* k2, int
     return as_status(skl::launch_bwd_wide_pass1(m, t1, t2, a, cs));
   }
   // CTA order: heads interleave in groups within L2's reach (not with the
-  // ordered dK of the deterministic grouped-head mode, whose ticket order
-  // is fixed)
+  // ordered dK of the deterministic grouped-head mode: there the query
+  // heads of a key-head group would reach the same key tile together and
+  // wait on each other's dK, 3-14 % slower than head after head)
   a.head_group = head_group_for(B * H, 2.0 * NQ * (d1 + d2) + 4.0 * NQ * dg);
   if (!deterministic) {
     const size_t dq_bytes = size_t(B) * H * NQ * dg * 4;
