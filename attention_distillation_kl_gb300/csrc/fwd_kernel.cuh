@@ -83,134 +83,17 @@ struct RowStats {
   float m1, m2, l1, l2, acc;
 };
 
-// Folds 64 consecutive key columns (two 32-column chunks) into the running
-// state exactly: the chunks' maxima and sums run as independent chains (for
-// instruction-level parallelism) and the state is rescaled once.  Columns k
-// with k > lim_rel (relative to the first chunk; causal, or past NK) are
-// masked: they neither move the maxima nor add to the sums.  Pairs of
-// columns go through the packed FP32 pipe.  c1, c2: s log2 e of each side;
-// nrho = -s2 / s1 (x1 - rho x2 is one fma, exactly x1 - x2 when the scales
-// are equal).
-template <bool kMask>
-__device__ __forceinline__ void fold_pair(RowStats& st, const uint32_t (&xa1)[32], const uint32_t (&xa2)[32],
-                                          const uint32_t (&xb1)[32], const uint32_t (&xb2)[32], float c1,
-                                          float c2, float nrho, int lim_rel) {
-  float ta1 = st.m1, ta2 = st.m2, tb1 = kNegBig, tb2 = kNegBig;
-#pragma unroll
-  for (int k = 0; k < 32; k += 2) {
-    const bool oa = !kMask || k <= lim_rel, ob = !kMask || k + 1 <= lim_rel;
-    const bool pa = !kMask || k + 32 <= lim_rel, pb = !kMask || k + 33 <= lim_rel;
-    ta1 = max3(ta1, oa ? __uint_as_float(xa1[k]) : kNegBig, ob ? __uint_as_float(xa1[k + 1]) : kNegBig);
-    ta2 = max3(ta2, oa ? __uint_as_float(xa2[k]) : kNegBig, ob ? __uint_as_float(xa2[k + 1]) : kNegBig);
-    tb1 = max3(tb1, pa ? __uint_as_float(xb1[k]) : kNegBig, pb ? __uint_as_float(xb1[k + 1]) : kNegBig);
-    tb2 = max3(tb2, pa ? __uint_as_float(xb2[k]) : kNegBig, pb ? __uint_as_float(xb2[k + 1]) : kNegBig);
-  }
-  const float t1 = fmaxf(ta1, tb1), t2 = fmaxf(ta2, tb2);
-  const float a1 = ex2((st.m1 - t1) * c1);
-  const float a2 = ex2((st.m2 - t2) * c2);
-  st.m1 = t1;
-  st.m2 = t2;
-  const uint64_t C1 = f2(c1, c1), C2 = f2(c2, c2), NR = f2(nrho, nrho);
-  const uint64_t NB1 = f2(-t1 * c1, -t1 * c1), NB2 = f2(-t2 * c2, -t2 * c2);
-  uint64_t L1a = f2(0.f, 0.f), L2a = L1a, ACCa = L1a, L1b = L1a, L2b = L1a, ACCb = L1a;
-#pragma unroll
-  for (int k = 0; k < 32; k += 2) {
-    const uint64_t XA1 = f2(__uint_as_float(xa1[k]), __uint_as_float(xa1[k + 1]));
-    const uint64_t XA2 = f2(__uint_as_float(xa2[k]), __uint_as_float(xa2[k + 1]));
-    const uint64_t XB1 = f2(__uint_as_float(xb1[k]), __uint_as_float(xb1[k + 1]));
-    const uint64_t XB2 = f2(__uint_as_float(xb2[k]), __uint_as_float(xb2[k + 1]));
-    float e1a, e1b, e2a, e2b, g1a, g1b, g2a, g2b;
-    f2_split(f2_fma(XA1, C1, NB1), e1a, e1b);
-    f2_split(f2_fma(XA2, C2, NB2), e2a, e2b);
-    f2_split(f2_fma(XB1, C1, NB1), g1a, g1b);
-    f2_split(f2_fma(XB2, C2, NB2), g2a, g2b);
-    float p1a = ex2(e1a), p1b = ex2(e1b), p2a = ex2(e2a), p2b = ex2(e2b);
-    float q1a = ex2(g1a), q1b = ex2(g1b), q2a = ex2(g2a), q2b = ex2(g2b);
-    if (kMask) {
-      if (k > lim_rel) { p1a = 0.f; p2a = 0.f; }
-      if (k + 1 > lim_rel) { p1b = 0.f; p2b = 0.f; }
-      if (k + 32 > lim_rel) { q1a = 0.f; q2a = 0.f; }
-      if (k + 33 > lim_rel) { q1b = 0.f; q2b = 0.f; }
-    }
-    const uint64_t P1 = f2(p1a, p1b), Q1 = f2(q1a, q1b);
-    L1a = f2_add(L1a, P1);
-    L2a = f2_add(L2a, f2(p2a, p2b));
-    ACCa = f2_fma(P1, f2_fma(XA2, NR, XA1), ACCa);
-    L1b = f2_add(L1b, Q1);
-    L2b = f2_add(L2b, f2(q2a, q2b));
-    ACCb = f2_fma(Q1, f2_fma(XB2, NR, XB1), ACCb);
-  }
-  const uint64_t L1 = f2_add(L1a, L1b), L2 = f2_add(L2a, L2b), ACC = f2_add(ACCa, ACCb);
-  float l1a, l1b, l2a, l2b, aca, acb;
-  f2_split(L1, l1a, l1b);
-  f2_split(L2, l2a, l2b);
-  f2_split(ACC, aca, acb);
-  st.l1 = fmaf(st.l1, a1, l1a + l1b);
-  st.acc = fmaf(st.acc, a1, aca + acb);
-  st.l2 = fmaf(st.l2, a2, l2a + l2b);
-}
-
-// Fast path of fold_pair: the 64 columns exponentiated against the running
-// maxima as they stand, with no maximum pass and no rescale.  The online
-// recurrence holds for any reference at or above the values seen so far, and
-// fp32 keeps its relative precision at any scale, so a reference that is
-// not the exact maximum changes nothing as long as no term overflows.
-// Returns false -- the state untouched -- when a partial sum reaches 2^64
-// (a logit above the reference by more than 64 / c, the first tile of a row
-// whose reference is still kNegBig, or a non-finite input): the caller then
-// folds the tile exactly with fold_pair.
-template <bool kMask>
-__device__ __forceinline__ bool fold_pair_fast(RowStats& st, const uint32_t (&xa1)[32], const uint32_t (&xa2)[32],
-                                               const uint32_t (&xb1)[32], const uint32_t (&xb2)[32], float c1,
-                                               float c2, float nrho, int lim_rel) {
-  const uint64_t C1 = f2(c1, c1), C2 = f2(c2, c2), NR = f2(nrho, nrho);
-  const float nb1 = -st.m1 * c1, nb2 = -st.m2 * c2;
-  const uint64_t NB1 = f2(nb1, nb1), NB2 = f2(nb2, nb2);
-  uint64_t L1a = f2(0.f, 0.f), L2a = L1a, ACCa = L1a, L1b = L1a, L2b = L1a, ACCb = L1a;
-#pragma unroll
-  for (int k = 0; k < 32; k += 2) {
-    const uint64_t XA1 = f2(__uint_as_float(xa1[k]), __uint_as_float(xa1[k + 1]));
-    const uint64_t XA2 = f2(__uint_as_float(xa2[k]), __uint_as_float(xa2[k + 1]));
-    const uint64_t XB1 = f2(__uint_as_float(xb1[k]), __uint_as_float(xb1[k + 1]));
-    const uint64_t XB2 = f2(__uint_as_float(xb2[k]), __uint_as_float(xb2[k + 1]));
-    float e1a, e1b, e2a, e2b, g1a, g1b, g2a, g2b;
-    f2_split(f2_fma(XA1, C1, NB1), e1a, e1b);
-    f2_split(f2_fma(XA2, C2, NB2), e2a, e2b);
-    f2_split(f2_fma(XB1, C1, NB1), g1a, g1b);
-    f2_split(f2_fma(XB2, C2, NB2), g2a, g2b);
-    float p1a = ex2(e1a), p1b = ex2(e1b), p2a = ex2(e2a), p2b = ex2(e2b);
-    float q1a = ex2(g1a), q1b = ex2(g1b), q2a = ex2(g2a), q2b = ex2(g2b);
-    if (kMask) {
-      if (k > lim_rel) { p1a = 0.f; p2a = 0.f; }
-      if (k + 1 > lim_rel) { p1b = 0.f; p2b = 0.f; }
-      if (k + 32 > lim_rel) { q1a = 0.f; q2a = 0.f; }
-      if (k + 33 > lim_rel) { q1b = 0.f; q2b = 0.f; }
-    }
-    const uint64_t P1 = f2(p1a, p1b), Q1 = f2(q1a, q1b);
-    L1a = f2_add(L1a, P1);
-    L2a = f2_add(L2a, f2(p2a, p2b));
-    ACCa = f2_fma(P1, f2_fma(XA2, NR, XA1), ACCa);
-    L1b = f2_add(L1b, Q1);
-    L2b = f2_add(L2b, f2(q2a, q2b));
-    ACCb = f2_fma(Q1, f2_fma(XB2, NR, XB1), ACCb);
-  }
-  const uint64_t L1 = f2_add(L1a, L1b), L2 = f2_add(L2a, L2b), ACC = f2_add(ACCa, ACCb);
-  float l1a, l1b, l2a, l2b, aca, acb;
-  f2_split(L1, l1a, l1b);
-  f2_split(L2, l2a, l2b);
-  f2_split(ACC, aca, acb);
-  const float l1 = l1a + l1b, l2 = l2a + l2b;
-  if (!(l1 < 18446744073709551616.f && l2 < 18446744073709551616.f)) return false;  // 2^64
-  st.l1 += l1;
-  st.acc += aca + acb;
-  st.l2 += l2;
-  return true;
-}
-
 // The sums of one 32-column chunk against the reference nb = -c m of each
 // side: l1 = sum 2^(c1 x1 + nb1), l2 = sum 2^(c2 x2 + nb2) and
-// acc = sum 2^(c1 x1 + nb1) (x1 - rho x2), columns past lim_rel masked.  Two
-// chains (pairs k, k + 1 and k + 2, k + 3) for instruction-level parallelism.
+// acc = sum 2^(c1 x1 + nb1) (x1 - rho x2), columns past lim_rel masked.
+// c1, c2: s log2 e of each side; NR = -s2 / s1 in both lanes (x1 - rho x2 is
+// one fma, exactly x1 - x2 when the scales are equal).  Pairs of columns go
+// through the packed FP32 pipe, in two chains (pairs k, k + 1 and k + 2,
+// k + 3) for instruction-level parallelism.  Taken against the running
+// maxima as they stand (the fast path, no maximum pass and no rescale),
+// the sums are exact as long as no term overflows: the online recurrence
+// holds for any reference at or above the values seen so far, and fp32
+// keeps its relative precision at any scale.
 template <bool kMask>
 __device__ __forceinline__ void chunk_sums(const uint32_t (&x1)[32], const uint32_t (&x2)[32], uint64_t C1,
                                            uint64_t C2, uint64_t NR, uint64_t NB1, uint64_t NB2, int lim_rel,
@@ -280,6 +163,63 @@ __device__ __forceinline__ void fold_one(RowStats& st, const uint32_t (&x1)[32],
   st.l1 = fmaf(st.l1, a1, l1);
   st.acc = fmaf(st.acc, a1, acc);
   st.l2 = fmaf(st.l2, a2, l2);
+}
+
+// Folds 64 consecutive key columns (two 32-column chunks) into the running
+// state exactly: the maxima move to the columns', the state is rescaled
+// once, and the chunks' sums are taken against the new maxima.  Columns k
+// with k > lim_rel (relative to the first chunk; causal, or past NK) are
+// masked: they neither move the maxima nor add to the sums.
+template <bool kMask>
+__device__ __forceinline__ void fold_pair(RowStats& st, const uint32_t (&xa1)[32], const uint32_t (&xa2)[32],
+                                          const uint32_t (&xb1)[32], const uint32_t (&xb2)[32], uint64_t C1,
+                                          uint64_t C2, uint64_t NR, float c1, float c2, int lim_rel) {
+  float ta1 = st.m1, ta2 = st.m2, tb1 = kNegBig, tb2 = kNegBig;
+#pragma unroll
+  for (int k = 0; k < 32; k += 2) {
+    const bool oa = !kMask || k <= lim_rel, ob = !kMask || k + 1 <= lim_rel;
+    const bool pa = !kMask || k + 32 <= lim_rel, pb = !kMask || k + 33 <= lim_rel;
+    ta1 = max3(ta1, oa ? __uint_as_float(xa1[k]) : kNegBig, ob ? __uint_as_float(xa1[k + 1]) : kNegBig);
+    ta2 = max3(ta2, oa ? __uint_as_float(xa2[k]) : kNegBig, ob ? __uint_as_float(xa2[k + 1]) : kNegBig);
+    tb1 = max3(tb1, pa ? __uint_as_float(xb1[k]) : kNegBig, pb ? __uint_as_float(xb1[k + 1]) : kNegBig);
+    tb2 = max3(tb2, pa ? __uint_as_float(xb2[k]) : kNegBig, pb ? __uint_as_float(xb2[k + 1]) : kNegBig);
+  }
+  const float t1 = fmaxf(ta1, tb1), t2 = fmaxf(ta2, tb2);
+  const float a1 = ex2((st.m1 - t1) * c1);
+  const float a2 = ex2((st.m2 - t2) * c2);
+  st.m1 = t1;
+  st.m2 = t2;
+  const float nb1 = -t1 * c1, nb2 = -t2 * c2;
+  const uint64_t NB1 = f2(nb1, nb1), NB2 = f2(nb2, nb2);
+  float l1a, l2a, aca, l1b, l2b, acb;
+  chunk_sums<kMask>(xa1, xa2, C1, C2, NR, NB1, NB2, lim_rel, l1a, l2a, aca);
+  chunk_sums<kMask>(xb1, xb2, C1, C2, NR, NB1, NB2, lim_rel - 32, l1b, l2b, acb);
+  st.l1 = fmaf(st.l1, a1, l1a + l1b);
+  st.acc = fmaf(st.acc, a1, aca + acb);
+  st.l2 = fmaf(st.l2, a2, l2a + l2b);
+}
+
+// Fast path of fold_pair: the 64 columns exponentiated against the running
+// maxima as they stand, with no maximum pass and no rescale (see chunk_sums
+// for why that is exact).  Returns false -- the state untouched -- when a
+// partial sum reaches 2^64 (a logit above the reference by more than 64 / c,
+// the first tile of a row whose reference is still kNegBig, or a non-finite
+// input): the caller then folds the tile exactly with fold_pair.
+template <bool kMask>
+__device__ __forceinline__ bool fold_pair_fast(RowStats& st, const uint32_t (&xa1)[32], const uint32_t (&xa2)[32],
+                                               const uint32_t (&xb1)[32], const uint32_t (&xb2)[32], uint64_t C1,
+                                               uint64_t C2, uint64_t NR, float c1, float c2, int lim_rel) {
+  const float nb1 = -st.m1 * c1, nb2 = -st.m2 * c2;
+  const uint64_t NB1 = f2(nb1, nb1), NB2 = f2(nb2, nb2);
+  float l1a, l2a, aca, l1b, l2b, acb;
+  chunk_sums<kMask>(xa1, xa2, C1, C2, NR, NB1, NB2, lim_rel, l1a, l2a, aca);
+  chunk_sums<kMask>(xb1, xb2, C1, C2, NR, NB1, NB2, lim_rel - 32, l1b, l2b, acb);
+  const float l1 = l1a + l1b, l2 = l2a + l2b;
+  if (!(l1 < 18446744073709551616.f && l2 < 18446744073709551616.f)) return false;  // 2^64
+  st.l1 += l1;
+  st.acc += aca + acb;
+  st.l2 += l2;
+  return true;
 }
 
 template <int D1, int D2>
@@ -539,16 +479,17 @@ __global__ void __launch_bounds__(FwdLayout<D1, D2>::kThreads, 1)
         tmem_ld4x32(t, t + 128, t + 32, t + 160, xa1, xa2, xb1, xb2);
         const int lr = need_mask ? lim - (k0 + col) : 0;
         // no reference yet on the first tile: every row folds it exactly
-        const bool fast = j > 0 && (need_mask ? fold_pair_fast<true>(st, xa1, xa2, xb1, xb2, c1, c2, nrho, lr)
-                                              : fold_pair_fast<false>(st, xa1, xa2, xb1, xb2, c1, c2, nrho, 0));
+        const bool fast =
+            j > 0 && (need_mask ? fold_pair_fast<true>(st, xa1, xa2, xb1, xb2, C1, C2, NR, c1, c2, lr)
+                                : fold_pair_fast<false>(st, xa1, xa2, xb1, xb2, C1, C2, NR, c1, c2, 0));
         if (j == 0) {
-          if (need_mask) fold_pair<true>(st, xa1, xa2, xb1, xb2, c1, c2, nrho, lr);
-          else fold_pair<false>(st, xa1, xa2, xb1, xb2, c1, c2, nrho, 0);
+          if (need_mask) fold_pair<true>(st, xa1, xa2, xb1, xb2, C1, C2, NR, c1, c2, lr);
+          else fold_pair<false>(st, xa1, xa2, xb1, xb2, C1, C2, NR, c1, c2, 0);
         } else if (__any_sync(0xffffffffu, !fast)) {  // the TMEM loads are warp-wide
           tmem_ld4x32(t, t + 128, t + 32, t + 160, xa1, xa2, xb1, xb2);
           if (!fast) {
-            if (need_mask) fold_pair<true>(st, xa1, xa2, xb1, xb2, c1, c2, nrho, lr);
-            else fold_pair<false>(st, xa1, xa2, xb1, xb2, c1, c2, nrho, 0);
+            if (need_mask) fold_pair<true>(st, xa1, xa2, xb1, xb2, C1, C2, NR, c1, c2, lr);
+            else fold_pair<false>(st, xa1, xa2, xb1, xb2, C1, C2, NR, c1, c2, 0);
           }
         }
         tc_fence_before();
