@@ -41,7 +41,7 @@ UNIT = "TFLOP/s"
 TRAFFIC = {
     # dram__bytes_read.sum + dram__bytes_write.sum of one full-size launch
     "bwd_fused": {"bytes": 3294571264 + 2136466432, "src_sha": "cdaacbf38a1b7730"},
-    "fwd": {"bytes": 2158700544 + 28129280, "src_sha": "0269f1cb4c4f4883"},
+    "fwd": {"bytes": 2160437760 + 28472320, "src_sha": "f0ca1b124adb173a"},
 }
 
 
